@@ -1,0 +1,297 @@
+// index_kernels.cu -- the block-map step: tile mean pooling, coarse scores
+// with per-row top-k, and the two block indices (Q-owned and KV-owned).
+//
+// Pages: FastVideo test_vsa256_backward.py (_zero_pad_tail: valid tokens
+// first in each tile; video_sparse_attn's topk), FastVideo
+// block_sparse_attn_cute_fwd.py (_map_to_index; _build_sparse_tensors: only
+// vbs > 0 tiles enter the index, and the backward index is KV-owned).
+//
+// Bit-exactness: pooling adds tokens in ascending order with __fadd_rn and
+// divides with __fdiv_rn; scores are an __fmaf_rn chain over ascending d.
+// These intrinsics are never contracted or reordered by the compiler, so
+// the selection is reproducible and equals the fixed-order definition.
+#include <climits>
+
+#include "vsa_internal.h"
+
+namespace vsa {
+
+// ------------------------------------------------------------------ pool
+// One warp per (b, h, tile); lane l owns dims 4l..4l+3 and reads 8 bytes
+// of each token row, so a warp reads whole 256-byte rows (coalesced).
+template <typename T>
+__global__ void __launch_bounds__(256) k_pool(Prob p, int q_side, const T *__restrict__ x,
+                                              float *__restrict__ out) {
+    const int H = q_side ? p.Hq : p.Hkv, nT = q_side ? p.nQ : p.nKV;
+    const int Tt = q_side ? p.tile_q : p.tile_kv;
+    const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= (long long)p.B * H * nT) return;
+    const int t = (int)(w % nT), h = (int)((w / nT) % H), b = (int)(w / ((long long)nT * H));
+    const int lane = threadIdx.x & 31;
+    const int var = q_side ? q_valid(p, b, t) : kv_valid(p, b, t);
+    const long long rs = (p.layout == L_BHSD) ? p.D : (long long)H * p.D;  // token stride
+    const T *base = x + tok_off(p, q_side, b, t * Tt, h) + lane * 4;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    int r = 0;
+    for (; r + 8 <= var; r += 8) {
+        uint2 buf[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) buf[u] = __ldg(reinterpret_cast<const uint2 *>(base + (long long)(r + u) * rs));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float2 a = unpack2<T>(buf[u].x), c = unpack2<T>(buf[u].y);
+            s[0] = __fadd_rn(s[0], a.x);
+            s[1] = __fadd_rn(s[1], a.y);
+            s[2] = __fadd_rn(s[2], c.x);
+            s[3] = __fadd_rn(s[3], c.y);
+        }
+    }
+    for (; r < var; ++r) {
+        uint2 v = __ldg(reinterpret_cast<const uint2 *>(base + (long long)r * rs));
+        float2 a = unpack2<T>(v.x), c = unpack2<T>(v.y);
+        s[0] = __fadd_rn(s[0], a.x);
+        s[1] = __fadd_rn(s[1], a.y);
+        s[2] = __fadd_rn(s[2], c.x);
+        s[3] = __fadd_rn(s[3], c.y);
+    }
+    float4 o;
+    const float fv = (float)var;
+    o.x = var > 0 ? __fdiv_rn(s[0], fv) : 0.f;
+    o.y = var > 0 ? __fdiv_rn(s[1], fv) : 0.f;
+    o.z = var > 0 ? __fdiv_rn(s[2], fv) : 0.f;
+    o.w = var > 0 ? __fdiv_rn(s[3], fv) : 0.f;
+    *reinterpret_cast<float4 *>(out + w * p.D + lane * 4) = o;
+}
+
+cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s) {
+    const int H = q_side ? p.Hq : p.Hkv, nT = q_side ? p.nQ : p.nKV;
+    const long long warps = (long long)p.B * H * nT;
+    const int blocks = (int)((warps + 7) / 8);
+    if (blocks == 0) return cudaSuccess;
+    prof_begin("pool", s);
+    if (p.dtype == T_BF16)
+        k_pool<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, q_side, (const __nv_bfloat16 *)x, out);
+    else
+        k_pool<__half><<<blocks, 256, 0, s>>>(p, q_side, (const __half *)x, out);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- select
+// Block = 8 warps = 8 query tiles of one (b, h). Key-tile means are staged
+// through shared memory in chunks of 128 tiles (rows padded to 129 floats so
+// lanes reading different tiles at the same d hit different banks). Lane l
+// of warp w computes the scores of tiles l, l+32, ... of query tile
+// i0 + w; the warp then takes the top-k by repeated warp-wide argmax under
+// (score desc, index asc).
+constexpr int kSelRows = 8;
+constexpr int kSelChunk = 128;
+
+__device__ __forceinline__ bool sel_better(float v, int j, float bv, int bj) {
+    return j != INT_MAX && (bj == INT_MAX || v > bv || (v == bv && j < bj));
+}
+
+__global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict__ pq,
+                                                const float *__restrict__ pk, int topk, uint8_t *map,
+                                                int *q_idx, int *q_cnt, int cap) {
+    extern __shared__ float sm[];
+    float *spk = sm;                                  // [kSelChunk][129]
+    float *spq = spk + kSelChunk * 129;               // [kSelRows][128]
+    float *ssc = spq + kSelRows * 128;                // [kSelRows][nKV]
+    uint8_t *ssel = reinterpret_cast<uint8_t *>(ssc + kSelRows * p.nKV);  // [kSelRows][nKV]
+    const int b = blockIdx.z, h = blockIdx.y, hk = h / (p.Hq / p.Hkv);
+    const int i0 = blockIdx.x * kSelRows, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = i0 + w;
+    const int D = p.D;  // 128
+    for (int e = threadIdx.x; e < kSelRows * D; e += blockDim.x) {
+        int r = e / D, ii = i0 + r;
+        spq[e] = ii < p.nQ ? pq[(((long long)b * p.Hq + h) * p.nQ + ii) * D + (e % D)] : 0.f;
+    }
+    const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * D;
+    for (int j0 = 0; j0 < p.nKV; j0 += kSelChunk) {
+        const int nj = min(kSelChunk, p.nKV - j0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nj * D; e += blockDim.x)
+            spk[(e / D) * 129 + (e % D)] = pkh[(long long)j0 * D + e];
+        __syncthreads();
+        if (i < p.nQ) {
+            for (int jj = lane; jj < nj; jj += 32) {
+                float acc = 0.f;
+                const float *a = spq + w * D, *c = spk + jj * 129;
+#pragma unroll 16
+                for (int e = 0; e < D; ++e) acc = __fmaf_rn(a[e], c[e], acc);
+                ssc[w * p.nKV + j0 + jj] = kv_valid(p, b, j0 + jj) > 0 ? acc : -INFINITY;
+            }
+        }
+    }
+    __syncthreads();
+    if (i >= p.nQ) return;
+    const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
+    float *sc = ssc + w * p.nKV;
+    uint8_t *sel = ssel + w * p.nKV;
+    for (int j = lane; j < p.nKV; j += 32) sel[j] = 0;
+    __syncwarp();
+    const int k = q_rows(p, b, i) > 0 ? min(topk, p.nKV) : 0;
+    for (int n = 0; n < k; ++n) {
+        float bv = -INFINITY;
+        int bj = INT_MAX;
+        for (int j = lane; j < p.nKV; j += 32)
+            if (!sel[j] && sel_better(sc[j], j, bv, bj)) {
+                bv = sc[j];
+                bj = j;
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+            if (sel_better(ov, oj, bv, bj)) {
+                bv = ov;
+                bj = oj;
+            }
+        }
+        if (lane == 0) sel[bj] = 1;
+        __syncwarp();
+    }
+    int cnt = 0;
+    for (int j0 = 0; j0 < p.nKV; j0 += 32) {
+        const int j = j0 + lane;
+        const bool on = j < p.nKV && sel[j];
+        if (j < p.nKV) map[row * p.nKV + j] = on ? 1 : 0;
+        const bool f = on && kv_valid(p, b, j) > 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (f) q_idx[row * cap + cnt + __popc(bal & ((1u << lane) - 1u))] = j;
+        cnt += __popc(bal);
+    }
+    for (int n = cnt + lane; n < cap; n += 32) q_idx[row * cap + n] = -1;
+    if (lane == 0) q_cnt[row] = cnt;
+}
+
+cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map, int *q_idx,
+                          int *q_cnt, int cap, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (kSelChunk * 129 + kSelRows * 128 + (size_t)kSelRows * p.nKV) +
+                        (size_t)kSelRows * p.nKV;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attr = true;
+    }
+    dim3 grid((p.nQ + kSelRows - 1) / kSelRows, p.Hq, p.B);
+    prof_begin("select_topk", s);
+    k_select<<<grid, 256, smem, s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ mask index
+// One warp per (b, h, query tile): ballot-compact the marked tiles that
+// hold valid tokens, ascending.
+__global__ void __launch_bounds__(256) k_mask_index(Prob p, const uint8_t *__restrict__ map, int *q_idx,
+                                                    int *q_cnt, int cap) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= (long long)p.B * p.Hq * p.nQ) return;
+    const int lane = threadIdx.x & 31;
+    const int i = (int)(row % p.nQ), b = (int)(row / ((long long)p.nQ * p.Hq));
+    const bool exists = q_rows(p, b, i) > 0;
+    int cnt = 0;
+    for (int j0 = 0; j0 < p.nKV; j0 += 32) {
+        const int j = j0 + lane;
+        const bool f = exists && j < p.nKV && map[row * p.nKV + j] != 0 && kv_valid(p, b, j) > 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (f) q_idx[row * cap + cnt + __popc(bal & ((1u << lane) - 1u))] = j;
+        cnt += __popc(bal);
+    }
+    for (int n = cnt + lane; n < cap; n += 32) q_idx[row * cap + n] = -1;
+    if (lane == 0) q_cnt[row] = cnt;
+}
+
+cudaError_t launch_mask_index(const Prob &p, const uint8_t *map, int *q_idx, int *q_cnt, int cap,
+                              cudaStream_t s) {
+    const long long rows = (long long)p.B * p.Hq * p.nQ;
+    if (rows == 0) return cudaSuccess;
+    prof_begin("mask_index", s);
+    k_mask_index<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, map, q_idx, q_cnt, cap);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- transpose
+// One block per (b, h). Thread-per-KV-tile column scans of the map count
+// the selecting query tiles, a block-wide exclusive scan gives kv_ptr, and
+// a second column scan writes the lists in ascending query-tile order. An
+// entry counts iff the map marks it, the KV tile holds valid tokens and the
+// query tile exists -- the same filter that built the Q-owned index.
+__global__ void __launch_bounds__(1024) k_transpose(Prob p, const uint8_t *__restrict__ map, int *kv_ptr,
+                                                    int *kv_qidx, int cap) {
+    extern __shared__ int cnt[];  // [nKV + 1]
+    __shared__ int warp_tot[32];
+    const int b = blockIdx.y, h = blockIdx.x;
+    const long long bh = (long long)b * p.Hq + h;
+    const uint8_t *m = map + bh * p.nQ * p.nKV;
+    for (int j = threadIdx.x; j < p.nKV; j += blockDim.x) {
+        int c = 0;
+        if (kv_valid(p, b, j) > 0)
+            for (int i = 0; i < p.nQ; ++i) c += (m[(long long)i * p.nKV + j] != 0 && q_rows(p, b, i) > 0);
+        cnt[j] = c;
+    }
+    __syncthreads();
+    // exclusive scan of cnt[0..nKV) into cnt[0..nKV], thread t owns a segment
+    const int per = (p.nKV + blockDim.x - 1) / blockDim.x;
+    const int lo = min(p.nKV, (int)threadIdx.x * per), hi = min(p.nKV, lo + per);
+    int local = 0;
+    for (int j = lo; j < hi; ++j) local += cnt[j];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int v = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        warp_tot[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = (incl - local) + (wid > 0 ? warp_tot[wid - 1] : 0);
+    int *ptr = kv_ptr + bh * (p.nKV + 1);
+    for (int j = lo; j < hi; ++j) {
+        const int c = cnt[j];
+        ptr[j] = run;
+        run += c;
+    }
+    const int total = warp_tot[(blockDim.x >> 5) - 1];
+    if (threadIdx.x == 0) ptr[p.nKV] = total;
+    __syncthreads();
+    int *lst = kv_qidx + bh * (long long)p.nQ * cap;
+    for (int j = threadIdx.x; j < p.nKV; j += blockDim.x) {
+        int pos = ptr[j];
+        if (kv_valid(p, b, j) > 0)
+            for (int i = 0; i < p.nQ; ++i)
+                if (m[(long long)i * p.nKV + j] != 0 && q_rows(p, b, i) > 0) lst[pos++] = i;
+    }
+    for (long long n = total + threadIdx.x; n < (long long)p.nQ * cap; n += blockDim.x) lst[n] = -1;
+}
+
+cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int *kv_qidx, int cap,
+                             cudaStream_t s) {
+    if (p.B == 0 || p.Hq == 0) return cudaSuccess;
+    dim3 grid(p.Hq, p.B);
+    const size_t smem = sizeof(int) * (p.nKV + 1);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_transpose, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+        attr = true;
+    }
+    prof_begin("transpose_index", s);
+    k_transpose<<<grid, 1024, smem, s>>>(p, map, kv_ptr, kv_qidx, cap);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace vsa

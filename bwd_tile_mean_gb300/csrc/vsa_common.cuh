@@ -1,0 +1,100 @@
+// vsa_common.cuh -- problem description, indexing and small device helpers
+// shared by the library's kernels. Internal to libvsa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vsa {
+
+enum { L_BHSD = 0, L_BSHD = 1, L_TND = 2 };
+enum { T_BF16 = 0, T_FP16 = 1 };
+
+// Problem description passed to kernels by value.
+struct Prob {
+    int layout, dtype;
+    int B, Hq, Hkv, D;
+    int Sq, Skv;          // padded per-batch tokens, or totals in TND
+    int tile_q, tile_kv;
+    int nQ, nKV;
+    const int *cu_q, *cu_kv;     // TND offsets (device)
+    const int *q_var, *kv_var;   // padded-layout tile fills (device)
+    float scale;
+};
+
+// Valid tokens of KV tile j of batch entry b (padded layouts: kv_var[j]
+// clamped to [0, tile]; TND: the part of the tile inside the sequence).
+__device__ __forceinline__ int kv_valid(const Prob &p, int b, int j) {
+    if (p.layout == L_TND) {
+        int v = (p.cu_kv[b + 1] - p.cu_kv[b]) - j * p.tile_kv;
+        return v < 0 ? 0 : (v > p.tile_kv ? p.tile_kv : v);
+    }
+    const int v = p.kv_var[j];
+    return v < 0 ? 0 : (v > p.tile_kv ? p.tile_kv : v);
+}
+__device__ __forceinline__ int q_valid(const Prob &p, int b, int i) {
+    if (p.layout == L_TND) {
+        int v = (p.cu_q[b + 1] - p.cu_q[b]) - i * p.tile_q;
+        return v < 0 ? 0 : (v > p.tile_q ? p.tile_q : v);
+    }
+    const int v = p.q_var[i];
+    return v < 0 ? 0 : (v > p.tile_q ? p.tile_q : v);
+}
+// Query rows of tile i that exist (all slots in the padded layouts).
+__device__ __forceinline__ int q_rows(const Prob &p, int b, int i) {
+    return p.layout == L_TND ? q_valid(p, b, i) : p.tile_q;
+}
+// Element offset of (batch b, token s within b, head h, d = 0).
+__device__ __forceinline__ long long tok_off(const Prob &p, bool q_side, int b, int s, int h) {
+    const int H = q_side ? p.Hq : p.Hkv;
+    if (p.layout == L_BHSD) {
+        const int S = q_side ? p.Sq : p.Skv;
+        return (((long long)b * H + h) * S + s) * p.D;
+    }
+    if (p.layout == L_BSHD) {
+        const int S = q_side ? p.Sq : p.Skv;
+        return (((long long)b * S + s) * H + h) * p.D;
+    }
+    const int *cu = q_side ? p.cu_q : p.cu_kv;
+    return ((long long)(cu[b] + s) * H + h) * p.D;
+}
+// Offset of the LSE / Dvec entry of (b, h, s): [B, Hq, Sq] or [Hq, T].
+__device__ __forceinline__ long long lse_off(const Prob &p, int b, int h, int s) {
+    if (p.layout == L_TND) return (long long)h * p.Sq + p.cu_q[b] + s;
+    return ((long long)b * p.Hq + h) * p.Sq + s;
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <> __device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+
+// Two floats packed to one 32-bit word of 16-bit values (lo = a).
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w));
+}
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<__half2 *>(&w));
+}
+
+// Device status word (first bytes of the caller's workspace).
+__device__ __forceinline__ void set_error(unsigned *err, unsigned code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+}  // namespace vsa

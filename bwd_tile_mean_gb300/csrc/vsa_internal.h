@@ -1,0 +1,74 @@
+// vsa_internal.h -- host-side declarations shared by the library's
+// translation units (kernel launchers and the instrumentation hooks).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vsa_common.cuh"
+
+namespace vsa {
+
+// Instrumentation: every launcher brackets its kernel with these.
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+// Tile pooling (fp32 means of the first var tokens), [B, H, nT, D].
+cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s);
+// Coarse scores + per-row top-k -> block map and Q-owned index.
+cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map,
+                          int *q_idx, int *q_cnt, int cap, cudaStream_t s);
+// Caller-given block map -> Q-owned index.
+cudaError_t launch_mask_index(const Prob &p, const uint8_t *map, int *q_idx, int *q_cnt, int cap,
+                              cudaStream_t s);
+// Block map -> KV-owned index.
+cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int *kv_qidx, int cap,
+                             cudaStream_t s);
+
+// Largest nKV the selection kernel handles (its shared-memory score rows).
+constexpr int kMaxSelectKV = 3072;
+// Largest number of 128-key chunks one query tile may visit.
+constexpr int kMaxChunks = 1024;
+
+// Forward attention (tcgen05). out / o_sparse / gate / c as in vsa_fwd.
+struct FwdArgs {
+    const void *q, *k, *v;
+    const int *q_idx, *q_cnt;
+    int cap;
+    void *out, *o_sparse;
+    float *lse;
+    const void *gate;   // NULL: no compression
+    const float *c;     // [B, Hq, nQ, D] compression output (gate != NULL)
+    unsigned *err;
+};
+cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s);
+
+// Compression branch, forward: c_i = sum_j softmax_j(scale pq.pk_j) pv_j.
+cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk, const float *pv,
+                                float *c, cudaStream_t s);
+
+// Backward pieces.
+cudaError_t launch_dvec(const Prob &p, const void *dO, const void *o, float *dvec, cudaStream_t s);
+struct BwdArgs {
+    const void *dO, *q, *k, *v;
+    const float *lse, *dvec;
+    const int *q_idx, *q_cnt;
+    int cap;
+    const int *kv_ptr, *kv_qidx;
+    void *dq, *dk, *dv;
+    const float *dpq, *dpk, *dpv;   // compression gradients (NULL without a gate)
+    unsigned *err;
+};
+cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s);
+// Compression branch, backward: dc, then A / ds per row, then the
+// per-KV-tile column sums.
+cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate, const float *pq,
+                                const float *pk, const float *pv, float *dc, float *A, float *ds,
+                                float *dpq, float *dpk, float *dpv, cudaStream_t s);
+
+// Tensor-map encoding (driver entry point fetched through the runtime).
+bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *base, int heads);
+
+}  // namespace vsa

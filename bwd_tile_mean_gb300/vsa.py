@@ -1,0 +1,239 @@
+"""Python binding of libvsa.so (include/vsa.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels. PyTorch provides device memory and streams. The
+functions named like the C entry points (``vsa_build_block_map``,
+``vsa_mask_to_index``, ``vsa_fwd``, ``vsa_bwd``, ...) take torch tensors
+and pass their device pointers; ``Plan`` wraps a problem's descriptor,
+workspace and index buffers for convenient use. There is no fallback: a
+missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+LAYOUTS = {"bhsd": 0, "bshd": 1, "tnd": 2}
+DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+
+STATUS = {0: "VSA_OK", 1: "VSA_ERR_NULL", 2: "VSA_ERR_SHAPE", 3: "VSA_ERR_DTYPE", 4: "VSA_ERR_LAYOUT",
+          5: "VSA_ERR_UNSUPPORTED", 6: "VSA_ERR_MISSING_SEQLENS", 7: "VSA_ERR_WORKSPACE",
+          8: "VSA_ERR_CUDA", 9: "VSA_ERR_DEVICE"}
+
+EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_mask_to_index", "vsa_fwd", "vsa_bwd",
+           "vsa_status_string", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
+           "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count")
+
+
+class VsaError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({_lib.vsa_status_string(code).decode()})")
+
+
+class VsaDesc(C.Structure):
+    _fields_ = [("layout", C.c_int32), ("dtype", C.c_int32), ("B", C.c_int32), ("Hq", C.c_int32),
+                ("Hkv", C.c_int32), ("D", C.c_int32), ("Sq", C.c_int32), ("Skv", C.c_int32),
+                ("tile_q", C.c_int32), ("tile_kv", C.c_int32), ("nQ", C.c_int32), ("nKV", C.c_int32),
+                ("cu_seqlens_q", C.c_void_p), ("cu_seqlens_kv", C.c_void_p), ("scale", C.c_float)]
+
+
+_lib = None
+P = C.c_void_p
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libvsa.so (built in-tree by __graft_entry__.build()); raise if absent."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libvsa.so is not built ({path}); run __graft_entry__.build()")
+        L = C.CDLL(path)
+        L.vsa_workspace_size.restype = C.c_size_t
+        L.vsa_workspace_size.argtypes = [C.POINTER(VsaDesc), C.c_int]
+        L.vsa_build_block_map.restype = C.c_int
+        L.vsa_build_block_map.argtypes = [C.POINTER(VsaDesc), P, P, P, P, C.c_int, C.c_int, P, P, P, C.c_int,
+                                          P, P, P, C.c_size_t, P]
+        L.vsa_mask_to_index.restype = C.c_int
+        L.vsa_mask_to_index.argtypes = [C.POINTER(VsaDesc), P, P, P, C.c_int, P, P, C.c_int, P, P, P]
+        L.vsa_fwd.restype = C.c_int
+        L.vsa_fwd.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, C.c_int, P, P, P, P, P, P, P, C.c_size_t, P]
+        L.vsa_bwd.restype = C.c_int
+        L.vsa_bwd.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P, P, P, P, P,
+                              C.c_size_t, P]
+        L.vsa_status_string.restype = C.c_char_p
+        L.vsa_status_string.argtypes = [C.c_int]
+        L.vsa_device_status.restype = C.c_int
+        L.vsa_device_status.argtypes = [P, P, C.POINTER(C.c_int32)]
+        L.vsa_profile_enable.argtypes = [C.c_int]
+        L.vsa_profile_count.restype = C.c_int
+        L.vsa_profile_name.restype = C.c_char_p
+        L.vsa_profile_name.argtypes = [C.c_int]
+        L.vsa_profile_ms.restype = C.c_float
+        L.vsa_profile_ms.argtypes = [C.c_int]
+        L.vsa_launch_count.restype = C.c_longlong
+        _lib = L
+    return _lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise VsaError(fn, code)
+
+
+# ------------------------------------------------------------- raw entry points
+
+def vsa_workspace_size(desc: VsaDesc, with_gate: bool) -> int:
+    return int(lib().vsa_workspace_size(C.byref(desc), int(bool(with_gate))))
+
+
+def vsa_build_block_map(desc, q, k, q_var, kv_var, topk, need_bwd_index, block_map, q_idx, q_cnt, idx_cap,
+                        kv_ptr, kv_qidx, workspace, stream=None):
+    _check("vsa_build_block_map", lib().vsa_build_block_map(
+        C.byref(desc), _p(q), _p(k), _p(q_var), _p(kv_var), int(topk), int(bool(need_bwd_index)),
+        _p(block_map), _p(q_idx), _p(q_cnt), int(idx_cap), _p(kv_ptr), _p(kv_qidx), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def vsa_mask_to_index(desc, block_map, q_var, kv_var, need_bwd_index, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx,
+                      stream=None):
+    _check("vsa_mask_to_index", lib().vsa_mask_to_index(
+        C.byref(desc), _p(block_map), _p(q_var), _p(kv_var), int(bool(need_bwd_index)), _p(q_idx), _p(q_cnt),
+        int(idx_cap), _p(kv_ptr), _p(kv_qidx), _stream(stream)))
+
+
+def vsa_fwd(desc, q, k, v, q_idx, q_cnt, idx_cap, q_var, kv_var, gate, out, lse, o_sparse, workspace,
+            stream=None):
+    _check("vsa_fwd", lib().vsa_fwd(
+        C.byref(desc), _p(q), _p(k), _p(v), _p(q_idx), _p(q_cnt), int(idx_cap), _p(q_var), _p(kv_var), _p(gate),
+        _p(out), _p(lse), _p(o_sparse), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def vsa_bwd(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx, q_var, kv_var, gate,
+            dq, dk, dv, workspace, stream=None):
+    _check("vsa_bwd", lib().vsa_bwd(
+        C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(o_sparse), _p(lse), _p(q_idx), _p(q_cnt), int(idx_cap),
+        _p(kv_ptr), _p(kv_qidx), _p(q_var), _p(kv_var), _p(gate), _p(dq), _p(dk), _p(dv), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def vsa_device_status(workspace, stream=None) -> int:
+    code = C.c_int32(0)
+    lib().vsa_device_status(_p(workspace), _stream(stream), C.byref(code))
+    return int(code.value)
+
+
+def vsa_launch_count() -> int:
+    return int(lib().vsa_launch_count())
+
+
+class profile:
+    """Context manager collecting per-kernel CUDA-event times (ms)."""
+
+    def __enter__(self):
+        L = lib()
+        L.vsa_profile_reset()
+        L.vsa_profile_enable(1)
+        self.records = []
+        return self
+
+    def __exit__(self, *exc):
+        L = lib()
+        L.vsa_profile_enable(0)
+        self.records = [(L.vsa_profile_name(i).decode(), float(L.vsa_profile_ms(i)))
+                        for i in range(L.vsa_profile_count())]
+        L.vsa_profile_reset()
+        return False
+
+
+# ----------------------------------------------------------------------- Plan
+
+class Plan:
+    """Descriptor, workspace and index buffers of one problem.
+
+    layout: "bhsd" | "bshd" | "tnd"; sizes as in vsa_desc. For TND pass
+    cu_seqlens_q / cu_seqlens_kv (int32 device tensors, [B+1]) and
+    max_seqlen_q / max_seqlen_kv (host ints) instead of Sq / Skv per batch.
+    """
+
+    def __init__(self, layout, dtype, B, Hq, Hkv, D, tile_q, tile_kv, nQ, nKV, Sq, Skv, idx_cap, gate=False,
+                 cu_seqlens_q=None, cu_seqlens_kv=None, q_var=None, kv_var=None, scale=0.0, device="cuda"):
+        self.layout, self.dtype = layout, dtype
+        self.B, self.Hq, self.Hkv, self.D = B, Hq, Hkv, D
+        self.tile_q, self.tile_kv, self.nQ, self.nKV = tile_q, tile_kv, nQ, nKV
+        self.Sq, self.Skv, self.idx_cap, self.gate = Sq, Skv, idx_cap, gate
+        self.cu_q, self.cu_kv = cu_seqlens_q, cu_seqlens_kv
+        self.q_var, self.kv_var = q_var, kv_var
+        self.device = torch.device(device)
+        self.desc = VsaDesc(LAYOUTS[layout], DTYPES[dtype], B, Hq, Hkv, D, Sq, Skv, tile_q, tile_kv, nQ, nKV,
+                            _p(cu_seqlens_q), _p(cu_seqlens_kv), float(scale))
+        ws = vsa_workspace_size(self.desc, gate)
+        if ws == 0:
+            raise ValueError("invalid problem description")
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=self.device)
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.block_map = torch.zeros((B, Hq, nQ, nKV), dtype=torch.uint8, device=self.device)
+        self.q_idx = torch.empty((B, Hq, nQ, idx_cap), **i32)
+        self.q_cnt = torch.empty((B, Hq, nQ), **i32)
+        self.kv_ptr = torch.empty((B, Hq, nKV + 1), **i32)
+        self.kv_qidx = torch.empty((B, Hq, nQ * idx_cap), **i32)
+
+    def lse_shape(self):
+        return (self.Hq, self.Sq) if self.layout == "tnd" else (self.B, self.Hq, self.Sq)
+
+    def build_block_map(self, q, k, topk, need_bwd_index=True, stream=None):
+        vsa_build_block_map(self.desc, q, k, self.q_var, self.kv_var, topk, need_bwd_index, self.block_map,
+                            self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr if need_bwd_index else None,
+                            self.kv_qidx if need_bwd_index else None, self.workspace, stream)
+
+    def mask_to_index(self, block_map, need_bwd_index=True, stream=None):
+        self.block_map = block_map
+        vsa_mask_to_index(self.desc, block_map, self.q_var, self.kv_var, need_bwd_index, self.q_idx, self.q_cnt,
+                          self.idx_cap, self.kv_ptr if need_bwd_index else None,
+                          self.kv_qidx if need_bwd_index else None, stream)
+
+    def forward(self, q, k, v, gate=None, out=None, lse=None, o_sparse=None, stream=None):
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty(self.lse_shape(), dtype=torch.float32, device=q.device) if lse is None else lse
+        if gate is not None and o_sparse is None:
+            o_sparse = torch.empty_like(q)
+        vsa_fwd(self.desc, q, k, v, self.q_idx, self.q_cnt, self.idx_cap, self.q_var, self.kv_var, gate, out, lse,
+                o_sparse, self.workspace, stream)
+        return out, lse, (o_sparse if o_sparse is not None else out)
+
+    def backward(self, dO, q, k, v, o_sparse, lse, gate=None, dq=None, dk=None, dv=None, stream=None):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        vsa_bwd(self.desc, dO, q, k, v, o_sparse, lse, self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr,
+                self.kv_qidx, self.q_var, self.kv_var, gate, dq, dk, dv, self.workspace, stream)
+        return dq, dk, dv
+
+    def device_status(self, stream=None) -> int:
+        return vsa_device_status(self.workspace, stream)
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

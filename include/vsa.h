@@ -1,0 +1,198 @@
+/*
+ * vsa.h -- C ABI of the GB300 (sm_103a) tile-top-k block-sparse video
+ * attention library (libvsa.so): forward and backward of softmax attention
+ * restricted, per query tile, to the key/value tiles chosen by top-k over
+ * tile-mean-pooled ("coarse") scores, with per-tile valid-token counts that
+ * trim padded 3D video tiles, and an optional gated compression branch.
+ *
+ * Sources (page titles, with the section that defines each operation):
+ *   [VSA-test]  FastVideo fastvideo-kernel/tests/test_vsa256_backward.py
+ *   [FA4-adapt] FastVideo fastvideo-kernel/python/fastvideo_kernel/
+ *               block_sparse_attn_cute_fwd.py
+ *   [NPU-test]  Ascend op-plugin test/test_custom_ops/
+ *               test_npu_block_sparse_attention_backward.py
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *   owned by the caller. The library allocates no device memory, frees
+ *   nothing and never synchronises: each call validates its arguments on
+ *   the host, enqueues kernels on `stream` and returns. Outputs are
+ *   overwritten, never accumulated into.
+ * - q, dO, out, o_sparse, gate and dq share the layout `layout` with Hq
+ *   heads; k, v, dk and dv share it with Hkv heads (GQA: query head h reads
+ *   key/value head h / (Hq / Hkv), as in [NPU-test]
+ *   cpu_block_sparse_attention_tnd_gqa_with_lse). All are dense (the last
+ *   dimension D is contiguous, no gaps) and 16-byte aligned.
+ *     VSA_LAYOUT_BHSD  [B, H, S, D]
+ *     VSA_LAYOUT_BSHD  [B, S, H, D]
+ *     VSA_LAYOUT_TND   [T, H, D], sequences packed along T with device
+ *                      offsets cu_seqlens_* ([B+1] int32, ascending).
+ * - In the padded video layouts each batch entry holds nQ query tiles of
+ *   tile_q tokens and nKV key/value tiles of tile_kv tokens; the first
+ *   q_var[i] / kv_var[j] slots of a tile are its valid tokens and the rest
+ *   are zero padding ([VSA-test] _zero_pad_tail). q_var / kv_var are device
+ *   int32 arrays [nQ] / [nKV], shared by every batch entry and head. In
+ *   TND the valid tokens of tile t of sequence b are
+ *   min(tile, len_b - t*tile) (zero past the end) and q_var / kv_var are
+ *   ignored (pass NULL).
+ * - Every query slot of a padded Q tile is a query row (the valid-length
+ *   mask applies to keys only, [FA4-adapt] _vbs_mask_mod); in TND only
+ *   rows inside a sequence exist and only those are written.
+ * - The LSE is fp32, natural log, head-major: [B, Hq, Sq] for the padded
+ *   layouts and [Hq, T] for TND ([VSA-test] test_vsa256_cute_lse_is_bhs).
+ *   A row whose selected tiles hold no valid key gets O = 0, LSE = -inf.
+ * - Block index (Q-owned CSR): q_idx [B, Hq, nQ, idx_cap] int32 lists, per
+ *   query tile, the selected KV tiles that hold at least one valid token,
+ *   ascending; q_cnt [B, Hq, nQ] counts them; unused slots are -1.
+ * - Transposed index (KV-owned CSR, one per query head): kv_ptr
+ *   [B, Hq, nKV+1] int32 offsets into kv_qidx [B, Hq, nQ*idx_cap], which
+ *   lists, for KV tile j, the query tiles whose index holds j, ascending
+ *   ([FA4-adapt] _build_sparse_tensors, KV-owned backward metadata).
+ *   Entries past kv_ptr[nKV] are -1.
+ * - workspace is caller-allocated device scratch of at least
+ *   vsa_workspace_size() bytes, 256-byte aligned. Its first 256 bytes hold
+ *   a device status word that kernels set if an internal wait times out
+ *   (read it with vsa_device_status). The rest is scratch that one call
+ *   does not pass to the next. Calls that share a workspace must not run
+ *   concurrently.
+ */
+#ifndef VSA_H
+#define VSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *vsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    VSA_OK = 0,
+    VSA_ERR_NULL = 1,            /* a required pointer is NULL */
+    VSA_ERR_SHAPE = 2,           /* sizes inconsistent, var out of [0, tile], idx_cap too small */
+    VSA_ERR_DTYPE = 3,           /* dtype not bf16 / fp16 */
+    VSA_ERR_LAYOUT = 4,          /* unknown layout, or a pointer not 16-byte aligned */
+    VSA_ERR_UNSUPPORTED = 5,     /* D != 128, tile not 128/256, or a size past a kernel limit */
+    VSA_ERR_MISSING_SEQLENS = 6, /* TND without both cu_seqlens_q and cu_seqlens_kv */
+    VSA_ERR_WORKSPACE = 7,       /* workspace NULL, misaligned or smaller than required */
+    VSA_ERR_CUDA = 8,            /* a CUDA runtime call or kernel launch failed */
+    VSA_ERR_DEVICE = 9           /* a kernel recorded a failed internal wait (see vsa_device_status) */
+} vsa_status;
+
+typedef enum { VSA_LAYOUT_BHSD = 0, VSA_LAYOUT_BSHD = 1, VSA_LAYOUT_TND = 2 } vsa_layout;
+typedef enum { VSA_DTYPE_BF16 = 0, VSA_DTYPE_FP16 = 1 } vsa_dtype;
+
+/* Problem descriptor (host memory; pointed-to seqlens are device memory). */
+typedef struct {
+    int32_t layout;     /* vsa_layout */
+    int32_t dtype;      /* vsa_dtype of q, k, v, dO, gate, out, o_sparse, dq, dk, dv */
+    int32_t B;          /* batch entries (TND: number of sequences) */
+    int32_t Hq, Hkv;    /* query heads, key/value heads; Hq % Hkv == 0 */
+    int32_t D;          /* head dim; must be 128 */
+    int32_t Sq, Skv;    /* padded layouts: tokens per batch entry, = nQ*tile_q and
+                           nKV*tile_kv. TND: total tokens T_q, T_kv */
+    int32_t tile_q;     /* tokens per query tile: 128 or 256 */
+    int32_t tile_kv;    /* tokens per key/value tile: 128 or 256 */
+    int32_t nQ, nKV;    /* tiles per batch entry. TND: ceil(max_len / tile) */
+    const int32_t *cu_seqlens_q;  /* TND only: device [B+1] token offsets */
+    const int32_t *cu_seqlens_kv; /* TND only: device [B+1] token offsets */
+    float scale;        /* softmax scale on q.k; 0 means 1/sqrt(D) */
+} vsa_desc;
+
+/* Bytes of workspace needed by every call below for this problem (with or
+ * without the gated compression branch). */
+size_t vsa_workspace_size(const vsa_desc *desc, int with_gate);
+
+/* Block-map step. Tile means of q (over the first q_var[i] tokens, per
+ * query head) and of k (first kv_var[j] tokens, per key/value head) in
+ * fp32, a sequential round-to-nearest sum then an IEEE divide; raw coarse
+ * scores r_ij = pq_i . pk_j as an fp32 fma chain over ascending d; per
+ * query tile, the min(topk, nKV) largest r_ij under (r desc, j asc), with
+ * r = -inf for tiles without valid tokens. The pages call the step with
+ * (q, k, q_var, kv_var, topk) ([VSA-test] video_sparse_attn's topk argument;
+ * [FA4-adapt] _map_to_index and the vbs > 0 split for the index).
+ * Writes block_map [B, Hq, nQ, nKV] uint8 (1 = selected), q_idx / q_cnt
+ * (idx_cap >= min(topk, nKV)) and, when need_bwd_index != 0, the
+ * transposed index kv_ptr / kv_qidx; with need_bwd_index == 0 those two may
+ * be NULL and are not touched (the inference fast path of [FA4-adapt]
+ * _build_sparse_tensors). The result is bit-identical across runs and
+ * independent of need_bwd_index. In TND a query tile past its sequence's
+ * end selects nothing. */
+vsa_status vsa_build_block_map(const vsa_desc *desc, const void *q, const void *k,
+                               const int32_t *q_var, const int32_t *kv_var, int topk,
+                               int need_bwd_index, uint8_t *block_map, int32_t *q_idx,
+                               int32_t *q_cnt, int idx_cap, int32_t *kv_ptr, int32_t *kv_qidx,
+                               void *workspace, size_t workspace_bytes, vsa_stream_t stream);
+
+/* Index step for a caller-given block map [B, Hq, nQ, nKV] uint8 (nonzero
+ * = attend), as in [NPU-test] (block_sparse_mask) and [FA4-adapt]
+ * _map_to_index. Tiles without valid tokens, and in TND blocks past either
+ * sequence's end, are dropped. idx_cap >= nKV. kv_ptr / kv_qidx as for
+ * vsa_build_block_map. */
+vsa_status vsa_mask_to_index(const vsa_desc *desc, const uint8_t *block_map,
+                             const int32_t *q_var, const int32_t *kv_var, int need_bwd_index,
+                             int32_t *q_idx, int32_t *q_cnt, int idx_cap, int32_t *kv_ptr,
+                             int32_t *kv_qidx, vsa_stream_t stream);
+
+/* Forward. For every query row t of query tile i: softmax over the valid
+ * keys of the KV tiles in q_idx[.., i, :] of scale * q_t . k_u, O_t =
+ * sum_u P_tu v_u, LSE_t = max + ln(sum exp(s - max)) ([NPU-test]
+ * cpu_block_sparse_attention_tnd_gqa_with_lse with the key mask of
+ * [FA4-adapt] _vbs_mask_mod). Writes o_sparse (the attention output) and
+ * lse. With gate == NULL, out receives O as well (o_sparse may then be
+ * NULL or equal to out). With a gate (q-shaped, elementwise), the gated
+ * compression branch adds, on every query row of tile i,
+ * out_t = O_t + gate_t (*) c_i, c_i = sum_j softmax_j(scale pq_i . pk_j) pv_j
+ * over the non-empty KV tiles, from the tile means of q, k, v ([VSA-test]
+ * test_vsa256_cute_backward_with_compress_gate); o_sparse must then be a
+ * separate buffer (the composition never overwrites the sparse output). */
+vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const void *v,
+                   const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
+                   const int32_t *q_var, const int32_t *kv_var, const void *gate, void *out,
+                   float *lse, void *o_sparse, void *workspace, size_t workspace_bytes,
+                   vsa_stream_t stream);
+
+/* Backward of vsa_fwd with the block index held fixed. Dvec_t = dO_t .
+ * O_t (o_sparse); P = exp(scale q.k - LSE); dS = P (dO.v - Dvec);
+ * dQ = scale sum dS k (Q-owned pass over q_idx); dK = scale sum dS^T q and
+ * dV = sum P^T dO (KV-owned pass over kv_ptr / kv_qidx, summed over each
+ * GQA group, no atomics) ([NPU-test] _softmax_backward_np and
+ * cpu_block_sparse_attention_backward_tnd_gqa; [FA4-adapt]
+ * _CuteAttentionQ128.backward). With a gate, the compression branch's
+ * gradients flow to q, k, v through the tile means (1/var on the valid
+ * slots); the gate receives none. dq has q's shape; dk, dv have k's.
+ * Padded key slots get dk = dv = 0. */
+vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const void *k,
+                   const void *v, const void *o_sparse, const float *lse, const int32_t *q_idx,
+                   const int32_t *q_cnt, int idx_cap, const int32_t *kv_ptr,
+                   const int32_t *kv_qidx, const int32_t *q_var, const int32_t *kv_var,
+                   const void *gate, void *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, vsa_stream_t stream);
+
+/* Human-readable name of a status. */
+const char *vsa_status_string(vsa_status status);
+
+/* Synchronises `stream`, reads the device status word in `workspace` into
+ * *code (0 = no failure; otherwise the site of the wait that timed out) and
+ * clears it. Returns VSA_ERR_DEVICE when *code != 0. */
+vsa_status vsa_device_status(void *workspace, vsa_stream_t stream, int32_t *code);
+
+/* Instrumentation. While enabled, every kernel the library launches is
+ * bracketed by CUDA events on its stream; vsa_profile_count / _name / _ms
+ * read the records (synchronising on the events) and vsa_profile_reset
+ * clears them. vsa_launch_count returns the number of kernels launched
+ * since the library was loaded. */
+void vsa_profile_enable(int on);
+int vsa_profile_count(void);
+const char *vsa_profile_name(int i);
+float vsa_profile_ms(int i);
+void vsa_profile_reset(void);
+long long vsa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VSA_H */

@@ -117,3 +117,24 @@ def masked_attention_f64(q, k, v, mask, scale):
     empty = ~mask.any(dim=-1)
     out = torch.where(empty[..., None], torch.zeros_like(out), out)
     return out, lse
+
+
+# ------------------------------------------------------- GPU path plumbing
+
+def plan_for(p, device="cuda"):
+    """A libvsa Plan for problem p (descriptor, workspace, index buffers)."""
+    from bwd_tile_mean_gb300 import vsa
+    from bwd_tile_mean_gb300.inputs import DTYPES
+    dev = torch.device(device)
+    i32 = dict(dtype=torch.int32, device=dev)
+    kw = {}
+    if p.varlen:
+        kw.update(cu_seqlens_q=torch.as_tensor(p.cu_q, **i32), cu_seqlens_kv=torch.as_tensor(p.cu_kv, **i32))
+    else:
+        kw.update(q_var=torch.as_tensor(p.q_var, **i32), kv_var=torch.as_tensor(p.kv_var, **i32))
+    return vsa.Plan(p.layout, DTYPES[p.dtype], p.B, p.Hq, p.Hkv, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV, p.Sq,
+                    p.Skv, p.cap, gate=p.gate is not None, scale=p.scale, device=dev, **kw)
+
+
+def to_device(t, device="cuda"):
+    return {n: x.to(device) for n, x in t.items()}

@@ -1,0 +1,79 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point include/vsa.h declares, and rejects bad arguments on the host before
+any CUDA call."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from bwd_tile_mean_gb300 import build as libbuild
+from bwd_tile_mean_gb300 import vsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    libbuild.build()
+    return vsa.lib()
+
+
+def declared():
+    src = open(os.path.join(ROOT, "include", "vsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared()
+    assert set(vsa.EXPORTS) == set(names), (names, vsa.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def desc(**kw):
+    d = dict(layout=1, dtype=0, B=1, Hq=2, Hkv=2, D=128, Sq=768, Skv=1024, tile_q=256, tile_kv=256, nQ=3, nKV=4,
+             cu_seqlens_q=None, cu_seqlens_kv=None, scale=0.0)
+    d.update(kw)
+    return vsa.VsaDesc(*[d[f] for f, _ in vsa.VsaDesc._fields_])
+
+
+def test_workspace_size(L):
+    assert vsa.vsa_workspace_size(desc(), False) > 0
+    assert vsa.vsa_workspace_size(desc(), True) > vsa.vsa_workspace_size(desc(), False)
+    assert vsa.vsa_workspace_size(desc(D=64), False) == 0
+    assert vsa.vsa_workspace_size(desc(Hq=3, Hkv=2), False) == 0
+
+
+FAKE = C.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd(L, d, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, q_idx=FAKE, q_cnt=FAKE, cap=2, q_var=FAKE, kv_var=FAKE, gate=None, out=FAKE,
+             lse=FAKE, osp=None, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return L.vsa_fwd(C.byref(d), a["q"], a["k"], a["v"], a["q_idx"], a["q_cnt"], a["cap"], a["q_var"],
+                     a["kv_var"], a["gate"], a["out"], a["lse"], a["osp"], a["ws"], a["wsb"], None)
+
+
+def test_host_validation_errors(L):
+    assert fwd(L, desc(D=64)) == 5                       # VSA_ERR_UNSUPPORTED
+    assert fwd(L, desc(tile_q=64)) == 5
+    assert fwd(L, desc(dtype=7)) == 3                    # VSA_ERR_DTYPE
+    assert fwd(L, desc(layout=9)) == 4                   # VSA_ERR_LAYOUT
+    assert fwd(L, desc(layout=2, Sq=100, Skv=200)) == 6  # TND without seqlens
+    assert fwd(L, desc(Sq=700)) == 2                     # Sq != nQ * tile_q
+    assert fwd(L, desc(), q=None) == 1                   # VSA_ERR_NULL
+    assert fwd(L, desc(), kv_var=None) == 1
+    assert fwd(L, desc(), gate=FAKE) == 1                # gated needs a separate o_sparse
+    assert fwd(L, desc(), q=C.c_void_p((1 << 20) + 2)) == 4
+    assert fwd(L, desc(), wsb=16) == 7                   # workspace too small
+    assert fwd(L, desc(), ws=C.c_void_p((1 << 20) + 16)) == 7
+    assert fwd(L, desc(), cap=9) == 2                    # idx_cap > nKV
+    assert L.vsa_build_block_map(C.byref(desc()), FAKE, FAKE, FAKE, FAKE, 0, 0, FAKE, FAKE, FAKE, 2, None, None,
+                                 FAKE, 1 << 30, None) == 2   # topk < 1
+    assert L.vsa_build_block_map(C.byref(desc()), FAKE, FAKE, FAKE, FAKE, 2, 1, FAKE, FAKE, FAKE, 2, None, None,
+                                 FAKE, 1 << 30, None) == 1   # bwd index needs kv_ptr / kv_qidx
+    assert L.vsa_mask_to_index(C.byref(desc()), FAKE, None, FAKE, 0, FAKE, FAKE, 3, None, None, None) == 2
+    assert L.vsa_status_string(5).decode().startswith("unsupported")
