@@ -1,11 +1,857 @@
-// bwd_kernels.cu -- placeholder launchers (backward kernels pending).
+// bwd_kernels.cu -- block-sparse attention backward on tcgen05, plus the
+// row-sum preprocess and the gated compression branch's backward.
+//
+// Pages: Ascend test_npu_block_sparse_attention_backward.py
+// (_softmax_backward_np: dS = P (dP - rowsum(P dP)); the TND/GQA backward
+// golden: dQ = dS K, dK += dS^T Q, dV += P^T dO, summed over the GQA group);
+// FastVideo block_sparse_attn_cute_fwd.py (the backward is KV-owned over
+// the transposed index; _CuteAttentionQ128.backward recomputes P from the
+// saved LSE with softmax_scale = D^-0.5).
+//
+// rowsum(P dP) equals Dvec = rowsum(dO * O), computed once per query row
+// by k_dvec. The KV-owned pass k_dkdv and the Q-owned pass k_dq each
+// recompute S and dP on the tensor core, so neither needs atomics and every
+// output element is written by exactly one CTA.
+#include "sm103_ptx.cuh"
 #include "vsa_internal.h"
 
 namespace vsa {
-cudaError_t launch_dvec(const Prob &, const void *, const void *, float *, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dkdv(const Prob &, const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dq(const Prob &, const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_compress_bwd(const Prob &, const void *, const void *, const float *, const float *,
-                                const float *, float *, float *, float *, float *, float *, float *,
-                                cudaStream_t) { return cudaErrorNotSupported; }
+using namespace ptx;
+
+namespace {
+
+constexpr int kTile = 32 * 1024;
+constexpr int kBox = 16 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : unsigned { kSiteDkProd = 0x201, kSiteDkMma = 0x202, kSiteDkSoft = 0x203,
+                  kSiteDqProd = 0x301, kSiteDqMma = 0x302, kSiteDqSoft = 0x303 };
+
+// D (+)= A B^T with A [128 x 128] and B [128 x 128], both K-major tiles
+// (two 64-column boxes, 128-byte swizzle).
+__device__ __forceinline__ void issue_kk(uint32_t d, uint32_t aA, uint32_t aB, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_f16_ss(d, sdesc_sw128(aA + off, 16, 1024), sdesc_sw128(aB + off, 16, 1024), idesc,
+                   (acc || kk > 0) ? 1u : 0u);
+    }
+}
+// D (+)= A B with A [128 x 128] K-major and B [K=128 rows x N=128] stored
+// row-major (N contiguous), read MN-major.
+__device__ __forceinline__ void issue_kn(uint32_t d, uint32_t aA, uint32_t aB, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t offa = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_f16_ss(d, sdesc_sw128(aA + offa, 16, 1024), sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
+                   (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+// Writes one thread's row of 128 16-bit values (64 packed words) into a
+// K-major 128-byte-swizzled [128 x 128] tile.
+__device__ __forceinline__ void store_row_sw128(uint8_t *tile, int r, const uint32_t (&w)[64]) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4 *>(tile + hf * kBox + sw128_off(r, u)) =
+                make_uint4(w[hf * 32 + u * 4], w[hf * 32 + u * 4 + 1], w[hf * 32 + u * 4 + 2], w[hf * 32 + u * 4 + 3]);
+}
+
+__device__ __forceinline__ void named_sync_softmax() {  // the four softmax warps only
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ dvec
+// Dvec_t = sum_d dO_t,d * O_t,d; one warp per query row.
+template <typename T>
+__global__ void __launch_bounds__(256) k_dvec(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
+                                              float *__restrict__ dvec) {
+    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    long long rows_per_h;
+    int b, s, h;
+    if (p.layout == L_TND) {
+        rows_per_h = p.Sq;
+        if (w >= rows_per_h * p.Hq) return;
+        const int tok = (int)(w / p.Hq);
+        h = (int)(w % p.Hq);
+        // batch entry of token tok (binary search over cu_q)
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu_q[mid] <= tok) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        s = tok - p.cu_q[b];
+    } else {
+        if (w >= (long long)p.B * p.Sq * p.Hq) return;
+        if (p.layout == L_BSHD) {
+            h = (int)(w % p.Hq);
+            s = (int)((w / p.Hq) % p.Sq);
+            b = (int)(w / ((long long)p.Hq * p.Sq));
+        } else {
+            s = (int)(w % p.Sq);
+            h = (int)((w / p.Sq) % p.Hq);
+            b = (int)(w / ((long long)p.Hq * p.Sq));
+        }
+    }
+    const long long o = tok_off(p, true, b, s, h) + lane * 4;
+    const uint2 a = __ldg(reinterpret_cast<const uint2 *>(dO + o));
+    const uint2 c = __ldg(reinterpret_cast<const uint2 *>(O + o));
+    const float2 a0 = unpack2<T>(a.x), a1 = unpack2<T>(a.y), c0 = unpack2<T>(c.x), c1 = unpack2<T>(c.y);
+    float acc = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dvec[lse_off(p, b, h, s)] = acc;
+}
+
+// ----------------------------------------------------------------- dK/dV
+// One CTA per (b, kv-head hk, 128-key chunk of KV tile j). Work items are
+// the 128-row chunks of every query tile that selected j, over the query
+// heads of hk's group, in (head, ascending tile, chunk) order. Per item:
+//   S^T = K Q^T and dP^T = V dO^T   (TMEM, thread = key row)
+//   P^T = exp(scale S^T - LSE_t), dS^T = P^T (dP^T - Dvec_t)
+//   dV += P^T dO, dK += dS^T Q       (TMEM accumulators)
+// P^T and dS^T take turns in one shared-memory tile. TMEM columns:
+// S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
+constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 4 * kTile, kDkOffX = 6 * kTile;
+constexpr int kDkOffCtl = 7 * kTile;
+constexpr size_t kDkSmem = 1024 + kDkOffCtl + 256;
+
+struct WorkIter {
+    int h, pos, end, sub, i, nsub;
+};
+
+__device__ __forceinline__ bool work_next_list(const Prob &p, const BwdArgs &a, int b, int h_end, int j,
+                                               WorkIter &w) {
+    while (w.pos >= w.end) {
+        if (++w.h >= h_end) return false;
+        const int *ptr = a.kv_ptr + ((long long)b * p.Hq + w.h) * (p.nKV + 1);
+        w.pos = ptr[j];
+        w.end = ptr[j + 1];
+    }
+    w.i = a.kv_qidx[((long long)b * p.Hq + w.h) * p.nQ * a.cap + w.pos];
+    w.nsub = (q_rows(p, b, w.i) + 127) >> 7;
+    w.sub = 0;
+    return true;
+}
+__device__ __forceinline__ bool work_first(const Prob &p, const BwdArgs &a, int b, int h0, int h_end, int j,
+                                           WorkIter &w) {
+    w.h = h0;
+    const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h0) * (p.nKV + 1);
+    w.pos = ptr[j];
+    w.end = ptr[j + 1];
+    return work_next_list(p, a, b, h_end, j, w);
+}
+__device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, int b, int h_end, int j,
+                                             WorkIter &w) {
+    if (++w.sub < w.nsub) return true;
+    ++w.pos;
+    return work_next_list(p, a, b, h_end, j, w);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+    k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
+           const BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sX = sm + kDkOffX;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_sfree = bars + 6;
+    uint64_t *b_pf = bars + 7, *b_dsf = bars + 8, *b_dv = bars + 9, *b_dk = bars + 10, *b_fin = bars + 11;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 12);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int subs_kv = p.tile_kv >> 7;
+    const int j = blockIdx.x / subs_kv, ck = blockIdx.x % subs_kv;
+    const int hk = blockIdx.y, b = blockIdx.z, g = p.Hq / p.Hkv;
+    const int h0 = hk * g, h_end = h0 + g;
+    const int kvalid_tile = kv_valid(p, b, j);
+    int kvalid = kvalid_tile - ck * 128;
+    kvalid = kvalid < 0 ? 0 : (kvalid > 128 ? 128 : kvalid);
+    const int key0 = j * p.tile_kv + ck * 128;  // within the batch entry
+    if (p.layout == L_TND && kvalid == 0) return;  // keys outside the sequence do not exist
+    const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0), qb = (p.layout == L_TND ? p.cu_q[b] : 0);
+    const int bc = (p.layout == L_TND ? 0 : b);
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(b_qf + s, 1);
+            mbar_init(b_qe + s, 1);
+        }
+        mbar_init(b_sf, 1);
+        mbar_init(b_sfree, 128);
+        mbar_init(b_pf, 128);
+        mbar_init(b_dsf, 128);
+        mbar_init(b_dv, 1);
+        mbar_init(b_dk, 1);
+        mbar_init(b_fin, 1);
+        *s_abort = 0;
+        // count the work items (a chunk with no valid key does no work)
+        int n = 0;
+        if (kvalid > 0)
+            for (int h = h0; h < h_end; ++h) {
+                const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
+                if (p.layout != L_TND) {  // every query tile has tile_q rows
+                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q >> 7);
+                    continue;
+                }
+                const int *lst = a.kv_qidx + ((long long)b * p.Hq + h) * p.nQ * a.cap;
+                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + 127) >> 7;
+            }
+        *s_nwork = n;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *s_tmem;
+    const int M = *s_nwork;
+    const bool bf16 = (p.dtype == T_BF16);
+    int issued_kv = 0, issued[2] = {0, 0}, mma_started = 0;
+
+    if (warp == 0 && lane == 0 && M > 0) {
+        // ------------------------------------------------------ producer
+        mbar_expect_tx(b_kv, 2 * kTile);
+        tma_load_4d(sK, &tk, b_kv, 0, kvb + key0, hk, bc);
+        tma_load_4d(sK + kBox, &tk, b_kv, 64, kvb + key0, hk, bc);
+        tma_load_4d(sV, &tv, b_kv, 0, kvb + key0, hk, bc);
+        tma_load_4d(sV + kBox, &tv, b_kv, 64, kvb + key0, hk, bc);
+        issued_kv = 1;
+        WorkIter w;
+        bool more = work_first(p, a, b, h0, h_end, j, w);
+        for (int m = 0; more && m < M; ++m) {
+            const int s = m & 1;
+            if (m >= 2 && !mbar_wait(b_qe + s, ((m >> 1) - 1) & 1, s_abort, a.err, kSiteDkProd)) break;
+            const int row = qb + w.i * p.tile_q + w.sub * 128;
+            mbar_expect_tx(b_qf + s, 2 * kTile);
+            tma_load_4d(sQ + s * kTile, &tq, b_qf + s, 0, row, w.h, bc);
+            tma_load_4d(sQ + s * kTile + kBox, &tq, b_qf + s, 64, row, w.h, bc);
+            tma_load_4d(sO + s * kTile, &tdo, b_qf + s, 0, row, w.h, bc);
+            tma_load_4d(sO + s * kTile + kBox, &tdo, b_qf + s, 64, row, w.h, bc);
+            issued[s]++;
+            more = work_advance(p, a, b, h_end, j, w);
+        }
+    } else if (warp == 1 && lane == 0 && M > 0) {
+        // ---------------------------------------------------- MMA issuer
+        const uint32_t idKK = idesc_f16(bf16, 128, 128, false, false);
+        const uint32_t idKN = idesc_f16(bf16, 128, 128, false, true);
+        const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO),
+                       aX = smem_addr(sX);
+        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma);
+        for (int m = 0; ok && m < M; ++m) {
+            const int s = m & 1;
+            if (!(ok = mbar_wait(b_qf + s, (m >> 1) & 1, s_abort, a.err, kSiteDkMma))) break;
+            if (m > 0 && !(ok = mbar_wait(b_sfree, (m - 1) & 1, s_abort, a.err, kSiteDkMma))) break;
+            tc_fence_after();
+            issue_kk(tbase + 0, aK, aQ + s * kTile, idKK, false);    // S^T = K Q^T
+            issue_kk(tbase + 128, aV, aO + s * kTile, idKK, false);  // dP^T = V dO^T
+            mma_commit(b_sf);
+            mma_started = 1;
+            if (m > 0) {
+                const int sp = (m - 1) & 1;
+                if (!(ok = mbar_wait(b_dsf, (m - 1) & 1, s_abort, a.err, kSiteDkMma))) break;
+                tc_fence_after();
+                issue_kn(tbase + 384, aX, aQ + sp * kTile, idKN, m - 1 > 0);  // dK += dS^T Q
+                mma_commit(b_dk);
+                mma_commit(b_qe + sp);
+            }
+            if (!(ok = mbar_wait(b_pf, m & 1, s_abort, a.err, kSiteDkMma))) break;
+            tc_fence_after();
+            issue_kn(tbase + 256, aX, aO + s * kTile, idKN, m > 0);  // dV += P^T dO
+            mma_commit(b_dv);
+        }
+        if (ok) {
+            const int sp = (M - 1) & 1;
+            if (mbar_wait(b_dsf, (M - 1) & 1, s_abort, a.err, kSiteDkMma)) {
+                tc_fence_after();
+                issue_kn(tbase + 384, aX, aQ + sp * kTile, idKN, M - 1 > 0);
+                mma_commit(b_dk);
+                mma_commit(b_qe + sp);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------- softmax + epilogue
+        const int u = (warp - 4) * 32 + lane;  // key row within the chunk
+        const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        const bool key_ok = u < kvalid;
+        WorkIter w;
+        bool more = M > 0 && work_first(p, a, b, h0, h_end, j, w);
+        bool ok = true;
+        for (int m = 0; more && m < M; ++m) {
+            const int qrow0 = w.i * p.tile_q + w.sub * 128;  // within the batch entry
+            int nq = q_rows(p, b, w.i) - w.sub * 128;
+            nq = nq > 128 ? 128 : nq;
+            const float *lse_row = a.lse + lse_off(p, b, w.h, qrow0);
+            const float *dv_row = a.dvec + lse_off(p, b, w.h, qrow0);
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t pw[64], dw[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tl + q4 * 32, sr);
+                tmem_ld32(tl + 128 + q4 * 32, dr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t2 = 0; t2 < 16; ++t2) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = q4 * 32 + t2 * 2 + e;
+                        const bool on = key_ok && t < nq;
+                        const float l2 = on ? __ldg(lse_row + t) * kLog2e : 0.f;
+                        const float dvv = on ? __ldg(dv_row + t) : 0.f;
+                        const float pr = on ? ex2(fmaf(__uint_as_float(sr[t2 * 2 + e]), sl2, -l2)) : 0.f;
+                        pp[e] = pr;
+                        dd[e] = pr * (__uint_as_float(dr[t2 * 2 + e]) - dvv);
+                    }
+                    pw[q4 * 16 + t2] = pack2<T>(pp[0], pp[1]);
+                    dw[q4 * 16 + t2] = pack2<T>(dd[0], dd[1]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(b_sfree);
+            if (m > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(b_dk, (m - 1) & 1, s_abort, a.err, kSiteDkSoft));
+                if (!ok) break;
+            }
+            store_row_sw128(sX, u, pw);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_pf);
+            ok = __all_sync(0xffffffffu, mbar_wait(b_dv, m & 1, s_abort, a.err, kSiteDkSoft));
+            if (!ok) break;
+            store_row_sw128(sX, u, dw);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_dsf);
+            more = work_advance(p, a, b, h_end, j, w);
+        }
+        if (ok && M > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_dk, (M - 1) & 1, s_abort, a.err, kSiteDkSoft) &&
+                                             mbar_wait(b_dv, (M - 1) & 1, s_abort, a.err, kSiteDkSoft));
+            if (ok) tc_fence_after();
+        }
+        const bool have = ok && M > 0;
+        const bool row_ok = (p.layout == L_TND) ? key_ok : true;
+        const long long ro = tok_off(p, false, b, key0 + u, hk);
+        T *dk = reinterpret_cast<T *>(a.dk) + ro;
+        T *dv = reinterpret_cast<T *>(a.dv) + ro;
+        const float inv = kvalid_tile > 0 ? 1.f / (float)kvalid_tile : 0.f;
+        const float *cpk = a.dpk ? a.dpk + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
+        const float *cpv = a.dpv ? a.dpv + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {  // 0: dV (cols 256..), 1: dK (cols 384..)
+            T *dst = which ? dk : dv;
+            const float *cadd = which ? cpk : cpv;
+            const float mul = which ? p.scale : 1.f;
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld32(tl + 256 + which * 128 + q4 * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (!row_ok) continue;
+                uint32_t wv[16];
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    float v0 = key_ok ? __uint_as_float(o[2 * e2]) * mul : 0.f;
+                    float v1 = key_ok ? __uint_as_float(o[2 * e2 + 1]) * mul : 0.f;
+                    if (cadd && key_ok) {
+                        v0 += cadd[q4 * 32 + 2 * e2] * inv;
+                        v1 += cadd[q4 * 32 + 2 * e2 + 1] * inv;
+                    }
+                    wv[e2] = pack2<T>(v0, v1);
+                }
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            }
+        }
+    }
+
+    if (*s_abort) {
+        int never = 0;
+        if (warp == 0 && lane == 0) {
+            if (issued_kv) mbar_wait(b_kv, 0, &never, nullptr, 0, 200000000ull);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+        }
+        if (warp == 1 && lane == 0 && mma_started) {
+            mma_commit(b_fin);
+            mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// -------------------------------------------------------------------- dQ
+// One CTA per (b, h, 128-row chunk of query tile i), looping over the
+// selected KV tiles' 128-key chunks:
+//   S = Q K^T, dP = dO V^T (TMEM), P = exp(scale S - LSE),
+//   dS = P (dP - Dvec) -> shared memory, dQ += dS K (TMEM).
+// TMEM columns: S [0,128), dP [128,256), dQ [256,384).
+constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = 4 * kTile, kDqOffX = 5 * kTile;
+constexpr int kDqOffCtl = 6 * kTile;
+constexpr size_t kDqSmem = 1024 + kDqOffCtl + 256 + kMaxChunks * 6;
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+    k_dq(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
+         const BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV, *sX = sm + kDqOffX;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
+    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 3, *b_vf = bars + 5, *b_ve = bars + 6;
+    uint64_t *b_sf = bars + 7, *b_sfree = bars + 8, *b_dsf = bars + 9, *b_dq = bars + 10, *b_fin = bars + 11;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 12);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
+    int *s_crow = reinterpret_cast<int *>(sm + kDqOffCtl + 256);
+    short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int subs = p.tile_q >> 7;
+    const int i = blockIdx.x / subs, half = blockIdx.x % subs;
+    const int h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    const int row0 = i * p.tile_q + half * 128;
+    int nrows = 128;
+    if (p.layout == L_TND) {
+        nrows = (p.cu_q[b + 1] - p.cu_q[b]) - row0;
+        if (nrows <= 0) return;
+        nrows = nrows > 128 ? 128 : nrows;
+    }
+    const int qrc = (p.layout == L_TND ? p.cu_q[b] : 0) + row0;
+    const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0);
+    const int bc = (p.layout == L_TND ? 0 : b);
+    const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_q, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(b_kf + s, 1);
+            mbar_init(b_ke + s, 1);
+        }
+        mbar_init(b_vf, 1);
+        mbar_init(b_ve, 1);
+        mbar_init(b_sf, 1);
+        mbar_init(b_sfree, 128);
+        mbar_init(b_dsf, 128);
+        mbar_init(b_dq, 1);
+        mbar_init(b_fin, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        const int cnt = a.q_cnt[qrow];
+        const int *idx = a.q_idx + qrow * a.cap;
+        const int per = p.tile_kv >> 7;
+        int total = 0;
+        for (int n0 = 0; n0 < cnt; n0 += 32) {
+            const int n = n0 + lane;
+            int jj = 0, kvv = 0, nc = 0;
+            if (n < cnt) {
+                jj = idx[n];
+                kvv = kv_valid(p, b, jj);
+                nc = min(per, (kvv + 127) >> 7);
+            }
+            int inc = nc;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += y;
+            }
+            const int base = total + inc - nc;
+            for (int c = 0; c < nc; ++c) {
+                const int pos = base + c;
+                if (pos < kMaxChunks) {
+                    s_crow[pos] = jj * p.tile_kv + c * 128;
+                    s_cval[pos] = (short)min(128, kvv - c * 128);
+                }
+            }
+            total += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) *s_nchunk = min(total, kMaxChunks);
+    } else if (warp == 1) {
+        tmem_alloc(s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *s_tmem;
+    const int N = *s_nchunk;
+    const bool bf16 = (p.dtype == T_BF16);
+    int issued_q = 0, issued[2] = {0, 0}, issued_v = 0, mma_started = 0;
+
+    if (warp == 0 && lane == 0 && N > 0) {
+        mbar_expect_tx(b_q, 2 * kTile);
+        tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
+        tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
+        tma_load_4d(sO, &tdo, b_q, 0, qrc, h, bc);
+        tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
+        issued_q = 1;
+        for (int c = 0; c < N; ++c) {
+            const int s = c & 1;
+            const int kr = kvb + s_crow[c];
+            if (c >= 2 && !mbar_wait(b_ke + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
+            mbar_expect_tx(b_kf + s, kTile);
+            tma_load_4d(sK + s * kTile, &tk, b_kf + s, 0, kr, hk, bc);
+            tma_load_4d(sK + s * kTile + kBox, &tk, b_kf + s, 64, kr, hk, bc);
+            issued[s]++;
+            if (c >= 1 && !mbar_wait(b_ve, (c - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
+            mbar_expect_tx(b_vf, kTile);
+            tma_load_4d(sV, &tv, b_vf, 0, kr, hk, bc);
+            tma_load_4d(sV + kBox, &tv, b_vf, 64, kr, hk, bc);
+            issued_v++;
+        }
+    } else if (warp == 1 && lane == 0 && N > 0) {
+        const uint32_t idKK = idesc_f16(bf16, 128, 128, false, false);
+        const uint32_t idKN = idesc_f16(bf16, 128, 128, false, true);
+        const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV),
+                       aX = smem_addr(sX);
+        bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteDqMma);
+        for (int c = 0; ok && c < N; ++c) {
+            const int s = c & 1;
+            if (!(ok = mbar_wait(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (!(ok = mbar_wait(b_vf, c & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (c > 0 && !(ok = mbar_wait(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            tc_fence_after();
+            issue_kk(tbase + 0, aQ, aK + s * kTile, idKK, false);  // S = Q K^T
+            issue_kk(tbase + 128, aO, aV, idKK, false);            // dP = dO V^T
+            mma_commit(b_sf);
+            mma_commit(b_ve);
+            mma_started = 1;
+            if (c > 0) {
+                const int sp = (c - 1) & 1;
+                if (!(ok = mbar_wait(b_dsf, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+                tc_fence_after();
+                issue_kn(tbase + 256, aX, aK + sp * kTile, idKN, c - 1 > 0);  // dQ += dS K
+                mma_commit(b_dq);
+                mma_commit(b_ke + sp);
+            }
+        }
+        if (ok) {
+            const int sp = (N - 1) & 1;
+            if (mbar_wait(b_dsf, (N - 1) & 1, s_abort, a.err, kSiteDqMma)) {
+                tc_fence_after();
+                issue_kn(tbase + 256, aX, aK + sp * kTile, idKN, N - 1 > 0);
+                mma_commit(b_dq);
+                mma_commit(b_ke + sp);
+            }
+        }
+    } else if (warp >= 4) {
+        const int r = (warp - 4) * 32 + lane;
+        const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        const bool row_ok = r < nrows;
+        const float l2 = row_ok && N > 0 ? a.lse[lse_off(p, b, h, row0 + r)] * kLog2e : INFINITY;
+        const float dvv = row_ok && N > 0 ? a.dvec[lse_off(p, b, h, row0 + r)] : 0.f;
+        bool ok = true;
+        for (int c = 0; c < N; ++c) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
+            if (!ok) break;
+            tc_fence_after();
+            const int valid = s_cval[c];
+            uint32_t dw[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tl + q4 * 32, sr);
+                tmem_ld32(tl + 128 + q4 * 32, dr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t2 = 0; t2 < 16; ++t2) {
+                    float dd[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int kk = q4 * 32 + t2 * 2 + e;
+                        const float pr = kk < valid ? ex2(fmaf(__uint_as_float(sr[t2 * 2 + e]), sl2, -l2)) : 0.f;
+                        dd[e] = pr * (__uint_as_float(dr[t2 * 2 + e]) - dvv);
+                    }
+                    dw[q4 * 16 + t2] = pack2<T>(dd[0], dd[1]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(b_sfree);
+            if (c > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(b_dq, (c - 1) & 1, s_abort, a.err, kSiteDqSoft));
+                if (!ok) break;
+            }
+            store_row_sw128(sX, r, dw);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_dsf);
+        }
+        if (ok && N > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_dq, (N - 1) & 1, s_abort, a.err, kSiteDqSoft));
+            if (ok) tc_fence_after();
+        }
+        const bool have = ok && N > 0;
+        const long long ro = tok_off(p, true, b, row0 + r, h);
+        T *dq = reinterpret_cast<T *>(a.dq) + ro;
+        const int qv = a.dpq ? q_valid(p, b, i) : 0;
+        const bool add_c = a.dpq && (half * 128 + r) < qv;
+        const float *cq = a.dpq ? a.dpq + qrow * 128 : nullptr;
+        const float inv = qv > 0 ? 1.f / (float)qv : 0.f;
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t o[32];
+            if (have) {
+                tmem_ld32(tl + 256 + q4 * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            if (!row_ok) continue;
+            uint32_t wv[16];
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2) {
+                float v0 = __uint_as_float(o[2 * e2]) * p.scale, v1 = __uint_as_float(o[2 * e2 + 1]) * p.scale;
+                if (add_c) {
+                    v0 += cq[q4 * 32 + 2 * e2] * inv;
+                    v1 += cq[q4 * 32 + 2 * e2 + 1] * inv;
+                }
+                wv[e2] = pack2<T>(v0, v1);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q4 * 32);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+        }
+    }
+
+    if (*s_abort) {
+        int never = 0;
+        if (warp == 0 && lane == 0) {
+            if (issued_q) mbar_wait(b_q, 0, &never, nullptr, 0, 200000000ull);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s]) mbar_wait(b_kf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+            if (issued_v) mbar_wait(b_vf, (issued_v - 1) & 1, &never, nullptr, 0, 200000000ull);
+        }
+        if (warp == 1 && lane == 0 && mma_started) {
+            mma_commit(b_fin);
+            mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// --------------------------------------------------- compression backward
+// dc_i = sum over the query rows of tile i of gate (*) dO (fp32, per dim).
+template <typename T>
+__global__ void __launch_bounds__(128) k_compress_dc(Prob p, const T *__restrict__ dO, const T *__restrict__ gate,
+                                                     float *__restrict__ dc) {
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, e = threadIdx.x;
+    const int rows = q_rows(p, b, i);
+    float acc = 0.f;
+    for (int t = 0; t < rows; ++t) {
+        const long long o = tok_off(p, true, b, i * p.tile_q + t, h) + e;
+        acc = fmaf(to_f<T>(gate[o]), to_f<T>(dO[o]), acc);
+    }
+    dc[(((long long)b * p.Hq + h) * p.nQ + i) * 128 + e] = acc;
+}
+
+// Per query tile: A_j (softmax over non-empty KV tiles of scale pq.pk_j),
+// dA_j = dc . pv_j, ds_j = A_j (dA_j - sum A dA); stores A and ds, and
+// dpq = scale sum_j ds_j pk_j.
+__global__ void __launch_bounds__(128) k_compress_rows(Prob p, const float *__restrict__ pq,
+                                                       const float *__restrict__ pk, const float *__restrict__ pv,
+                                                       const float *__restrict__ dc, float *__restrict__ A,
+                                                       float *__restrict__ ds, float *__restrict__ dpq) {
+    extern __shared__ float sh[];  // sA[nKV], sD[nKV]
+    float *sA = sh, *sD = sh + p.nKV;
+    __shared__ float spq[128], sdc[128], red[4];
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
+    spq[t] = pq[row * 128 + t];
+    sdc[t] = dc[row * 128 + t];
+    __syncthreads();
+    const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    float mx = -INFINITY;
+    for (int j = t; j < p.nKV; j += 128) {
+        float x = -INFINITY, da = 0.f;
+        if (kv_valid(p, b, j) > 0) {
+            float acc = 0.f, acc2 = 0.f;
+            for (int e = 0; e < 128; ++e) {
+                acc = fmaf(spq[e], pkh[(long long)j * 128 + e], acc);
+                acc2 = fmaf(sdc[e], pvh[(long long)j * 128 + e], acc2);
+            }
+            x = acc * p.scale;
+            da = acc2;
+        }
+        sA[j] = x;
+        sD[j] = da;
+        mx = fmaxf(mx, x);
+    }
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[w] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    float sum = 0.f;
+    for (int j = t; j < p.nKV; j += 128) {
+        const float ev = sA[j] == -INFINITY ? 0.f : __expf(sA[j] - mx);
+        sA[j] = ev;
+        sum += ev;
+    }
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) red[w] = sum;
+    __syncthreads();
+    sum = red[0] + red[1] + red[2] + red[3];
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    __syncthreads();
+    float sad = 0.f;
+    for (int j = t; j < p.nKV; j += 128) {
+        sA[j] *= inv;
+        sad += sA[j] * sD[j];
+    }
+    for (int off = 16; off > 0; off >>= 1) sad += __shfl_xor_sync(0xffffffffu, sad, off);
+    if (lane == 0) red[w] = sad;
+    __syncthreads();
+    sad = red[0] + red[1] + red[2] + red[3];
+    for (int j = t; j < p.nKV; j += 128) {
+        const float d = sA[j] * (sD[j] - sad);
+        sD[j] = d;
+        A[row * p.nKV + j] = sA[j];
+        ds[row * p.nKV + j] = d;
+    }
+    __syncthreads();
+    float acc = 0.f;
+    for (int j = 0; j < p.nKV; ++j) acc = fmaf(sD[j], pkh[(long long)j * 128 + t], acc);
+    dpq[row * 128 + t] = acc * p.scale;
+}
+
+// Per KV tile: dpv_j = sum_{h in group, i} A_ij dc_i and
+// dpk_j = scale sum_{h, i} ds_ij pq_i.
+__global__ void __launch_bounds__(128) k_compress_cols(Prob p, const float *__restrict__ pq,
+                                                       const float *__restrict__ dc, const float *__restrict__ A,
+                                                       const float *__restrict__ ds, float *__restrict__ dpk,
+                                                       float *__restrict__ dpv) {
+    const int j = blockIdx.x, hk = blockIdx.y, b = blockIdx.z, e = threadIdx.x, g = p.Hq / p.Hkv;
+    float ak = 0.f, av = 0.f;
+    for (int h = hk * g; h < hk * g + g; ++h) {
+        const long long base = ((long long)b * p.Hq + h) * p.nQ;
+        for (int i = 0; i < p.nQ; ++i) {
+            const long long row = base + i;
+            ak = fmaf(ds[row * p.nKV + j], pq[row * 128 + e], ak);
+            av = fmaf(A[row * p.nKV + j], dc[row * 128 + e], av);
+        }
+    }
+    const long long o = (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 + e;
+    dpk[o] = ak * p.scale;
+    dpv[o] = av;
+}
+
+}  // namespace
+
+cudaError_t launch_dvec(const Prob &p, const void *dO, const void *o, float *dvec, cudaStream_t s) {
+    const long long rows = (p.layout == L_TND ? (long long)p.Sq : (long long)p.B * p.Sq) * p.Hq;
+    if (rows == 0) return cudaSuccess;
+    prof_begin("bwd_dvec", s);
+    if (p.dtype == T_BF16)
+        k_dvec<__nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, (const __nv_bfloat16 *)dO,
+                                                                          (const __nv_bfloat16 *)o, dvec);
+    else
+        k_dvec<__half><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, dvec);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
+        return cudaErrorInvalidValue;
+    dim3 grid(p.nKV * (p.tile_kv / 128), p.Hkv, p.B);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_dkdv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem);
+        cudaFuncSetAttribute(k_dkdv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem);
+        attr = true;
+    }
+    prof_begin("bwd_dkdv", s);
+    if (p.dtype == T_BF16)
+        k_dkdv<__nv_bfloat16><<<grid, 256, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+    else
+        k_dkdv<__half><<<grid, 256, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
+        return cudaErrorInvalidValue;
+    dim3 grid(p.nQ * (p.tile_q / 128), p.Hq, p.B);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_dq<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem);
+        cudaFuncSetAttribute(k_dq<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem);
+        attr = true;
+    }
+    prof_begin("bwd_dq", s);
+    if (p.dtype == T_BF16)
+        k_dq<__nv_bfloat16><<<grid, 256, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+    else
+        k_dq<__half><<<grid, 256, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate, const float *pq, const float *pk,
+                                const float *pv, float *dc, float *A, float *ds, float *dpq, float *dpk,
+                                float *dpv, cudaStream_t s) {
+    dim3 gq(p.nQ, p.Hq, p.B), gk(p.nKV, p.Hkv, p.B);
+    prof_begin("compress_dc", s);
+    if (p.dtype == T_BF16)
+        k_compress_dc<__nv_bfloat16><<<gq, 128, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)gate, dc);
+    else
+        k_compress_dc<__half><<<gq, 128, 0, s>>>(p, (const __half *)dO, (const __half *)gate, dc);
+    prof_end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prof_begin("compress_rows", s);
+    k_compress_rows<<<gq, 128, sizeof(float) * 2 * p.nKV, s>>>(p, pq, pk, pv, dc, A, ds, dpq);
+    prof_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prof_begin("compress_cols", s);
+    k_compress_cols<<<gk, 128, 0, s>>>(p, pq, dc, A, ds, dpk, dpv);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
 }  // namespace vsa

@@ -51,7 +51,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // device status word records a failure anywhere in the grid; on a timeout
 // it raises *abort and records `site` in the device status word.
 // Returns false when the wait did not complete.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                        unsigned *err, unsigned site,
                                        uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;

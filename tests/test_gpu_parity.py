@@ -136,3 +136,63 @@ def test_forward_bhsd_equals_bshd_and_inference_equals_training():
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)          # inference == training
     assert torch.equal(out1, out3.transpose(1, 2)) and torch.equal(lse1, lse3)  # BHSD == BSHD
     assert torch.equal(out1, out4) and torch.equal(lse1, lse4)          # run to run
+
+
+def gated_cases():
+    kv = [256, 160, 64, 40, 256, 256, 160, 64, 256]
+    return [
+        Problem("gated-ragged-small", "bshd", 1, 4, 2, 128, 256, 256, 5, 9, q_var=kv[:5], kv_var=kv, topk=3,
+                gate="uniform_token_head", seed=31),
+        Problem("gated-bhsd-gqa", "bhsd", 2, 6, 3, 128, 256, 256, 3, 4, q_var=[256, 61, 199],
+                kv_var=[256, 173, 0, 79], topk=2, gate="randn01", seed=32),
+        tnd_problem("gated-tnd-topk", [300, 17, 129], [540, 23, 200], 4, 2, dtype="fp16", topk=2,
+                    gate="randn01", seed=33),
+    ]
+
+
+BWD_CASES = page_cases() + extra_cases() + gated_cases()
+
+
+def _bwd_check(p, t, plan, g, ref):
+    gate = g.get("gate")
+    out, lse, osp = plan.forward(g["q"], g["k"], g["v"], gate=gate)
+    dq, dk, dv = plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse, gate=gate)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    check_tol(f"{p.name} out", ref["out"], out.double().cpu().numpy(), OUT_TOL)
+    for n, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        check_tol(f"{p.name} {n}", ref[n], x.double().cpu().numpy(), GRAD_TOL)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("p", BWD_CASES, ids=lambda p: p.name)
+def test_backward_parity(p):
+    t = make_tensors(p)
+    plan, g = run_map(p, t)
+    ref = orc.run_full(p, t)
+    assert np.array_equal(plan.q_idx.cpu().numpy(), ref["q_idx"])
+    _bwd_check(p, t, plan, g, ref)
+
+
+@pytest.mark.parametrize("p", [config(2)] + [npu_problem(c) for c in load_golden("npu_tnd_cases.json")["cases"]],
+                         ids=lambda p: p.name)
+def test_backward_parity_varlen_mask(p):
+    t = make_tensors(p)
+    mask = make_mask(p)
+    plan = plan_for(p)
+    g = to_device(t)
+    plan.mask_to_index(torch.as_tensor(mask).cuda(), need_bwd_index=True)
+    ref = orc.run_full(p, t, mask=mask)
+    _bwd_check(p, t, plan, g, ref)
+
+
+def test_backward_bitwise_deterministic():
+    p = gated_cases()[0]
+    t = make_tensors(p)
+    plan, g = run_map(p, t)
+    out, lse, osp = plan.forward(g["q"], g["k"], g["v"], gate=g["gate"])
+    r1 = plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse, gate=g["gate"])
+    r2 = plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse, gate=g["gate"])
+    torch.cuda.synchronize()
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
