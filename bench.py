@@ -160,6 +160,9 @@ def ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     p = inputs.config(3)
+    if args.heads != p.Hq:  # smaller replica of the same workload (profiling captures)
+        p = inputs.Problem(p.name, p.layout, p.B, args.heads, args.heads, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV,
+                           q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, seed=p.seed)
     T = inputs.DTYPES[p.dtype]
     t = inputs.make_tensors(p, device=dev)
     q, k, v, dO = t["q"], t["k"], t["v"], t["dO"]
@@ -287,7 +290,7 @@ def ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "video-dit-76800: latent 20x48x80 tiled 4x8x8 -> 300 tiles, 76,800 tokens; "
-                               "B=1, H=40, D=128, bf16, BSHD; topk 30 (10% density)",
+                               f"B=1, H={p.Hq}, D=128, bf16, BSHD; topk 30 (10% density)",
                    "selected_pairs": pairs, "tflop_per_step": step_flops / 1e12,
                    "fwd_tflop_per_step": fwd_flops / 1e12,
                    "l2": "inputs larger than L2 (each of q, k, v, dO is 786 MB vs 126 MB L2); no flush",
@@ -313,6 +316,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=40, help="heads of the workload (40; fewer only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -63,48 +63,61 @@ __device__ __forceinline__ void named_sync_softmax() {  // the four softmax warp
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-// ------------------------------------------------------------------ dvec
-// Dvec_t = sum_d dO_t,d * O_t,d; one warp per query row.
+// ------------------------------------------------------------------ prep
+// Per query slot w of the padded tile layout [B, Hq, nQ * tile_q]:
+// lse2[w] = LSE * log2(e) and dvec[w] = sum_d dO_d O_d (rowsum(P dP) of the
+// softmax backward). Slots that are not query rows (past a varlen
+// sequence's end) get lse2 = +inf and dvec = 0, so P = 0 there. A half-warp
+// reads one 256-byte row (16 bytes per lane); each warp keeps four row
+// pairs in flight.
 template <typename T>
-__global__ void __launch_bounds__(256) k_dvec(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
-                                              float *__restrict__ dvec) {
-    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    long long rows_per_h;
-    int b, s, h;
-    if (p.layout == L_TND) {
-        rows_per_h = p.Sq;
-        if (w >= rows_per_h * p.Hq) return;
-        const int tok = (int)(w / p.Hq);
-        h = (int)(w % p.Hq);
-        // batch entry of token tok (binary search over cu_q)
-        int lo = 0, hi = p.B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.cu_q[mid] <= tok) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-        s = tok - p.cu_q[b];
-    } else {
-        if (w >= (long long)p.B * p.Sq * p.Hq) return;
-        if (p.layout == L_BSHD) {
-            h = (int)(w % p.Hq);
-            s = (int)((w / p.Hq) % p.Sq);
-            b = (int)(w / ((long long)p.Hq * p.Sq));
-        } else {
-            s = (int)(w % p.Sq);
-            h = (int)((w / p.Sq) % p.Hq);
-            b = (int)(w / ((long long)p.Hq * p.Sq));
+__global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
+                                                  const float *__restrict__ lse, float *__restrict__ lse2,
+                                                  float *__restrict__ dvec) {
+    const int per = p.nQ * p.tile_q;
+    const long long slots = (long long)p.B * p.Hq * per;
+    const int half = (threadIdx.x >> 4) & 1, hl = threadIdx.x & 15;
+    const long long wbase = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * 8;
+    uint4 av[4], cv[4];
+    bool ex[4];
+    long long lo[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const long long w = wbase + it * 2 + half;
+        ex[it] = false;
+        lo[it] = -1;
+        av[it] = make_uint4(0, 0, 0, 0);
+        cv[it] = make_uint4(0, 0, 0, 0);
+        if (w < slots) {
+            const int s = (int)(w % per), h = (int)((w / per) % p.Hq), b = (int)(w / ((long long)per * p.Hq));
+            ex[it] = p.layout == L_TND ? (s < p.cu_q[b + 1] - p.cu_q[b]) : true;
+            if (ex[it]) {
+                const long long o = tok_off(p, true, b, s, h) + hl * 8;
+                av[it] = __ldg(reinterpret_cast<const uint4 *>(dO + o));
+                cv[it] = __ldg(reinterpret_cast<const uint4 *>(O + o));
+                lo[it] = lse_off(p, b, h, s);
+            }
         }
     }
-    const long long o = tok_off(p, true, b, s, h) + lane * 4;
-    const uint2 a = __ldg(reinterpret_cast<const uint2 *>(dO + o));
-    const uint2 c = __ldg(reinterpret_cast<const uint2 *>(O + o));
-    const float2 a0 = unpack2<T>(a.x), a1 = unpack2<T>(a.y), c0 = unpack2<T>(c.x), c1 = unpack2<T>(c.y);
-    float acc = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) dvec[lse_off(p, b, h, s)] = acc;
+    for (int it = 0; it < 4; ++it) {
+        const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
+        const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 x = unpack2<T>(aw[u]), y = unpack2<T>(cw[u]);
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long w = wbase + it * 2 + half;
+        if (hl == 0 && w < slots) {
+            dvec[w] = ex[it] ? acc : 0.f;
+            lse2[w] = ex[it] ? lse[lo[it]] * kLog2e : INFINITY;
+        }
+    }
 }
 
 // ----------------------------------------------------------------- dK/dV
@@ -117,8 +130,9 @@ __global__ void __launch_bounds__(256) k_dvec(Prob p, const T *__restrict__ dO, 
 // P^T and dS^T take turns in one shared-memory tile. TMEM columns:
 // S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
 constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 4 * kTile, kDkOffX = 6 * kTile;
-constexpr int kDkOffCtl = 7 * kTile;
-constexpr size_t kDkSmem = 1024 + kDkOffCtl + 256;
+constexpr int kDkOffLd = 7 * kTile;             // per stage: lse2[128], dvec[128]
+constexpr int kDkOffCtl = kDkOffLd + 2 * 1024;
+constexpr size_t kDkSmem = kDkOffCtl + 256;
 
 struct WorkIter {
     int h, pos, end, sub, i, nsub;
@@ -157,9 +171,14 @@ __global__ void __launch_bounds__(256, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
            const BwdArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_error(a.err, 0x2FF);
+        return;
+    }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sX = sm + kDkOffX;
+    uint8_t *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
     uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_sfree = bars + 6;
     uint64_t *b_pf = bars + 7, *b_dsf = bars + 8, *b_dv = bars + 9, *b_dk = bars + 10, *b_fin = bars + 11;
@@ -235,7 +254,10 @@ __global__ void __launch_bounds__(256, 1)
             const int s = m & 1;
             if (m >= 2 && !mbar_wait(b_qe + s, ((m >> 1) - 1) & 1, s_abort, a.err, kSiteDkProd)) break;
             const int row = qb + w.i * p.tile_q + w.sub * 128;
-            mbar_expect_tx(b_qf + s, 2 * kTile);
+            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
+            mbar_expect_tx(b_qf + s, 2 * kTile + 1024);
+            bulk_load(sLd + s * 1024, a.lse2 + slot, 512, b_qf + s);
+            bulk_load(sLd + s * 1024 + 512, a.dvec + slot, 512, b_qf + s);
             tma_load_4d(sQ + s * kTile, &tq, b_qf + s, 0, row, w.h, bc);
             tma_load_4d(sQ + s * kTile + kBox, &tq, b_qf + s, 64, row, w.h, bc);
             tma_load_4d(sO + s * kTile, &tdo, b_qf + s, 0, row, w.h, bc);
@@ -287,18 +309,15 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
         const float sl2 = p.scale * kLog2e;
         const bool key_ok = u < kvalid;
-        WorkIter w;
-        bool more = M > 0 && work_first(p, a, b, h0, h_end, j, w);
         bool ok = true;
-        for (int m = 0; more && m < M; ++m) {
-            const int qrow0 = w.i * p.tile_q + w.sub * 128;  // within the batch entry
-            int nq = q_rows(p, b, w.i) - w.sub * 128;
-            nq = nq > 128 ? 128 : nq;
-            const float *lse_row = a.lse + lse_off(p, b, w.h, qrow0);
-            const float *dv_row = a.dvec + lse_off(p, b, w.h, qrow0);
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft));
+        for (int m = 0; m < M; ++m) {
+            const int st = m & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
+                                             mbar_wait(b_qf + st, (m >> 1) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
+            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024);
+            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512);
             uint32_t pw[64], dw[64];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -307,20 +326,20 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld32(tl + 128 + q4 * 32, dr);
                 tmem_wait_ld();
 #pragma unroll
-                for (int t2 = 0; t2 < 16; ++t2) {
-                    float pp[2], dd[2];
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 l4 = sl4[q4 * 8 + t4], d4 = sd4[q4 * 8 + t4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pp[4], dd[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = q4 * 32 + t2 * 2 + e;
-                        const bool on = key_ok && t < nq;
-                        const float l2 = on ? __ldg(lse_row + t) * kLog2e : 0.f;
-                        const float dvv = on ? __ldg(dv_row + t) : 0.f;
-                        const float pr = on ? ex2(fmaf(__uint_as_float(sr[t2 * 2 + e]), sl2, -l2)) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
                         pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(dr[t2 * 2 + e]) - dvv);
+                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
                     }
-                    pw[q4 * 16 + t2] = pack2<T>(pp[0], pp[1]);
-                    dw[q4 * 16 + t2] = pack2<T>(dd[0], dd[1]);
+                    pw[q4 * 16 + t4 * 2] = pack2<T>(pp[0], pp[1]);
+                    pw[q4 * 16 + t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
+                    dw[q4 * 16 + t4 * 2] = pack2<T>(dd[0], dd[1]);
+                    dw[q4 * 16 + t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
             }
             tc_fence_before();
@@ -339,7 +358,6 @@ __global__ void __launch_bounds__(256, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_dsf);
-            more = work_advance(p, a, b, h_end, j, w);
         }
         if (ok && M > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_dk, (M - 1) & 1, s_abort, a.err, kSiteDkSoft) &&
@@ -416,15 +434,19 @@ __global__ void __launch_bounds__(256, 1)
 // TMEM columns: S [0,128), dP [128,256), dQ [256,384).
 constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = 4 * kTile, kDqOffX = 5 * kTile;
 constexpr int kDqOffCtl = 6 * kTile;
-constexpr size_t kDqSmem = 1024 + kDqOffCtl + 256 + kMaxChunks * 6;
+constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks * 6;
 
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
     k_dq(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
          const BwdArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if ((smem_addr(sm) & 1023u) != 0) {
+        if (threadIdx.x == 0) set_error(a.err, 0x3FF);
+        return;
+    }
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV, *sX = sm + kDqOffX;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 3, *b_vf = bars + 5, *b_ve = bars + 6;
@@ -570,8 +592,9 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
         const float sl2 = p.scale * kLog2e;
         const bool row_ok = r < nrows;
-        const float l2 = row_ok && N > 0 ? a.lse[lse_off(p, b, h, row0 + r)] * kLog2e : INFINITY;
-        const float dvv = row_ok && N > 0 ? a.dvec[lse_off(p, b, h, row0 + r)] : 0.f;
+        const long long slot = ((long long)b * p.Hq + h) * p.nQ * p.tile_q + row0 + r;
+        const float l2 = N > 0 ? a.lse2[slot] : INFINITY;
+        const float dvv = N > 0 ? a.dvec[slot] : 0.f;
         bool ok = true;
         for (int c = 0; c < N; ++c) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
@@ -777,15 +800,17 @@ __global__ void __launch_bounds__(128) k_compress_cols(Prob p, const float *__re
 
 }  // namespace
 
-cudaError_t launch_dvec(const Prob &p, const void *dO, const void *o, float *dvec, cudaStream_t s) {
-    const long long rows = (p.layout == L_TND ? (long long)p.Sq : (long long)p.B * p.Sq) * p.Hq;
-    if (rows == 0) return cudaSuccess;
-    prof_begin("bwd_dvec", s);
+cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *lse2,
+                            float *dvec, cudaStream_t s) {
+    const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;
+    if (slots == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((slots + 63) / 64);
+    prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
-        k_dvec<__nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, (const __nv_bfloat16 *)dO,
-                                                                          (const __nv_bfloat16 *)o, dvec);
+        k_bwd_prep<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)o,
+                                                        lse, lse2, dvec);
     else
-        k_dvec<__half><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, dvec);
+        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, lse2, dvec);
     prof_end(s);
     return cudaGetLastError();
 }

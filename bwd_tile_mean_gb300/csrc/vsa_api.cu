@@ -140,7 +140,7 @@ vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var,
 }
 
 struct WsLayout {
-    size_t pq, pk, pv, c, dvec, dc, A, ds, dpq, dpk, dpv, total;
+    size_t pq, pk, pv, c, lse2, dvec, dc, A, ds, dpq, dpk, dpv, total;
 };
 
 WsLayout ws_layout(const Prob &p, bool gate) {
@@ -152,10 +152,11 @@ WsLayout ws_layout(const Prob &p, bool gate) {
         return o;
     };
     const size_t fq = (size_t)p.B * p.Hq * p.nQ * p.D * 4, fk = (size_t)p.B * p.Hkv * p.nKV * p.D * 4;
-    const size_t rows = p.layout == L_TND ? (size_t)p.Sq : (size_t)p.B * p.Sq;
+    const size_t slots = (size_t)p.B * p.Hq * p.nQ * p.tile_q;  // padded tile layout
     L.pq = take(fq);
     L.pk = take(fk);
-    L.dvec = take((size_t)p.Hq * rows * 4);
+    L.lse2 = take(slots * 4);
+    L.dvec = take(slots * 4);
     if (gate) {
         L.pv = take(fk);
         L.c = take(fq);
@@ -308,7 +309,6 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
     a.q = q;
     a.k = k;
     a.v = v;
-    a.lse = lse;
     a.q_idx = q_idx;
     a.q_cnt = q_cnt;
     a.cap = idx_cap;
@@ -318,9 +318,10 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
     a.dk = dk;
     a.dv = dv;
     a.err = at<unsigned>(workspace, 0);
-    float *dvec = at<float>(workspace, L.dvec);
+    float *dvec = at<float>(workspace, L.dvec), *lse2 = at<float>(workspace, L.lse2);
     a.dvec = dvec;
-    VSA_CUDA(launch_dvec(p, dO, o_sparse, dvec, s));
+    a.lse2 = lse2;
+    VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, lse2, dvec, s));
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
         VSA_CUDA(launch_pool(p, true, q, pq, s));

@@ -49,10 +49,14 @@ cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk,
                                 float *c, cudaStream_t s);
 
 // Backward pieces.
-cudaError_t launch_dvec(const Prob &p, const void *dO, const void *o, float *dvec, cudaStream_t s);
+// Backward preprocess: per query slot of the padded tile layout
+// [B, Hq, nQ * tile_q], lse2 = LSE * log2(e) and Dvec = dO . O (slots
+// past a varlen sequence's end get lse2 = +inf, Dvec = 0).
+cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *lse2,
+                            float *dvec, cudaStream_t s);
 struct BwdArgs {
     const void *dO, *q, *k, *v;
-    const float *lse, *dvec;
+    const float *lse2, *dvec;   // padded tile layout, see launch_bwd_prep
     const int *q_idx, *q_cnt;
     int cap;
     const int *kv_ptr, *kv_qidx;
