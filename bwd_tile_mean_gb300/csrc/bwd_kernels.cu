@@ -59,9 +59,22 @@ __device__ __forceinline__ void store_row_sw128(uint8_t *tile, int r, const uint
                 make_uint4(w[hf * 32 + u * 4], w[hf * 32 + u * 4 + 1], w[hf * 32 + u * 4 + 2], w[hf * 32 + u * 4 + 3]);
 }
 
-__device__ __forceinline__ void named_sync_softmax() {  // the four softmax warps only
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+// Writes half a row (64 16-bit values in 32 packed words, column half ch)
+// of a K-major 128-byte-swizzled [128 x 128] tile: exactly one 64-column box.
+__device__ __forceinline__ void store_half_sw128(uint8_t *tile, int r, int ch, const uint32_t (&w)[32]) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4 *>(tile + ch * kBox + sw128_off(r, u)) =
+            make_uint4(w[u * 4], w[u * 4 + 1], w[u * 4 + 2], w[u * 4 + 3]);
 }
+
+// Warp roles of the backward kernels: warps 0-7 compute the softmax
+// gradient, two warps per TMEM lane quarter (warp w owns lanes
+// 32*(w%4).. and column half w/4); warp 8 issues TMA copies; warp 9 owns
+// TMEM and issues the MMAs.
+constexpr int kBwdThreads = 320;
+constexpr int kSoftThreads = 256;
+constexpr int kProdWarp = 8, kMmaWarp = 9;
 
 // ------------------------------------------------------------------ prep
 // Per query slot w of the padded tile layout [B, Hq, nQ * tile_q]:
@@ -167,7 +180,7 @@ __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, in
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
            const BwdArgs a) {
@@ -206,9 +219,9 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(b_qe + s, 1);
         }
         mbar_init(b_sf, 1);
-        mbar_init(b_sfree, 128);
-        mbar_init(b_pf, 128);
-        mbar_init(b_dsf, 128);
+        mbar_init(b_sfree, kSoftThreads);
+        mbar_init(b_pf, kSoftThreads);
+        mbar_init(b_dsf, kSoftThreads);
         mbar_init(b_dv, 1);
         mbar_init(b_dk, 1);
         mbar_init(b_fin, 1);
@@ -228,7 +241,7 @@ __global__ void __launch_bounds__(256, 1)
         *s_nwork = n;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
@@ -240,7 +253,7 @@ __global__ void __launch_bounds__(256, 1)
     const bool bf16 = (p.dtype == T_BF16);
     int issued_kv = 0, issued[2] = {0, 0}, mma_started = 0;
 
-    if (warp == 0 && lane == 0 && M > 0) {
+    if (warp == kProdWarp && lane == 0 && M > 0) {
         // ------------------------------------------------------ producer
         mbar_expect_tx(b_kv, 2 * kTile);
         tma_load_4d(sK, &tk, b_kv, 0, kvb + key0, hk, bc);
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(256, 1)
             issued[s]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
-    } else if (warp == 1 && lane == 0 && M > 0) {
+    } else if (warp == kMmaWarp && lane == 0 && M > 0) {
         // ---------------------------------------------------- MMA issuer
         const uint32_t idKK = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idKN = idesc_f16(bf16, 128, 128, false, true);
@@ -303,10 +316,11 @@ __global__ void __launch_bounds__(256, 1)
                 mma_commit(b_qe + sp);
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp < 8) {
         // ------------------------------------------- softmax + epilogue
-        const int u = (warp - 4) * 32 + lane;  // key row within the chunk
-        const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+        const int lg = warp & 3, ch = warp >> 2;  // lane quarter, column half
+        const int u = lg * 32 + lane;            // key row within the chunk
+        const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
         const float sl2 = p.scale * kLog2e;
         const bool key_ok = u < kvalid;
         bool ok = true;
@@ -316,18 +330,18 @@ __global__ void __launch_bounds__(256, 1)
                                              mbar_wait(b_qf + st, (m >> 1) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024);
-            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512);
-            uint32_t pw[64], dw[64];
+            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
+            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
+            uint32_t pw[32], dw[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t sr[32], dr[32];
-                tmem_ld32(tl + q4 * 32, sr);
-                tmem_ld32(tl + 128 + q4 * 32, dr);
+                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
+                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
                 tmem_wait_ld();
 #pragma unroll
                 for (int t4 = 0; t4 < 8; ++t4) {
-                    const float4 l4 = sl4[q4 * 8 + t4], d4 = sd4[q4 * 8 + t4];
+                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
                     float pp[4], dd[4];
 #pragma unroll
@@ -336,10 +350,10 @@ __global__ void __launch_bounds__(256, 1)
                         pp[e] = pr;
                         dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
                     }
-                    pw[q4 * 16 + t4 * 2] = pack2<T>(pp[0], pp[1]);
-                    pw[q4 * 16 + t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
-                    dw[q4 * 16 + t4 * 2] = pack2<T>(dd[0], dd[1]);
-                    dw[q4 * 16 + t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
+                    pw[q2 * 16 + t4 * 2] = pack2<T>(pp[0], pp[1]);
+                    pw[q2 * 16 + t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
+                    dw[q2 * 16 + t4 * 2] = pack2<T>(dd[0], dd[1]);
+                    dw[q2 * 16 + t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
             }
             tc_fence_before();
@@ -348,13 +362,13 @@ __global__ void __launch_bounds__(256, 1)
                 ok = __all_sync(0xffffffffu, mbar_wait(b_dk, (m - 1) & 1, s_abort, a.err, kSiteDkSoft));
                 if (!ok) break;
             }
-            store_row_sw128(sX, u, pw);
+            store_half_sw128(sX, u, ch, pw);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_pf);
             ok = __all_sync(0xffffffffu, mbar_wait(b_dv, m & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
-            store_row_sw128(sX, u, dw);
+            store_half_sw128(sX, u, ch, dw);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_dsf);
@@ -366,22 +380,22 @@ __global__ void __launch_bounds__(256, 1)
         }
         const bool have = ok && M > 0;
         const bool row_ok = (p.layout == L_TND) ? key_ok : true;
-        const long long ro = tok_off(p, false, b, key0 + u, hk);
+        const long long ro = tok_off(p, false, b, key0 + u, hk) + ch * 64;
         T *dk = reinterpret_cast<T *>(a.dk) + ro;
         T *dv = reinterpret_cast<T *>(a.dv) + ro;
         const float inv = kvalid_tile > 0 ? 1.f / (float)kvalid_tile : 0.f;
-        const float *cpk = a.dpk ? a.dpk + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
-        const float *cpv = a.dpv ? a.dpv + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
+        const float *cpk = a.dpk ? a.dpk + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 + ch * 64 : nullptr;
+        const float *cpv = a.dpv ? a.dpv + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 + ch * 64 : nullptr;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {  // 0: dV (cols 256..), 1: dK (cols 384..)
             T *dst = which ? dk : dv;
             const float *cadd = which ? cpk : cpv;
             const float mul = which ? p.scale : 1.f;
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t o[32];
                 if (have) {
-                    tmem_ld32(tl + 256 + which * 128 + q4 * 32, o);
+                    tmem_ld32(tl + 256 + which * 128 + ch * 64 + q2 * 32, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -394,12 +408,12 @@ __global__ void __launch_bounds__(256, 1)
                     float v0 = key_ok ? __uint_as_float(o[2 * e2]) * mul : 0.f;
                     float v1 = key_ok ? __uint_as_float(o[2 * e2 + 1]) * mul : 0.f;
                     if (cadd && key_ok) {
-                        v0 += cadd[q4 * 32 + 2 * e2] * inv;
-                        v1 += cadd[q4 * 32 + 2 * e2 + 1] * inv;
+                        v0 += cadd[q2 * 32 + 2 * e2] * inv;
+                        v1 += cadd[q2 * 32 + 2 * e2 + 1] * inv;
                     }
                     wv[e2] = pack2<T>(v0, v1);
                 }
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + q2 * 32);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
             }
@@ -408,19 +422,19 @@ __global__ void __launch_bounds__(256, 1)
 
     if (*s_abort) {
         int never = 0;
-        if (warp == 0 && lane == 0) {
+        if (warp == kProdWarp && lane == 0) {
             if (issued_kv) mbar_wait(b_kv, 0, &never, nullptr, 0, 200000000ull);
             for (int s = 0; s < 2; ++s)
                 if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
-        if (warp == 1 && lane == 0 && mma_started) {
+        if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
             mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -437,7 +451,7 @@ constexpr int kDqOffCtl = 6 * kTile;
 constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks * 6;
 
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     k_dq(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
          const BwdArgs a) {
@@ -482,8 +496,8 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(b_vf, 1);
         mbar_init(b_ve, 1);
         mbar_init(b_sf, 1);
-        mbar_init(b_sfree, 128);
-        mbar_init(b_dsf, 128);
+        mbar_init(b_sfree, kSoftThreads);
+        mbar_init(b_dsf, kSoftThreads);
         mbar_init(b_dq, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -519,7 +533,7 @@ __global__ void __launch_bounds__(256, 1)
             total += __shfl_sync(0xffffffffu, inc, 31);
         }
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
@@ -531,7 +545,7 @@ __global__ void __launch_bounds__(256, 1)
     const bool bf16 = (p.dtype == T_BF16);
     int issued_q = 0, issued[2] = {0, 0}, issued_v = 0, mma_started = 0;
 
-    if (warp == 0 && lane == 0 && N > 0) {
+    if (warp == kProdWarp && lane == 0 && N > 0) {
         mbar_expect_tx(b_q, 2 * kTile);
         tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
         tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
@@ -552,7 +566,7 @@ __global__ void __launch_bounds__(256, 1)
             tma_load_4d(sV + kBox, &tv, b_vf, 64, kr, hk, bc);
             issued_v++;
         }
-    } else if (warp == 1 && lane == 0 && N > 0) {
+    } else if (warp == kMmaWarp && lane == 0 && N > 0) {
         const uint32_t idKK = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idKN = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV),
@@ -587,9 +601,10 @@ __global__ void __launch_bounds__(256, 1)
                 mma_commit(b_ke + sp);
             }
         }
-    } else if (warp >= 4) {
-        const int r = (warp - 4) * 32 + lane;
-        const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+    } else if (warp < 8) {
+        const int lg = warp & 3, ch = warp >> 2;  // lane quarter, column half
+        const int r = lg * 32 + lane;
+        const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
         const float sl2 = p.scale * kLog2e;
         const bool row_ok = r < nrows;
         const long long slot = ((long long)b * p.Hq + h) * p.nQ * p.tile_q + row0 + r;
@@ -600,24 +615,24 @@ __global__ void __launch_bounds__(256, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;
             tc_fence_after();
-            const int valid = s_cval[c];
-            uint32_t dw[64];
+            const int valid = s_cval[c] - ch * 64;  // valid keys within this column half
+            uint32_t dw[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t sr[32], dr[32];
-                tmem_ld32(tl + q4 * 32, sr);
-                tmem_ld32(tl + 128 + q4 * 32, dr);
+                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
+                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
                 tmem_wait_ld();
 #pragma unroll
                 for (int t2 = 0; t2 < 16; ++t2) {
                     float dd[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int kk = q4 * 32 + t2 * 2 + e;
+                        const int kk = q2 * 32 + t2 * 2 + e;
                         const float pr = kk < valid ? ex2(fmaf(__uint_as_float(sr[t2 * 2 + e]), sl2, -l2)) : 0.f;
                         dd[e] = pr * (__uint_as_float(dr[t2 * 2 + e]) - dvv);
                     }
-                    dw[q4 * 16 + t2] = pack2<T>(dd[0], dd[1]);
+                    dw[q2 * 16 + t2] = pack2<T>(dd[0], dd[1]);
                 }
             }
             tc_fence_before();
@@ -626,7 +641,7 @@ __global__ void __launch_bounds__(256, 1)
                 ok = __all_sync(0xffffffffu, mbar_wait(b_dq, (c - 1) & 1, s_abort, a.err, kSiteDqSoft));
                 if (!ok) break;
             }
-            store_row_sw128(sX, r, dw);
+            store_half_sw128(sX, r, ch, dw);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_dsf);
@@ -636,17 +651,17 @@ __global__ void __launch_bounds__(256, 1)
             if (ok) tc_fence_after();
         }
         const bool have = ok && N > 0;
-        const long long ro = tok_off(p, true, b, row0 + r, h);
+        const long long ro = tok_off(p, true, b, row0 + r, h) + ch * 64;
         T *dq = reinterpret_cast<T *>(a.dq) + ro;
         const int qv = a.dpq ? q_valid(p, b, i) : 0;
         const bool add_c = a.dpq && (half * 128 + r) < qv;
-        const float *cq = a.dpq ? a.dpq + qrow * 128 : nullptr;
+        const float *cq = a.dpq ? a.dpq + qrow * 128 + ch * 64 : nullptr;
         const float inv = qv > 0 ? 1.f / (float)qv : 0.f;
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t o[32];
             if (have) {
-                tmem_ld32(tl + 256 + q4 * 32, o);
+                tmem_ld32(tl + 256 + ch * 64 + q2 * 32, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -658,12 +673,12 @@ __global__ void __launch_bounds__(256, 1)
             for (int e2 = 0; e2 < 16; ++e2) {
                 float v0 = __uint_as_float(o[2 * e2]) * p.scale, v1 = __uint_as_float(o[2 * e2 + 1]) * p.scale;
                 if (add_c) {
-                    v0 += cq[q4 * 32 + 2 * e2] * inv;
-                    v1 += cq[q4 * 32 + 2 * e2 + 1] * inv;
+                    v0 += cq[q2 * 32 + 2 * e2] * inv;
+                    v1 += cq[q2 * 32 + 2 * e2 + 1] * inv;
                 }
                 wv[e2] = pack2<T>(v0, v1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q4 * 32);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q2 * 32);
 #pragma unroll
             for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
         }
@@ -671,20 +686,20 @@ __global__ void __launch_bounds__(256, 1)
 
     if (*s_abort) {
         int never = 0;
-        if (warp == 0 && lane == 0) {
+        if (warp == kProdWarp && lane == 0) {
             if (issued_q) mbar_wait(b_q, 0, &never, nullptr, 0, 200000000ull);
             for (int s = 0; s < 2; ++s)
                 if (issued[s]) mbar_wait(b_kf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
             if (issued_v) mbar_wait(b_vf, (issued_v - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
-        if (warp == 1 && lane == 0 && mma_started) {
+        if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
             mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -829,9 +844,9 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     }
     prof_begin("bwd_dkdv", s);
     if (p.dtype == T_BF16)
-        k_dkdv<__nv_bfloat16><<<grid, 256, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__nv_bfloat16><<<grid, kBwdThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
     else
-        k_dkdv<__half><<<grid, 256, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__half><<<grid, kBwdThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
     prof_end(s);
     return cudaGetLastError();
 }
@@ -850,9 +865,9 @@ cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     }
     prof_begin("bwd_dq", s);
     if (p.dtype == T_BF16)
-        k_dq<__nv_bfloat16><<<grid, 256, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__nv_bfloat16><<<grid, kBwdThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
     else
-        k_dq<__half><<<grid, 256, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__half><<<grid, kBwdThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
     prof_end(s);
     return cudaGetLastError();
 }
