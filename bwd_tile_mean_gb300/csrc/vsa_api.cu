@@ -352,6 +352,7 @@ const char *vsa_status_string(vsa_status st) {
         case VSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case VSA_ERR_CUDA: return "CUDA launch or runtime error";
         case VSA_ERR_DEVICE: return "a kernel reported a failed internal wait";
+        case VSA_ERR_SCRATCH: return "problem exceeds the fixed scratch of vsa_build_block_map_static";
     }
     return "unknown status";
 }

@@ -24,9 +24,10 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 STATUS = {0: "VSA_OK", 1: "VSA_ERR_NULL", 2: "VSA_ERR_SHAPE", 3: "VSA_ERR_DTYPE", 4: "VSA_ERR_LAYOUT",
           5: "VSA_ERR_UNSUPPORTED", 6: "VSA_ERR_MISSING_SEQLENS", 7: "VSA_ERR_WORKSPACE",
-          8: "VSA_ERR_CUDA", 9: "VSA_ERR_DEVICE"}
+          8: "VSA_ERR_CUDA", 9: "VSA_ERR_DEVICE", 10: "VSA_ERR_SCRATCH"}
 
-EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_mask_to_index", "vsa_fwd", "vsa_bwd",
+EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_static", "vsa_mask_to_index",
+           "vsa_fwd", "vsa_bwd",
            "vsa_status_string", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count")
 
@@ -65,6 +66,9 @@ def lib():
         L.vsa_build_block_map.restype = C.c_int
         L.vsa_build_block_map.argtypes = [C.POINTER(VsaDesc), P, P, P, P, C.c_int, C.c_int, P, P, P, C.c_int,
                                           P, P, P, C.c_size_t, P]
+        L.vsa_build_block_map_static.restype = C.c_int
+        L.vsa_build_block_map_static.argtypes = [C.POINTER(VsaDesc), P, P, P, P, C.c_int, C.c_int, P, P, P,
+                                                 C.c_int, P, P, P]
         L.vsa_mask_to_index.restype = C.c_int
         L.vsa_mask_to_index.argtypes = [C.POINTER(VsaDesc), P, P, P, C.c_int, P, P, C.c_int, P, P, P]
         L.vsa_fwd.restype = C.c_int
@@ -114,6 +118,15 @@ def vsa_build_block_map(desc, q, k, q_var, kv_var, topk, need_bwd_index, block_m
         C.byref(desc), _p(q), _p(k), _p(q_var), _p(kv_var), int(topk), int(bool(need_bwd_index)),
         _p(block_map), _p(q_idx), _p(q_cnt), int(idx_cap), _p(kv_ptr), _p(kv_qidx), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def vsa_build_block_map_static(desc, q, k, q_var, kv_var, topk, need_bwd_index, block_map, q_idx, q_cnt,
+                               idx_cap, kv_ptr, kv_qidx, stream=None):
+    """vsa_build_block_map without a workspace: for callers that cannot
+    allocate device memory (the scratch is a fixed array in the library)."""
+    _check("vsa_build_block_map_static", lib().vsa_build_block_map_static(
+        C.byref(desc), _p(q), _p(k), _p(q_var), _p(kv_var), int(topk), int(bool(need_bwd_index)),
+        _p(block_map), _p(q_idx), _p(q_cnt), int(idx_cap), _p(kv_ptr), _p(kv_qidx), _stream(stream)))
 
 
 def vsa_mask_to_index(desc, block_map, q_var, kv_var, need_bwd_index, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx,

@@ -79,7 +79,8 @@ typedef enum {
     VSA_ERR_MISSING_SEQLENS = 6, /* TND without both cu_seqlens_q and cu_seqlens_kv */
     VSA_ERR_WORKSPACE = 7,       /* workspace NULL, misaligned or smaller than required */
     VSA_ERR_CUDA = 8,            /* a CUDA runtime call or kernel launch failed */
-    VSA_ERR_DEVICE = 9           /* a kernel recorded a failed internal wait (see vsa_device_status) */
+    VSA_ERR_DEVICE = 9,          /* a kernel recorded a failed internal wait (see vsa_device_status) */
+    VSA_ERR_SCRATCH = 10         /* problem too large for vsa_build_block_map_static's fixed scratch */
 } vsa_status;
 
 typedef enum { VSA_LAYOUT_BHSD = 0, VSA_LAYOUT_BSHD = 1, VSA_LAYOUT_TND = 2 } vsa_layout;
@@ -126,6 +127,29 @@ vsa_status vsa_build_block_map(const vsa_desc *desc, const void *q, const void *
                                int need_bwd_index, uint8_t *block_map, int32_t *q_idx,
                                int32_t *q_cnt, int idx_cap, int32_t *kv_ptr, int32_t *kv_qidx,
                                void *workspace, size_t workspace_bytes, vsa_stream_t stream);
+
+/* vsa_build_block_map for callers that cannot allocate device memory.
+ * The pages have no counterpart: it exists for callers such as code that
+ * runs inside CUDA graph capture, custom allocators that forbid
+ * cudaMalloc, or runtimes that own all device memory and cannot hand the
+ * library a workspace. Same arguments, results and errors as
+ * vsa_build_block_map, minus the workspace: the scratch for the fp32 tile
+ * means lives in a fixed array inside libvsa.so (16 MiB, 4,194,304 floats,
+ * held on every GPU that loads the library until the process exits). A
+ * problem needs B*Hq*nQ*128 + B*Hkv*nKV*128 floats of it (plus alignment
+ * padding of at most 63 floats); larger problems return VSA_ERR_SCRATCH.
+ * No cudaMalloc, cudaFree or allocating library routine is called. The
+ * first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture. Every call shares the one array: calls whose
+ * kernels may overlap on the GPU (different streams, or several host
+ * threads) race on it and must be serialised by the caller. Nothing in the
+ * array needs clearing between calls: each call overwrites what it reads. */
+vsa_status vsa_build_block_map_static(const vsa_desc *desc, const void *q, const void *k,
+                                      const int32_t *q_var, const int32_t *kv_var, int topk,
+                                      int need_bwd_index, uint8_t *block_map, int32_t *q_idx,
+                                      int32_t *q_cnt, int idx_cap, int32_t *kv_ptr, int32_t *kv_qidx,
+                                      vsa_stream_t stream);
 
 /* Index step for a caller-given block map [B, Hq, nQ, nKV] uint8 (nonzero
  * = attend), as in [NPU-test] (block_sparse_mask) and [FA4-adapt]

@@ -1,0 +1,52 @@
+"""vsa_build_block_map_static: the block-map entry point for callers that
+cannot allocate device memory (code running under graph capture, custom
+allocators that forbid cudaMalloc, runtimes that own all device memory).
+Its scratch is a fixed array inside the library. It must give the same
+block map and indices as vsa_build_block_map, bit for bit, on two calls in
+a row (the array keeps the previous call's contents)."""
+import pytest
+import torch
+
+from bwd_tile_mean_gb300 import vsa
+from bwd_tile_mean_gb300.inputs import Problem, make_tensors
+from tests.helpers import plan_for, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _outputs(plan):
+    return [plan.block_map.clone(), plan.q_idx.clone(), plan.q_cnt.clone(), plan.kv_ptr.clone(),
+            plan.kv_qidx.clone()]
+
+
+def test_static_scratch_matches_workspace_entry_point_twice():
+    problems = [
+        Problem("noalloc-a", "bshd", 1, 4, 2, 128, 256, 256, 6, 9, q_var=[256, 61, 199, 256, 0, 256],
+                kv_var=[256, 173, 0, 79, 256, 256, 12, 256, 128], topk=3, seed=41),
+        Problem("noalloc-b", "bhsd", 2, 2, 2, 128, 128, 128, 5, 7, q_var=[128] * 5,
+                kv_var=[128, 5, 128, 0, 77, 128, 1], topk=2, seed=42, dtype="fp16"),
+    ]
+    for p in problems:  # two calls in a row, on different problems, reuse the array
+        t = to_device(make_tensors(p))
+        ref = plan_for(p)
+        ref.build_block_map(t["q"], t["k"], p.topk, need_bwd_index=True)
+        want = _outputs(ref)
+        for _ in range(2):
+            got = plan_for(p)
+            vsa.vsa_build_block_map_static(got.desc, t["q"], t["k"], got.q_var, got.kv_var, p.topk, True,
+                                           got.block_map, got.q_idx, got.q_cnt, got.idx_cap, got.kv_ptr,
+                                           got.kv_qidx)
+            torch.cuda.synchronize()
+            for a, b in zip(want, _outputs(got)):
+                assert torch.equal(a, b)
+
+
+def test_static_scratch_rejects_problems_beyond_its_size():
+    p = Problem("too-big", "bshd", 1, 64, 64, 128, 256, 256, 300, 300, q_var=[256] * 300, kv_var=[256] * 300,
+                topk=4)
+    plan = plan_for(p)
+    q = torch.zeros(p.shape(True), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(vsa.VsaError) as e:
+        vsa.vsa_build_block_map_static(plan.desc, q, q, plan.q_var, plan.kv_var, p.topk, False, plan.block_map,
+                                       plan.q_idx, plan.q_cnt, plan.idx_cap, None, None)
+    assert e.value.code == 10
