@@ -47,6 +47,17 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x, world_size, device):
+    """Max of a per-rank float over all ranks (identity on one rank)."""
+    if world_size == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -187,11 +198,7 @@ def ours(args):
         torch.cuda.synchronize(dev)
 
     def max_over_ranks(x):
-        if ws == 1:
-            return x
-        tt = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        return float(tt.item())
+        return reduce_max(x, ws, dev)
 
     for _ in range(args.warmup):
         step(q, k, v, dO)

@@ -46,7 +46,9 @@ def test_workspace_size(L):
     assert vsa.vsa_workspace_size(desc(Hq=3, Hkv=2), False) == 0
 
 
-FAKE = C.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced: validation fails first
+# 16-byte aligned and never dereferenced: every call below fails host
+# validation before any CUDA call, so this file is safe on a GPU machine too.
+FAKE = C.c_void_p(1 << 20)
 
 
 def fwd(L, d, **kw):
@@ -77,3 +79,6 @@ def test_host_validation_errors(L):
                                  FAKE, 1 << 30, None) == 1   # bwd index needs kv_ptr / kv_qidx
     assert L.vsa_mask_to_index(C.byref(desc()), FAKE, None, FAKE, 0, FAKE, FAKE, 3, None, None, None) == 2
     assert L.vsa_status_string(5).decode().startswith("unsupported")
+    big = desc(nKV=4000, Skv=4000 * 256)
+    assert L.vsa_build_block_map(C.byref(big), FAKE, FAKE, FAKE, FAKE, 2, 0, FAKE, FAKE, FAKE, 2, None, None,
+                                 FAKE, 1 << 40, None) == 5   # nKV past the selection kernel limit
