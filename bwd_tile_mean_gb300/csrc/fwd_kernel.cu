@@ -10,21 +10,26 @@
 // FastVideo test_vsa256_backward.py (gated compression composes
 // out = sparse_out + gate * compress_out without touching sparse_out).
 //
-// One CTA computes 128 query rows (half of a 256-token video tile, or one
-// 128-token block) of one head against its list of selected KV tiles, cut
-// into 128-key chunks (chunks without valid keys are skipped). Warp roles:
-//   warp 0      builds the chunk list, then one lane issues TMA loads
-//               (Q once; K and V per chunk, double-buffered);
-//   warp 1      allocates TMEM, then one lane issues the MMAs:
-//               S_c = Q K_c^T into one of two TMEM S buffers, and
-//               O += P_c V_c into the TMEM O accumulator;
-//   warps 4..7  one thread per query row: read S_c from TMEM, mask keys past
-//               the chunk's valid count, online softmax in the exp2 domain
-//               (rescaling O in TMEM only when the running max grows by more
-//               than 2^8), write P_c (16-bit) to shared memory for the PV
-//               MMA; finally normalise O, add gate * c when gated, and write
-//               O and the LSE.
-// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256,384).
+// One CTA computes one query tile: two groups of 128 rows (A and B; the
+// two halves of a 256-token video tile, or a single group for 128-token
+// tiles) of one head against the tile's selected KV tiles, cut into
+// 128-key chunks (chunks without valid keys are skipped). Both groups share
+// every K/V chunk. Warp roles:
+//   warps 0-3   softmax of group A, one thread per query row;
+//   warps 4-7   softmax of group B;
+//   warp 8      builds the chunk list, then one lane issues TMA loads
+//               (Q of both groups once; K and V per chunk, two stages);
+//   warp 9      allocates TMEM, then one lane issues the MMAs.
+// Per chunk c the MMAs go S_A(c) = Q_A K_c^T, O_B += P_B(c-1) V_(c-1),
+// S_B(c) = Q_B K_c^T, O_A += P_A(c) V_c, so each group's softmax runs while
+// the tensor core works for the other group. The softmax reads S from
+// TMEM twice (row max, then probabilities), masks keys past the chunk's
+// valid count, keeps a running max in the exp2 domain (rescaling O in TMEM
+// only when the max grows by more than 2^8), and writes P back into the
+// first 64 columns of its S buffer as packed 16-bit pairs; the PV MMA reads
+// P from TMEM as its A operand. The epilogue normalises O, adds gate * c
+// when gated, and writes O and the LSE.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "sm103_ptx.cuh"
 #include "vsa_internal.h"
 
@@ -35,9 +40,11 @@ namespace {
 
 constexpr int kTile = 32 * 1024;  // one [128 x 128] 16-bit tile = two 64-column TMA boxes
 constexpr int kBox = 16 * 1024;
-constexpr int kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffP = 5 * kTile, kOffCtl = 6 * kTile;
+constexpr int kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile, kOffCtl = 6 * kTile;
 constexpr int kCtlBytes = 256 + kMaxChunks * 4 + kMaxChunks * 2;
-constexpr size_t kFwdSmem = 1024 + kOffCtl + kCtlBytes;
+constexpr size_t kFwdSmem = kOffCtl + kCtlBytes;
+constexpr int kFwdThreads = 320;
+constexpr int kFwdProdWarp = 8, kFwdMmaWarp = 9;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -54,46 +61,52 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t aQ, uint32_t aK, u
         mma_f16_ss(d, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), idesc, kk > 0);
     }
 }
-// O += P V: A = P (K-major over keys), B = V [keys x D] read MN-major
-// (D contiguous): 64-wide D halves are LBO = 16 KB apart, 8-key row groups
-// SBO = 1 KB apart; each K = 16 step advances 16 keys = 2 KB.
-__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t aP, uint32_t aV, uint32_t idesc, bool acc) {
+// O += P V: A = P in TMEM (128 keys = 64 packed columns, 8 per K = 16
+// step), B = V [keys x D] read MN-major (D contiguous): 64-wide D halves
+// are LBO = 16 KB apart, 8-key row groups SBO = 1 KB apart; each K = 16
+// step advances 16 keys = 2 KB.
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t aV, uint32_t idesc, bool acc) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t offp = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_f16_ss(d, sdesc_sw128(aP + offp, 16, 1024), sdesc_sw128(aV + kk * 2048, kBox, 1024), idesc,
-                   (acc || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < 8; ++kk)
+        mma_f16_ts(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
           const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sQ = sm + kOffQ, *sK = sm + kOffK, *sV = sm + kOffV, *sP = sm + kOffP;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_error(a.err, 0x1FF);
+        return;
+    }
+    uint8_t *sQ = sm + kOffQ, *sK = sm + kOffK, *sV = sm + kOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_vf = bars + 3, *b_ke = bars + 5, *b_sf = bars + 7;
-    uint64_t *b_pf = bars + 9, *b_od = bars + 10, *b_fin = bars + 11;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *b_pf = bars + 9, *b_od = bars + 11, *b_fin = bars + 13;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 14);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     int *s_crow = reinterpret_cast<int *>(sm + kOffCtl + 256);
     short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int subs = p.tile_q >> 7;
-    const int i = blockIdx.x / subs, half = blockIdx.x % subs;
-    const int h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
-    const int row0 = i * p.tile_q + half * 128;
-    int nrows = 128;
-    if (p.layout == L_TND) {
-        nrows = (p.cu_q[b + 1] - p.cu_q[b]) - row0;
-        if (nrows <= 0) return;  // whole CTA outside its sequence
-        nrows = nrows > 128 ? 128 : nrows;
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    // rows of each 128-row group (0 if the group does not exist)
+    int nrows[2];
+    for (int g = 0; g < 2; ++g) {
+        const int r0 = i * p.tile_q + g * 128;
+        int n = (g * 128 < p.tile_q) ? 128 : 0;
+        if (p.layout == L_TND && n > 0) {
+            n = (p.cu_q[b + 1] - p.cu_q[b]) - r0;
+            n = n < 0 ? 0 : (n > 128 ? 128 : n);
+        }
+        nrows[g] = n;
     }
-    const int qrc = (p.layout == L_TND ? p.cu_q[b] : 0) + row0;
+    if (nrows[0] == 0) return;  // the whole tile lies outside its sequence
+    const bool has_b = nrows[1] > 0;
+    const int qbase = (p.layout == L_TND ? p.cu_q[b] : 0) + i * p.tile_q;
     const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0);
     const int bc = (p.layout == L_TND ? 0 : b);
     const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
@@ -105,14 +118,14 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(b_vf + s, 1);
             mbar_init(b_ke + s, 1);
             mbar_init(b_sf + s, 1);
+            mbar_init(b_pf + s, 128);
+            mbar_init(b_od + s, 1);
         }
-        mbar_init(b_pf, 128);
-        mbar_init(b_od, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == kFwdProdWarp) {
         // chunk list: (KV row start within the batch entry, valid keys)
         const int cnt = a.q_cnt[qrow];
         const int *idx = a.q_idx + qrow * a.cap;
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(256, 1)
             total += __shfl_sync(0xffffffffu, inc, 31);
         }
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
-    } else if (warp == 1) {
+    } else if (warp == kFwdMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
@@ -155,14 +168,16 @@ __global__ void __launch_bounds__(256, 1)
     const bool bf16 = (p.dtype == T_BF16);
     int issued_q = 0, issued[2] = {0, 0}, mma_started = 0;
 
-    if (warp == 0 && lane == 0 && N > 0) {
+    if (warp == kFwdProdWarp && lane == 0 && N > 0) {
         // ---------------------------------------------------- TMA producer
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
-        mbar_expect_tx(b_q, kTile);
-        tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
-        tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
+        mbar_expect_tx(b_q, has_b ? 2 * kTile : kTile);
+        for (int g = 0; g < (has_b ? 2 : 1); ++g) {
+            tma_load_4d(sQ + g * kTile, &tq, b_q, 0, qbase + g * 128, h, bc);
+            tma_load_4d(sQ + g * kTile + kBox, &tq, b_q, 64, qbase + g * 128, h, bc);
+        }
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
             const int s = c & 1;
@@ -176,68 +191,73 @@ __global__ void __launch_bounds__(256, 1)
             tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
             issued[s]++;
         }
-    } else if (warp == 1 && lane == 0 && N > 0) {
+    } else if (warp == kFwdMmaWarp && lane == 0 && N > 0) {
         // ----------------------------------------------------- MMA issuer
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idO = idesc_f16(bf16, 128, 128, false, true);
-        const uint32_t aQ = smem_addr(sQ), aP = smem_addr(sP), aK = smem_addr(sK), aV = smem_addr(sV);
-        bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteMma) && mbar_wait(b_kf, 0, s_abort, a.err, kSiteMma);
-        if (ok) {
-            tc_fence_after();
-            issue_qk(tbase, aQ, aK, idS);
-            mma_commit(b_sf);
-            mma_started = 1;
-        }
+        const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
+        const uint32_t tS[2] = {tbase, tbase + 128}, tO[2] = {tbase + 256, tbase + 384};
+        bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteMma);
         for (int c = 0; ok && c < N; ++c) {
-            if (c + 1 < N) {
-                const int s1 = (c + 1) & 1;
-                if (!(ok = mbar_wait(b_kf + s1, ((c + 1) >> 1) & 1, s_abort, a.err, kSiteMma))) break;
-                tc_fence_after();
-                issue_qk(tbase + s1 * 128, aQ, aK + s1 * kTile, idS);
-                mma_commit(b_sf + s1);
-            }
-            if (!(ok = mbar_wait(b_pf, c & 1, s_abort, a.err, kSiteMma))) break;
-            if (!(ok = mbar_wait(b_vf + (c & 1), (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
+            const int s = c & 1, sp = (c - 1) & 1;
+            if (!(ok = mbar_wait(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
             tc_fence_after();
-            issue_pv(tbase + 256, aP, aV + (c & 1) * kTile, idO, c > 0);
-            mma_commit(b_od);
-            mma_commit(b_ke + (c & 1));
+            issue_qk(tS[0], aQ, aK + s * kTile, idS);  // S_A(c); P_A(c-1) was consumed by PV_A(c-1)
+            mma_commit(b_sf + 0);
+            mma_started = 1;
+            if (has_b) {
+                if (c > 0) {
+                    if (!(ok = mbar_wait(b_pf + 1, (c - 1) & 1, s_abort, a.err, kSiteMma))) break;
+                    tc_fence_after();
+                    issue_pv(tO[1], tS[1], aV + sp * kTile, idO, c - 1 > 0);  // O_B += P_B(c-1) V_(c-1)
+                    mma_commit(b_od + 1);
+                    mma_commit(b_ke + sp);
+                }
+                issue_qk(tS[1], aQ + kTile, aK + s * kTile, idS);  // S_B(c)
+                mma_commit(b_sf + 1);
+            }
+            if (!(ok = mbar_wait(b_pf + 0, c & 1, s_abort, a.err, kSiteMma))) break;
+            if (!(ok = mbar_wait(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
+            tc_fence_after();
+            issue_pv(tO[0], tS[0], aV + s * kTile, idO, c > 0);  // O_A += P_A(c) V_c
+            mma_commit(b_od + 0);
+            if (!has_b) mma_commit(b_ke + s);
         }
-    } else if (warp >= 4) {
+        if (ok && has_b) {
+            const int sp = (N - 1) & 1;
+            if (mbar_wait(b_pf + 1, (N - 1) & 1, s_abort, a.err, kSiteMma)) {
+                tc_fence_after();
+                issue_pv(tO[1], tS[1], aV + sp * kTile, idO, N - 1 > 0);
+                mma_commit(b_od + 1);
+                mma_commit(b_ke + sp);
+            }
+        }
+    } else if (warp < 8 && (warp < 4 || has_b)) {
         // -------------------------------------------- softmax + epilogue
-        const int r = (warp - 4) * 32 + lane;
-        const uint32_t tl = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+        const int g = warp >> 2, lg = warp & 3;
+        const int r = lg * 32 + lane;
+        const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
+        const uint32_t cS = g * 128, cO = 256 + g * 128;
         const float sl2 = p.scale * kLog2e;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int c = 0; c < N; ++c) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + (c & 1), (c >> 1) & 1, s_abort, a.err, kSiteSoft));
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + g, c & 1, s_abort, a.err, kSiteSoft));
             if (!ok) break;
             tc_fence_after();
-            float x[128];
+            const int valid = s_cval[c];
+            // pass 1: row max of the (masked) scaled scores
+            float mx = -INFINITY;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t rr[32];
-                tmem_ld32(tl + (c & 1) * 128 + q4 * 32, rr);
+                tmem_ld32(tl + cS + q4 * 32, rr);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[q4 * 32 + j] = __uint_as_float(rr[j]);
+                for (int j = 0; j < 32; ++j)
+                    if (valid >= 128 || q4 * 32 + j < valid) mx = fmaxf(mx, __uint_as_float(rr[j]));
             }
-            const int valid = s_cval[c];
-            float mx = -INFINITY;
-            if (valid >= 128) {
-#pragma unroll
-                for (int j = 0; j < 128; ++j) {
-                    x[j] *= sl2;
-                    mx = fmaxf(mx, x[j]);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 128; ++j) {
-                    x[j] = j < valid ? x[j] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, x[j]);
-                }
-            }
+            mx *= sl2;
             float alpha = 1.f;
             bool resc = false;
             if (c == 0) {
@@ -247,18 +267,28 @@ __global__ void __launch_bounds__(256, 1)
                 m_ref = mx;
                 resc = true;
             }
-            l *= alpha;
-            uint32_t pk[64];
+            // pass 2: probabilities, packed to 16 bits into S's first 64 columns
             float ls = 0.f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float p0 = ex2(x[2 * j] - m_ref), p1 = ex2(x[2 * j + 1] - m_ref);
-                ls += p0 + p1;
-                pk[j] = pack2<T>(p0, p1);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t rr[32];
+                tmem_ld32(tl + cS + q4 * 32, rr);
+                tmem_wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = q4 * 32 + 2 * j;
+                    const bool v0 = valid >= 128 || c0 < valid, v1 = valid >= 128 || c0 + 1 < valid;
+                    const float p0 = v0 ? ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -m_ref)) : 0.f;
+                    const float p1 = v1 ? ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -m_ref)) : 0.f;
+                    ls += p0 + p1;
+                    w[j] = pack2<T>(p0, p1);
+                }
+                tmem_st16(tl + cS + q4 * 16, w);
             }
-            l += ls;
+            l = l * alpha + ls;
             if (c > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(b_od, (c - 1) & 1, s_abort, a.err, kSiteSoft));
+                ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (c - 1) & 1, s_abort, a.err, kSiteSoft));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -266,38 +296,27 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t o[32];
-                    tmem_ld32(tl + 256 + q4 * 32, o);
+                    tmem_ld32(tl + cO + q4 * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                    tmem_st32(tl + 256 + q4 * 32, o);
+                    tmem_st32(tl + cO + q4 * 32, o);
                 }
-                tmem_wait_st();
             }
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint4 v;
-                    v.x = pk[hf * 32 + u * 4 + 0];
-                    v.y = pk[hf * 32 + u * 4 + 1];
-                    v.z = pk[hf * 32 + u * 4 + 2];
-                    v.w = pk[hf * 32 + u * 4 + 3];
-                    *reinterpret_cast<uint4 *>(sP + hf * kBox + sw128_off(r, u)) = v;
-                }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_pf);
+            mbar_arrive(b_pf + g);
         }
         if (ok && N > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_od, (N - 1) & 1, s_abort, a.err, kSiteEpi));
+            ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (N - 1) & 1, s_abort, a.err, kSiteEpi));
             if (ok) tc_fence_after();
         }
         const bool have = ok && N > 0;
         const float inv_l = have ? 1.f / l : 0.f;
         const float lse_v = have ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-        const bool row_ok = r < nrows;
-        const long long ro = tok_off(p, true, b, row0 + r, h);
+        const bool row_ok = r < nrows[g];
+        const int row = i * p.tile_q + g * 128 + r;  // within the batch entry
+        const long long ro = tok_off(p, true, b, row, h);
         T *osp = a.o_sparse ? reinterpret_cast<T *>(a.o_sparse) + ro : nullptr;
         T *out = reinterpret_cast<T *>(a.out) + ro;
         const T *gt = a.gate ? reinterpret_cast<const T *>(a.gate) + ro : nullptr;
@@ -306,7 +325,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t o[32];
             if (have) {
-                tmem_ld32(tl + 256 + q4 * 32, o);
+                tmem_ld32(tl + cO + q4 * 32, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -345,7 +364,7 @@ __global__ void __launch_bounds__(256, 1)
                 for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             }
         }
-        if (row_ok && a.lse) a.lse[lse_off(p, b, h, row0 + r)] = lse_v;
+        if (row_ok && a.lse) a.lse[lse_off(p, b, h, row)] = lse_v;
     }
 
     // ------------------------------------------------------------ teardown
@@ -353,7 +372,7 @@ __global__ void __launch_bounds__(256, 1)
         // Drain what this CTA started before leaving: outstanding TMA copies
         // (producer) and MMAs (issuer), each with a bounded wait.
         int never = 0;
-        if (warp == 0 && lane == 0) {
+        if (warp == kFwdProdWarp && lane == 0) {
             if (issued_q) mbar_wait(b_q, 0, &never, nullptr, 0, 200000000ull);
             for (int s = 0; s < 2; ++s)
                 if (issued[s]) {
@@ -361,14 +380,14 @@ __global__ void __launch_bounds__(256, 1)
                     mbar_wait(b_vf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
                 }
         }
-        if (warp == 1 && lane == 0 && mma_started) {
+        if (warp == kFwdMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
             mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kFwdMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -437,7 +456,7 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
         !make_tmap_rows(&tv, p, false, a.v, p.Hkv))
         return cudaErrorInvalidValue;
-    dim3 grid(p.nQ * (p.tile_q / 128), p.Hq, p.B);
+    dim3 grid(p.nQ, p.Hq, p.B);
     if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
     static bool attr = false;
     if (!attr) {
@@ -447,9 +466,9 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     }
     prof_begin("fwd_attn", s);
     if (p.dtype == T_BF16)
-        k_fwd<__nv_bfloat16><<<grid, 256, kFwdSmem, s>>>(tq, tk, tv, p, a);
+        k_fwd<__nv_bfloat16><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a);
     else
-        k_fwd<__half><<<grid, 256, kFwdSmem, s>>>(tq, tk, tv, p, a);
+        k_fwd<__half><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a);
     prof_end(s);
     return cudaGetLastError();
 }

@@ -66,7 +66,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 4D map (D, S, H, B) over a q- or kv-shaped 16-bit tensor; box = 64 dims x
 // 128 tokens of one head, 128-byte swizzle (the operand layout the tcgen05
 // descriptors expect). TND maps (D, T, H, 1).
-bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *base, int H) {
+bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *base, int H, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es = 2, S = (cuuint64_t)(q_side ? p.Sq : p.Skv), D = (cuuint64_t)p.D;
@@ -81,7 +81,7 @@ bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *ba
         strides[1] = D * es;
         strides[2] = S * H * D * es;
     }
-    cuuint32_t box[4] = {64, 128, 1, 1}, estr[4] = {1, 1, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1}, estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, p.dtype == T_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -300,7 +300,7 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (gate && !aligned16(gate)))
         return VSA_ERR_LAYOUT;
     if (idx_cap < 1 || idx_cap > p.nKV) return VSA_ERR_SHAPE;
-    if ((long long)idx_cap * (p.tile_kv / 128) > kMaxChunks) return VSA_ERR_UNSUPPORTED;
+    if ((long long)idx_cap * (p.tile_kv / 64) > kMaxChunks64) return VSA_ERR_UNSUPPORTED;
     VSA_TRY(check_ws(p, gate != nullptr, workspace, workspace_bytes));
     const WsLayout L = ws_layout(p, gate != nullptr);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

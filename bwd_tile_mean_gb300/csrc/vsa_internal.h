@@ -28,8 +28,10 @@ cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int
 
 // Largest nKV the selection kernel handles (its shared-memory score rows).
 constexpr int kMaxSelectKV = 3072;
-// Largest number of 128-key chunks one query tile may visit.
+// Largest number of 128-key chunks one query tile may visit (forward), and
+// of 64-key chunks (dQ pass).
 constexpr int kMaxChunks = 1024;
+constexpr int kMaxChunks64 = 2048;
 
 // Forward attention (tcgen05). out / o_sparse / gate / c as in vsa_fwd.
 struct FwdArgs {
@@ -72,7 +74,9 @@ cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate,
                                 const float *pk, const float *pv, float *dc, float *A, float *ds,
                                 float *dpq, float *dpk, float *dpv, cudaStream_t s);
 
-// Tensor-map encoding (driver entry point fetched through the runtime).
-bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *base, int heads);
+// Tensor-map encoding (driver entry point fetched through the runtime):
+// boxes of 64 head dims x box_rows tokens of one head, 128-byte swizzle.
+bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *base, int heads,
+                    int box_rows = 128);
 
 }  // namespace vsa
