@@ -91,48 +91,50 @@ __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ 
 }
 
 // ----------------------------------------------------------- MMA helpers
-constexpr int kHalf = 16 * 1024;  // one [64 x 128] 16-bit tile = two 64-column boxes of 8 KB
-constexpr int kBox64 = 8 * 1024;
+// Measured on GB300 (all SMs busy, M = 128, K = 16 per instruction): an
+// MMA with N = 64 takes about as long as one with N = 128, so every MMA
+// here uses N = 128 (A and B from shared memory, or A from TMEM).
 
-// D = A B^T, A [128 x 128] and B [n x 128] K-major 128-byte-swizzled tiles
-// (64-column boxes boxA / boxB bytes apart); 8 MMAs of K = 16.
-__device__ __forceinline__ void issue_ss(uint32_t d, uint32_t aA, uint32_t aB, uint32_t idesc, uint32_t boxA,
-                                         uint32_t boxB) {
+// D = A B^T, A and B [128 x 128] K-major 128-byte-swizzled tiles (two
+// 64-column boxes 16 KB apart); 8 MMAs of K = 16.
+__device__ __forceinline__ void issue_ss(uint32_t d, uint32_t aA, uint32_t aB, uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t o = (kk & 3) * 32;
-        mma_f16_ss(d, sdesc_sw128(aA + (kk >> 2) * boxA + o, 16, 1024), sdesc_sw128(aB + (kk >> 2) * boxB + o, 16, 1024),
-                   idesc, kk > 0);
+        const uint32_t o = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_f16_ss(d, sdesc_sw128(aA + o, 16, 1024), sdesc_sw128(aB + o, 16, 1024), idesc, kk > 0);
     }
 }
-// D (+)= A B with A in TMEM (packed 16-bit pairs, 8 columns per K = 16)
-// and B [K = 64 rows x N = 128] stored row-major (N contiguous, two 64-
-// column boxes of 8 KB), read MN-major; 4 MMAs of K = 16.
-__device__ __forceinline__ void issue_ts64(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
+// D (+)= A B with A [128 x 128] in TMEM (packed 16-bit pairs, 8 columns per
+// K = 16) and B [K = 128 rows x N = 128] stored row-major (N contiguous),
+// read MN-major (D halves 16 KB apart, 8-row groups 1 KB apart).
+__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox64, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < 8; ++kk)
+        mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void named_sync_softmax() {  // warps 0-7 only
+    asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- dK/dV
 // One CTA per (b, kv-head hk, 128-key chunk of KV tile j). K and V of the
-// chunk stay in shared memory. Work items are 64-row pieces of every query
-// tile that selected j, over the query heads of hk's group, in (head,
-// ascending tile, piece) order; even items go to softmax group A (warps
-// 0-3), odd items to group B (warps 4-7), one thread per key row. Per item:
-//   S^T = K Q^T, dP^T = V dO^T           (TMEM, 64 columns each)
+// chunk stay in shared memory. Work items are the 128-row chunks of every
+// query tile that selected j, over the query heads of hk's group, in
+// (head, ascending tile, chunk) order. Per item:
+//   S^T = K Q^T, dP^T = V dO^T            (TMEM, thread = key row)
 //   P^T = exp(scale S^T - LSE_t), dS^T = P^T (dP^T - Dvec_t)
-//                                        (packed back into the first 32
-//                                         columns of S^T and of dP^T)
-//   dV += P^T dO, dK += dS^T Q           (A operands read from TMEM)
-// The MMA order S/dP(m), dV/dK(m-1), S/dP(m+1), ... lets one group's
-// softmax run while the tensor core works on the other group's item.
-// TMEM columns: group A S^T [0,64) dP^T [64,128); group B S^T [128,192)
-// dP^T [192,256); dV [256,384); dK [384,512).
-constexpr int kDkStages = 4;
-constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kHalf;
-constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kHalf;  // per stage: lse2[64], dvec[64]
-constexpr int kDkOffCtl = kDkOffLd + kDkStages * 512;
+//                                         (packed 16-bit, written back over
+//                                          the consumed S^T / dP^T columns)
+//   dV += P^T dO, dK += dS^T Q            (A operands read from TMEM)
+// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and query columns
+// 64*(w/4)..+63; all eight finish reading before any writes back.
+// TMEM columns: S^T [0,128) (P^T packed in [0,64)), dP^T [128,256)
+// (dS^T packed in [128,192)), dV [256,384), dK [384,512).
+constexpr int kDkStages = 2;
+constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
+constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: lse2[128], dvec[128]
+constexpr int kDkOffCtl = kDkOffLd + kDkStages * 1024;
 constexpr size_t kDkSmem = kDkOffCtl + 256;
 
 struct WorkIter {
@@ -148,7 +150,7 @@ __device__ __forceinline__ bool work_next_list(const Prob &p, const BwdArgs &a, 
         w.end = ptr[j + 1];
     }
     w.i = a.kv_qidx[((long long)b * p.Hq + w.h) * p.nQ * a.cap + w.pos];
-    w.nsub = (q_rows(p, b, w.i) + 63) >> 6;
+    w.nsub = (q_rows(p, b, w.i) + 127) >> 7;
     w.sub = 0;
     return true;
 }
@@ -168,7 +170,7 @@ __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, in
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __maxnreg__(200)  // 320 threads x 200 registers fits the SM's 64 K
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
            const BwdArgs a) {
@@ -180,9 +182,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
-    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 1 + kDkStages, *b_sf = bars + 1 + 2 * kDkStages;
-    uint64_t *b_pd = b_sf + 2, *b_acc = b_sf + 4, *b_fin = b_sf + 5;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(b_sf + 6);
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_pd = bars + 6;
+    uint64_t *b_acc = bars + 7, *b_fin = bars + 8;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 9);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -205,10 +207,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b_qf + s, 1);
             mbar_init(b_qe + s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(b_sf + s, 1);
-            mbar_init(b_pd + s, 128);
-        }
+        mbar_init(b_sf, 1);
+        mbar_init(b_pd, 256);
         mbar_init(b_acc, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -218,11 +218,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int h = h0; h < h_end; ++h) {
                 const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
                 if (p.layout != L_TND) {  // every query tile has tile_q rows
-                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q >> 6);
+                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q >> 7);
                     continue;
                 }
                 const int *lst = a.kv_qidx + ((long long)b * p.Hq + h) * p.nQ * a.cap;
-                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + 63) >> 6;
+                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + 127) >> 7;
             }
         *s_nwork = n;
         fence_mbar_init();
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int M = *s_nwork;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_kv = 0, issued[kDkStages] = {0, 0, 0, 0}, mma_started = 0;
+    int issued_kv = 0, issued[kDkStages] = {0, 0}, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && M > 0) {
         // ------------------------------------------------------ producer
@@ -253,99 +253,106 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int st = m % kDkStages;
             if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
                 break;
-            const int row = qb + w.i * p.tile_q + w.sub * 64;
-            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 64;
-            mbar_expect_tx(b_qf + st, 2 * kHalf + 512);
-            tma_load_4d(sQ + st * kHalf, &tq, b_qf + st, 0, row, w.h, bc);
-            tma_load_4d(sQ + st * kHalf + kBox64, &tq, b_qf + st, 64, row, w.h, bc);
-            tma_load_4d(sO + st * kHalf, &tdo, b_qf + st, 0, row, w.h, bc);
-            tma_load_4d(sO + st * kHalf + kBox64, &tdo, b_qf + st, 64, row, w.h, bc);
-            bulk_load(sLd + st * 512, a.lse2 + slot, 256, b_qf + st);
-            bulk_load(sLd + st * 512 + 256, a.dvec + slot, 256, b_qf + st);
+            const int row = qb + w.i * p.tile_q + w.sub * 128;
+            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
+            mbar_expect_tx(b_qf + st, 2 * kTile + 1024);
+            tma_load_4d(sQ + st * kTile, &tq, b_qf + st, 0, row, w.h, bc);
+            tma_load_4d(sQ + st * kTile + kBox, &tq, b_qf + st, 64, row, w.h, bc);
+            tma_load_4d(sO + st * kTile, &tdo, b_qf + st, 0, row, w.h, bc);
+            tma_load_4d(sO + st * kTile + kBox, &tdo, b_qf + st, 64, row, w.h, bc);
+            bulk_load(sLd + st * 1024, a.lse2 + slot, 512, b_qf + st);
+            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_qf + st);
             issued[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
     } else if (warp == kMmaWarp && lane == 0 && M > 0) {
         // ---------------------------------------------------- MMA issuer
-        const uint32_t idS = idesc_f16(bf16, 128, 64, false, false);
+        const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
-        const uint32_t tS[2] = {tbase, tbase + 128}, tP[2] = {tbase + 64, tbase + 192};
-        const uint32_t tdV = tbase + 256, tdK = tbase + 384;
+        const uint32_t tS = tbase, tP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
         bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma);
         for (int m = 0; ok && m < M; ++m) {
-            const int st = m % kDkStages, gm = m & 1;
+            const int st = m % kDkStages;
             if (!(ok = mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
-            tc_fence_after();
-            issue_ss(tS[gm], aK, aQ + st * kHalf, idS, kBox, kBox64);  // S^T = K Q^T
-            issue_ss(tP[gm], aV, aO + st * kHalf, idS, kBox, kBox64);  // dP^T = V dO^T
-            mma_commit(b_sf + gm);
-            mma_started = 1;
             if (m > 0) {
-                const int mp = m - 1, sp = mp % kDkStages, gp = mp & 1;
-                if (!(ok = mbar_wait(b_pd + gp, (mp >> 1) & 1, s_abort, a.err, kSiteDkMma))) break;
+                // finish item m-1 first: its P^T / dS^T live in the columns S/dP(m) overwrite
+                const int mp = m - 1, sp = mp % kDkStages;
+                if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts64(tdV, tS[gp], aO + sp * kHalf, idA, mp > 0);  // dV += P^T dO
-                issue_ts64(tdK, tP[gp], aQ + sp * kHalf, idA, mp > 0);  // dK += dS^T Q
+                issue_ts(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
+                issue_ts(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
                 mma_commit(b_qe + sp);
             }
+            tc_fence_after();
+            issue_ss(tS, aK, aQ + st * kTile, idS);  // S^T = K Q^T
+            issue_ss(tP, aV, aO + st * kTile, idS);  // dP^T = V dO^T
+            mma_commit(b_sf);
+            mma_started = 1;
         }
         if (ok) {
-            const int mp = M - 1, sp = mp % kDkStages, gp = mp & 1;
-            if (mbar_wait(b_pd + gp, (mp >> 1) & 1, s_abort, a.err, kSiteDkMma)) {
+            const int mp = M - 1, sp = mp % kDkStages;
+            if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
-                issue_ts64(tdV, tS[gp], aO + sp * kHalf, idA, mp > 0);
-                issue_ts64(tdK, tP[gp], aQ + sp * kHalf, idA, mp > 0);
+                issue_ts(tdV, tS, aO + sp * kTile, idA, mp > 0);
+                issue_ts(tdK, tP, aQ + sp * kTile, idA, mp > 0);
                 mma_commit(b_qe + sp);
                 mma_commit(b_acc);
             }
         }
     } else if (warp < 8) {
         // ------------------------------------------- softmax + epilogue
-        const int gw = warp >> 2, lg = warp & 3;  // group, lane quarter
+        const int lg = warp & 3, ch = warp >> 2;  // lane quarter, query-column half
         const int u = lg * 32 + lane;             // key row within the chunk
         const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
-        const uint32_t cS = gw * 128, cP = gw * 128 + 64;
         const float sl2 = p.scale * kLog2e;
         const bool key_ok = u < kvalid;
         bool ok = true;
-        for (int m = gw; m < M; m += 2) {
+        for (int m = 0; m < M; ++m) {
             const int st = m % kDkStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + gw, (m >> 1) & 1, s_abort, a.err, kSiteDkSoft) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
-            if (!ok) break;
-            tc_fence_after();
-            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 512);
-            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 512 + 256);
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tl + cS + q2 * 32, sr);
-                tmem_ld32(tl + cP + q2 * 32, dr);
+            // every softmax warp takes part in the named barrier below, even after a failed wait
+            uint32_t sr[64], dr[64];
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+                tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
+                tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
                 tmem_wait_ld();
-                uint32_t pw[16], dw[16];
-#pragma unroll
-                for (int t4 = 0; t4 < 8; ++t4) {
-                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pp[4], dd[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
-                        pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
-                    }
-                    pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
-                    pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
-                    dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
-                    dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
-                }
-                tmem_st16(tl + cS + q2 * 16, pw);  // P^T over S^T's consumed columns
-                tmem_st16(tl + cP + q2 * 16, dw);  // dS^T over dP^T's consumed columns
             }
+            named_sync_softmax();  // all S^T / dP^T reads done before any write-back
+            // a failed wait anywhere has raised the CTA's abort flag before the
+            // barrier, so every softmax warp leaves the loop together
+            if (*s_abort) {
+                ok = false;
+                break;
+            }
+            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
+            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
+            uint32_t pw[32], dw[32];
+#pragma unroll
+            for (int t4 = 0; t4 < 16; ++t4) {
+                const float4 l4 = sl4[t4], d4 = sd4[t4];
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                float pp[4], dd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
+                    pp[e] = pr;
+                    dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
+                }
+                pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
+                pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
+                dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
+                dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
+            }
+            tmem_st32(tl + ch * 32, pw);        // P^T, packed, over consumed S^T columns
+            tmem_st32(tl + 128 + ch * 32, dw);  // dS^T, packed, over consumed dP^T columns
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_pd + gw);
+            mbar_arrive(b_pd);
         }
         if (ok && M > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_acc, 0, s_abort, a.err, kSiteDkSoft));
@@ -354,16 +361,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool have = ok && M > 0;
         const bool row_ok = (p.layout == L_TND) ? key_ok : true;
         const long long ro = tok_off(p, false, b, key0 + u, hk);
-        T *dst = reinterpret_cast<T *>(gw ? a.dk : a.dv) + ro;   // group A writes dV, group B dK
+        T *dst = reinterpret_cast<T *>(ch ? a.dk : a.dv) + ro;   // half 0 writes dV, half 1 dK
         const float inv = kvalid_tile > 0 ? 1.f / (float)kvalid_tile : 0.f;
-        const float *cbase = gw ? a.dpk : a.dpv;
+        const float *cbase = ch ? a.dpk : a.dpv;
         const float *cadd = cbase ? cbase + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
-        const float mul = gw ? p.scale : 1.f;
+        const float mul = ch ? p.scale : 1.f;
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t o[32];
             if (have) {
-                tmem_ld32(tl + 256 + gw * 128 + q4 * 32, o);
+                tmem_ld32(tl + 256 + ch * 128 + q4 * 32, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -408,19 +415,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // -------------------------------------------------------------------- dQ
-// One CTA per (b, h, query tile i): two groups of 128 rows (A: warps 0-3,
-// B: warps 4-7; one group for 128-token tiles) share 64-key chunks of the
-// selected KV tiles. Per chunk and group:
-//   S = Q K^T, dP = dO V^T                 (TMEM, 64 columns each)
-//   dS = P (dP - Dvec), P = exp(scale S - LSE)
-//                                          (packed into S's first 32 columns)
-//   dQ += dS K                             (A operand read from TMEM)
-// MMA order per chunk c: S/dP_A(c), dQ_B(c-1), S/dP_B(c), dQ_A(c).
-// TMEM columns: group A S [0,64) dP [64,128); group B S [128,192)
-// dP [192,256); dQ_A [256,384); dQ_B [384,512).
-constexpr int kDqOffQ = 0, kDqOffO = 2 * kTile, kDqOffK = 4 * kTile, kDqOffV = 4 * kTile + 2 * kHalf;
+// One CTA per (b, h, 128-row chunk of query tile i), looping over the
+// selected KV tiles' 128-key chunks:
+//   S = Q K^T, dP = dO V^T (TMEM), P = exp(scale S - LSE),
+//   dS = P (dP - Dvec) -> TMEM (packed, two buffers), dQ += dS K (TMEM).
+// The eight softmax warps (lane quarter x key-column half) read S and dP
+// into registers and release them at once, so S/dP of the next chunk run
+// on the tensor core while this chunk's dS is computed; dQ += dS K reads
+// dS from TMEM. MMA order: S/dP(c), dQ(c-1), S/dP(c+1), dQ(c), ...
+// TMEM columns: S [0,128), dP [128,256), dQ [256,384), dS buffers
+// [384,448) and [448,512).
+constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = 4 * kTile;
 constexpr int kDqOffCtl = 6 * kTile;
-constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks64 * 6;
+constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks * 6;
 
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -436,28 +443,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 3, *b_vf = bars + 5, *b_ve = bars + 7;
-    uint64_t *b_sf = bars + 9, *b_dsf = bars + 11, *b_dq = bars + 13, *b_fin = bars + 15;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 16);
+    uint64_t *b_sf = bars + 9, *b_sfree = bars + 10, *b_dsf = bars + 11, *b_dq = bars + 12, *b_fin = bars + 14;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     int *s_crow = reinterpret_cast<int *>(sm + kDqOffCtl + 256);
-    short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks64);
+    short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
-    int nrows[2];
-    for (int gg = 0; gg < 2; ++gg) {
-        const int r0 = i * p.tile_q + gg * 128;
-        int n = (gg * 128 < p.tile_q) ? 128 : 0;
-        if (p.layout == L_TND && n > 0) {
-            n = (p.cu_q[b + 1] - p.cu_q[b]) - r0;
-            n = n < 0 ? 0 : (n > 128 ? 128 : n);
-        }
-        nrows[gg] = n;
+    const int subs = p.tile_q >> 7;
+    const int i = blockIdx.x / subs, half = blockIdx.x % subs;
+    const int h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    const int row0 = i * p.tile_q + half * 128;
+    int nrows = 128;
+    if (p.layout == L_TND) {
+        nrows = (p.cu_q[b + 1] - p.cu_q[b]) - row0;
+        if (nrows <= 0) return;
+        nrows = nrows > 128 ? 128 : nrows;
     }
-    if (nrows[0] == 0) return;
-    const bool has_b = nrows[1] > 0;
-    const int qbase = (p.layout == L_TND ? p.cu_q[b] : 0) + i * p.tile_q;
+    const int qrc = (p.layout == L_TND ? p.cu_q[b] : 0) + row0;
     const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0);
     const int bc = (p.layout == L_TND ? 0 : b);
     const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
@@ -469,19 +473,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b_ke + s, 1);
             mbar_init(b_vf + s, 1);
             mbar_init(b_ve + s, 1);
-            mbar_init(b_sf + s, 1);
-            mbar_init(b_dsf + s, 128);
             mbar_init(b_dq + s, 1);
         }
+        mbar_init(b_sf, 1);
+        mbar_init(b_sfree, 256);
+        mbar_init(b_dsf, 256);
         mbar_init(b_fin, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
     if (warp == kProdWarp) {
-        // chunk list of 64-key chunks: (KV row start within the batch entry, valid keys)
         const int cnt = a.q_cnt[qrow];
         const int *idx = a.q_idx + qrow * a.cap;
-        const int per = p.tile_kv >> 6;
+        const int per = p.tile_kv >> 7;
         int total = 0;
         for (int n0 = 0; n0 < cnt; n0 += 32) {
             const int n = n0 + lane;
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (n < cnt) {
                 jj = idx[n];
                 kvv = kv_valid(p, b, jj);
-                nc = min(per, (kvv + 63) >> 6);
+                nc = min(per, (kvv + 127) >> 7);
             }
             int inc = nc;
 #pragma unroll
@@ -500,14 +504,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int base = total + inc - nc;
             for (int c = 0; c < nc; ++c) {
                 const int pos = base + c;
-                if (pos < kMaxChunks64) {
-                    s_crow[pos] = jj * p.tile_kv + c * 64;
-                    s_cval[pos] = (short)min(64, kvv - c * 64);
+                if (pos < kMaxChunks) {
+                    s_crow[pos] = jj * p.tile_kv + c * 128;
+                    s_cval[pos] = (short)min(128, kvv - c * 128);
                 }
             }
             total += __shfl_sync(0xffffffffu, inc, 31);
         }
-        if (lane == 0) *s_nchunk = min(total, kMaxChunks64);
+        if (lane == 0) *s_nchunk = min(total, kMaxChunks);
     } else if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
@@ -521,130 +525,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int issued_q = 0, issued_k[2] = {0, 0}, issued_v[2] = {0, 0}, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && N > 0) {
-        const int ng = has_b ? 2 : 1;
-        mbar_expect_tx(b_q, ng * 2 * kTile);
-        for (int gg = 0; gg < ng; ++gg) {
-            tma_load_4d(sQ + gg * kTile, &tq, b_q, 0, qbase + gg * 128, h, bc);
-            tma_load_4d(sQ + gg * kTile + kBox, &tq, b_q, 64, qbase + gg * 128, h, bc);
-            tma_load_4d(sO + gg * kTile, &tdo, b_q, 0, qbase + gg * 128, h, bc);
-            tma_load_4d(sO + gg * kTile + kBox, &tdo, b_q, 64, qbase + gg * 128, h, bc);
-        }
+        mbar_expect_tx(b_q, 2 * kTile);
+        tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
+        tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
+        tma_load_4d(sO, &tdo, b_q, 0, qrc, h, bc);
+        tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
             const int s = c & 1;
             const int kr = kvb + s_crow[c];
-            if (c >= 2 && !mbar_wait(b_ke + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
-            mbar_expect_tx(b_kf + s, kHalf);
-            tma_load_4d(sK + s * kHalf, &tk, b_kf + s, 0, kr, hk, bc);
-            tma_load_4d(sK + s * kHalf + kBox64, &tk, b_kf + s, 64, kr, hk, bc);
-            issued_k[s]++;
             if (c >= 2 && !mbar_wait(b_ve + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
-            mbar_expect_tx(b_vf + s, kHalf);
-            tma_load_4d(sV + s * kHalf, &tv, b_vf + s, 0, kr, hk, bc);
-            tma_load_4d(sV + s * kHalf + kBox64, &tv, b_vf + s, 64, kr, hk, bc);
+            mbar_expect_tx(b_vf + s, kTile);
+            tma_load_4d(sV + s * kTile, &tv, b_vf + s, 0, kr, hk, bc);
+            tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
             issued_v[s]++;
+            if (c >= 2 && !mbar_wait(b_ke + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
+            mbar_expect_tx(b_kf + s, kTile);
+            tma_load_4d(sK + s * kTile, &tk, b_kf + s, 0, kr, hk, bc);
+            tma_load_4d(sK + s * kTile + kBox, &tk, b_kf + s, 64, kr, hk, bc);
+            issued_k[s]++;
         }
     } else if (warp == kMmaWarp && lane == 0 && N > 0) {
-        const uint32_t idS = idesc_f16(bf16, 128, 64, false, false);
+        const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idQ = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV);
-        const uint32_t tS[2] = {tbase, tbase + 128}, tP[2] = {tbase + 64, tbase + 192};
-        const uint32_t tQ[2] = {tbase + 256, tbase + 384};
+        const uint32_t tS = tbase, tP = tbase + 128, tQ = tbase + 256, tX = tbase + 384;
         bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
-            const int s = c & 1, sp = (c - 1) & 1;
+            const int s = c & 1;
             if (!(ok = mbar_wait(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             if (!(ok = mbar_wait(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (c > 0 && !(ok = mbar_wait(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tS[0], aQ, aK + s * kHalf, idS, kBox, kBox64);  // S_A = Q_A K^T
-            issue_ss(tP[0], aO, aV + s * kHalf, idS, kBox, kBox64);  // dP_A = dO_A V^T
-            mma_commit(b_sf + 0);
-            mma_started = 1;
-            if (has_b) {
-                if (c > 0) {
-                    if (!(ok = mbar_wait(b_dsf + 1, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
-                    tc_fence_after();
-                    issue_ts64(tQ[1], tS[1], aK + sp * kHalf, idQ, c - 1 > 0);  // dQ_B += dS_B K
-                    mma_commit(b_dq + 1);
-                    mma_commit(b_ke + sp);
-                }
-                issue_ss(tS[1], aQ + kTile, aK + s * kHalf, idS, kBox, kBox64);
-                issue_ss(tP[1], aO + kTile, aV + s * kHalf, idS, kBox, kBox64);
-                mma_commit(b_sf + 1);
-            }
+            issue_ss(tS, aQ, aK + s * kTile, idS);  // S = Q K^T
+            issue_ss(tP, aO, aV + s * kTile, idS);  // dP = dO V^T
+            mma_commit(b_sf);
             mma_commit(b_ve + s);
-            if (!(ok = mbar_wait(b_dsf + 0, c & 1, s_abort, a.err, kSiteDqMma))) break;
-            tc_fence_after();
-            issue_ts64(tQ[0], tS[0], aK + s * kHalf, idQ, c > 0);  // dQ_A += dS_A K
-            mma_commit(b_dq + 0);
-            if (!has_b) mma_commit(b_ke + s);
-        }
-        if (ok && has_b) {
-            const int sp = (N - 1) & 1;
-            if (mbar_wait(b_dsf + 1, (N - 1) & 1, s_abort, a.err, kSiteDqMma)) {
+            mma_started = 1;
+            if (c > 0) {
+                const int cp = c - 1, sp = cp & 1;
+                if (!(ok = mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma))) break;
                 tc_fence_after();
-                issue_ts64(tQ[1], tS[1], aK + sp * kHalf, idQ, N - 1 > 0);
-                mma_commit(b_dq + 1);
+                issue_ts(tQ, tX + sp * 64, aK + sp * kTile, idQ, cp > 0);  // dQ += dS K
+                mma_commit(b_dq + sp);
                 mma_commit(b_ke + sp);
             }
         }
-    } else if (warp < 8 && (warp < 4 || has_b)) {
-        const int gw = warp >> 2, lg = warp & 3;
+        if (ok) {
+            const int cp = N - 1, sp = cp & 1;
+            if (mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma)) {
+                tc_fence_after();
+                issue_ts(tQ, tX + sp * 64, aK + sp * kTile, idQ, cp > 0);
+                mma_commit(b_dq + sp);
+                mma_commit(b_ke + sp);
+            }
+        }
+    } else if (warp < 8) {
+        const int lg = warp & 3, ch = warp >> 2;  // lane quarter, key-column half
         const int r = lg * 32 + lane;
         const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
-        const uint32_t cS = gw * 128, cP = gw * 128 + 64, cQ = 256 + gw * 128;
         const float sl2 = p.scale * kLog2e;
-        const bool row_ok = r < nrows[gw];
-        const int row = i * p.tile_q + gw * 128 + r;  // within the batch entry
-        const long long slot = ((long long)b * p.Hq + h) * p.nQ * p.tile_q + row;
+        const bool row_ok = r < nrows;
+        const long long slot = ((long long)b * p.Hq + h) * p.nQ * p.tile_q + row0 + r;
         const float l2 = N > 0 ? a.lse2[slot] : INFINITY;
         const float dvv = N > 0 ? a.dvec[slot] : 0.f;
         bool ok = true;
         for (int c = 0; c < N; ++c) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + gw, c & 1, s_abort, a.err, kSiteDqSoft));
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;
             tc_fence_after();
-            const int valid = s_cval[c];
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
+            tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(b_sfree);  // S and dP of this chunk are in registers
+            const int valid = s_cval[c] - ch * 64;
+            uint32_t dw[32];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tl + cS + q2 * 32, sr);
-                tmem_ld32(tl + cP + q2 * 32, dr);
-                tmem_wait_ld();
-                uint32_t dw[16];
+            for (int t2 = 0; t2 < 32; ++t2) {
+                float dd[2];
 #pragma unroll
-                for (int t2 = 0; t2 < 16; ++t2) {
-                    float dd[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int kk = q2 * 32 + t2 * 2 + e;
-                        const float pr = kk < valid ? ex2(fmaf(__uint_as_float(sr[t2 * 2 + e]), sl2, -l2)) : 0.f;
-                        dd[e] = pr * (__uint_as_float(dr[t2 * 2 + e]) - dvv);
-                    }
-                    dw[t2] = pack2<T>(dd[0], dd[1]);
+                for (int e = 0; e < 2; ++e) {
+                    const int kk = t2 * 2 + e;
+                    const float pr = kk < valid ? ex2(fmaf(__uint_as_float(sr[kk]), sl2, -l2)) : 0.f;
+                    dd[e] = pr * (__uint_as_float(dr[kk]) - dvv);
                 }
-                tmem_st16(tl + cS + q2 * 16, dw);  // dS over S's consumed columns
+                dw[t2] = pack2<T>(dd[0], dd[1]);
             }
+            if (c >= 2) {  // dS buffer c&1 was read by dQ(c-2)
+                ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (c & 1), ((c >> 1) - 1) & 1, s_abort, a.err,
+                                                       kSiteDqSoft));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st32(tl + 384 + (c & 1) * 64 + ch * 32, dw);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_dsf + gw);
+            mbar_arrive(b_dsf);
         }
         if (ok && N > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_dq + gw, (N - 1) & 1, s_abort, a.err, kSiteDqSoft));
+            const int cp = N - 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (cp & 1), (cp >> 1) & 1, s_abort, a.err, kSiteDqSoft));
             if (ok) tc_fence_after();
         }
         const bool have = ok && N > 0;
-        const long long ro = tok_off(p, true, b, row, h);
+        const long long ro = tok_off(p, true, b, row0 + r, h) + ch * 64;
         T *dq = reinterpret_cast<T *>(a.dq) + ro;
         const int qv = a.dpq ? q_valid(p, b, i) : 0;
-        const bool add_c = a.dpq && (gw * 128 + r) < qv;
-        const float *cq = a.dpq ? a.dpq + qrow * 128 : nullptr;
+        const bool add_c = a.dpq && (half * 128 + r) < qv;
+        const float *cq = a.dpq ? a.dpq + qrow * 128 + ch * 64 : nullptr;
         const float inv = qv > 0 ? 1.f / (float)qv : 0.f;
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t o[32];
             if (have) {
-                tmem_ld32(tl + cQ + q4 * 32, o);
+                tmem_ld32(tl + 256 + ch * 64 + q2 * 32, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -656,12 +654,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int e2 = 0; e2 < 16; ++e2) {
                 float v0 = __uint_as_float(o[2 * e2]) * p.scale, v1 = __uint_as_float(o[2 * e2 + 1]) * p.scale;
                 if (add_c) {
-                    v0 += cq[q4 * 32 + 2 * e2] * inv;
-                    v1 += cq[q4 * 32 + 2 * e2 + 1] * inv;
+                    v0 += cq[q2 * 32 + 2 * e2] * inv;
+                    v1 += cq[q2 * 32 + 2 * e2 + 1] * inv;
                 }
                 wv[e2] = pack2<T>(v0, v1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q4 * 32);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q2 * 32);
 #pragma unroll
             for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
         }
@@ -815,9 +813,9 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
 }
 
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, tdo;  // q / dO in 64-row boxes, k / v in 128-row boxes
-    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq, 64) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv, 128) ||
-        !make_tmap_rows(&tv, p, false, a.v, p.Hkv, 128) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, 64))
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
         return cudaErrorInvalidValue;
     dim3 grid(p.nKV * (p.tile_kv / 128), p.Hkv, p.B);
     static bool attr = false;
@@ -836,11 +834,11 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, tdo;  // q / dO in 128-row boxes, k / v in 64-row boxes
-    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq, 128) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv, 64) ||
-        !make_tmap_rows(&tv, p, false, a.v, p.Hkv, 64) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, 128))
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
         return cudaErrorInvalidValue;
-    dim3 grid(p.nQ, p.Hq, p.B);
+    dim3 grid(p.nQ * (p.tile_q / 128), p.Hq, p.B);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_dq<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem);

@@ -300,7 +300,7 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (gate && !aligned16(gate)))
         return VSA_ERR_LAYOUT;
     if (idx_cap < 1 || idx_cap > p.nKV) return VSA_ERR_SHAPE;
-    if ((long long)idx_cap * (p.tile_kv / 64) > kMaxChunks64) return VSA_ERR_UNSUPPORTED;
+    if ((long long)idx_cap * (p.tile_kv / 128) > kMaxChunks) return VSA_ERR_UNSUPPORTED;
     VSA_TRY(check_ws(p, gate != nullptr, workspace, workspace_bytes));
     const WsLayout L = ws_layout(p, gate != nullptr);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -28,10 +28,8 @@ cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int
 
 // Largest nKV the selection kernel handles (its shared-memory score rows).
 constexpr int kMaxSelectKV = 3072;
-// Largest number of 128-key chunks one query tile may visit (forward), and
-// of 64-key chunks (dQ pass).
+// Largest number of 128-key chunks one query tile may visit.
 constexpr int kMaxChunks = 1024;
-constexpr int kMaxChunks64 = 2048;
 
 // Forward attention (tcgen05). out / o_sparse / gate / c as in vsa_fwd.
 struct FwdArgs {
