@@ -113,8 +113,14 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
         mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-__device__ __forceinline__ void named_sync_softmax() {  // warps 0-7 only
-    asm volatile("bar.sync 1, 256;" ::: "memory");
+// As issue_ts, with the packed A operand held in two 32-column pieces:
+// K steps 0-3 read columns [a_tmem, a_tmem+32), steps 4-7 read
+// [a_tmem+64, a_tmem+96).
+__device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_f16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
+                   (acc || kk > 0) ? 1u : 0u);
 }
 
 // ----------------------------------------------------------------- dK/dV
@@ -128,9 +134,12 @@ __device__ __forceinline__ void named_sync_softmax() {  // warps 0-7 only
 //                                          the consumed S^T / dP^T columns)
 //   dV += P^T dO, dK += dS^T Q            (A operands read from TMEM)
 // Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and query columns
-// 64*(w/4)..+63; all eight finish reading before any writes back.
-// TMEM columns: S^T [0,128) (P^T packed in [0,64)), dP^T [128,256)
-// (dS^T packed in [128,192)), dV [256,384), dK [384,512).
+// 64*(w/4)..+63, and writes its packed results into the first 32 of its
+// own 64 columns, 32-column slice by slice, so no warp overwrites columns
+// another warp still reads.
+// TMEM columns: S^T [0,128) (P^T packed in [0,32) and [64,96)), dP^T
+// [128,256) (dS^T packed in [128,160) and [192,224)), dV [256,384),
+// dK [384,512).
 constexpr int kDkStages = 2;
 constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
 constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: lse2[128], dvec[128]
@@ -170,7 +179,7 @@ __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, in
 }
 
 template <typename T>
-__global__ void __maxnreg__(200)  // 320 threads x 200 registers fits the SM's 64 K
+__global__ void __launch_bounds__(kBwdThreads, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
            const BwdArgs a) {
@@ -280,8 +289,8 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fits the SM's 6
                 const int mp = m - 1, sp = mp % kDkStages;
                 if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
-                issue_ts(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
+                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
+                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
                 mma_commit(b_qe + sp);
             }
             tc_fence_after();
@@ -294,8 +303,8 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fits the SM's 6
             const int mp = M - 1, sp = mp % kDkStages;
             if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
-                issue_ts(tdV, tS, aO + sp * kTile, idA, mp > 0);
-                issue_ts(tdK, tP, aQ + sp * kTile, idA, mp > 0);
+                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);
+                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);
                 mma_commit(b_qe + sp);
                 mma_commit(b_acc);
             }
@@ -312,44 +321,37 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fits the SM's 6
             const int st = m % kDkStages;
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
-            // every softmax warp takes part in the named barrier below, even after a failed wait
-            uint32_t sr[64], dr[64];
-            if (ok) {
-                tc_fence_after();
-                tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-                tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-                tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
-                tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
-                tmem_wait_ld();
-            }
-            named_sync_softmax();  // all S^T / dP^T reads done before any write-back
-            // a failed wait anywhere has raised the CTA's abort flag before the
-            // barrier, so every softmax warp leaves the loop together
-            if (*s_abort) {
-                ok = false;
-                break;
-            }
+            if (!ok) break;
+            tc_fence_after();
             const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
             const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
-            uint32_t pw[32], dw[32];
 #pragma unroll
-            for (int t4 = 0; t4 < 16; ++t4) {
-                const float4 l4 = sl4[t4], d4 = sd4[t4];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                float pp[4], dd[4];
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
+                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
+                tmem_wait_ld();
+                uint32_t pw[16], dw[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
-                    pp[e] = pr;
-                    dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pp[4], dd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
+                        pp[e] = pr;
+                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
+                    }
+                    pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
+                    pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
+                    dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
+                    dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
-                pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
-                pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
-                dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
-                dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
+                // into this warp's own, already read columns
+                tmem_st16(tl + ch * 64 + q2 * 16, pw);
+                tmem_st16(tl + 128 + ch * 64 + q2 * 16, dw);
             }
-            tmem_st32(tl + ch * 32, pw);        // P^T, packed, over consumed S^T columns
-            tmem_st32(tl + 128 + ch * 32, dw);  // dS^T, packed, over consumed dP^T columns
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_pd);

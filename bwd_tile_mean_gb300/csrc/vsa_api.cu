@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdio>
 #include <vector>
 
 #include "vsa.h"
@@ -35,8 +36,11 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
+const char *g_last_launch = "";
+
 void prof_begin(const char *name, cudaStream_t s) {
     ++g_launches;
+    g_last_launch = name;
     if (!g_prof) return;
     ProfRec r{name, take_event(), take_event()};
     cudaEventRecord(r.a, s);
@@ -183,7 +187,13 @@ X *at(void *ws, size_t off) {
     return reinterpret_cast<X *>(reinterpret_cast<uint8_t *>(ws) + off);
 }
 
-vsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VSA_OK : VSA_ERR_CUDA; }
+cudaError_t g_last_cuda = cudaSuccess;
+
+vsa_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return VSA_OK;
+    g_last_cuda = e;
+    return VSA_ERR_CUDA;
+}
 
 #define VSA_TRY(expr)                              \
     do {                                           \
@@ -366,6 +376,13 @@ vsa_status vsa_device_status(void *workspace, vsa_stream_t stream, int32_t *code
     if (v != 0 && cudaMemset(workspace, 0, sizeof(v)) != cudaSuccess) return VSA_ERR_CUDA;
     *code = (int32_t)v;
     return v ? VSA_ERR_DEVICE : VSA_OK;
+}
+
+const char *vsa_last_cuda_error(void) {
+    static thread_local char buf[256];
+    if (g_last_cuda == cudaSuccess) return "no error";
+    snprintf(buf, sizeof(buf), "%s (last kernel launched: %s)", cudaGetErrorString(g_last_cuda), g_last_launch);
+    return buf;
 }
 
 void vsa_profile_enable(int on) { g_prof = on != 0; }

@@ -28,14 +28,17 @@ STATUS = {0: "VSA_OK", 1: "VSA_ERR_NULL", 2: "VSA_ERR_SHAPE", 3: "VSA_ERR_DTYPE"
 
 EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_static", "vsa_mask_to_index",
            "vsa_fwd", "vsa_bwd",
-           "vsa_status_string", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
+           "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count")
 
 
 class VsaError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
-        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({_lib.vsa_status_string(code).decode()})")
+        msg = f"{fn} failed: {STATUS.get(code, code)} ({_lib.vsa_status_string(code).decode()})"
+        if code == 8:
+            msg += f": {_lib.vsa_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 class VsaDesc(C.Structure):
@@ -78,6 +81,7 @@ def lib():
                               C.c_size_t, P]
         L.vsa_status_string.restype = C.c_char_p
         L.vsa_status_string.argtypes = [C.c_int]
+        L.vsa_last_cuda_error.restype = C.c_char_p
         L.vsa_device_status.restype = C.c_int
         L.vsa_device_status.argtypes = [P, P, C.POINTER(C.c_int32)]
         L.vsa_profile_enable.argtypes = [C.c_int]

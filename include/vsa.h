@@ -199,6 +199,11 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
 /* Human-readable name of a status. */
 const char *vsa_status_string(vsa_status status);
 
+/* Message of the last CUDA error behind a VSA_ERR_CUDA return, with the
+ * name of the last kernel the library launched ("no error" if there was
+ * none). The string is owned by the library (per calling thread). */
+const char *vsa_last_cuda_error(void);
+
 /* Synchronises `stream`, reads the device status word in `workspace` into
  * *code (0 = no failure; otherwise the site of the wait that timed out) and
  * clears it. Returns VSA_ERR_DEVICE when *code != 0. */
