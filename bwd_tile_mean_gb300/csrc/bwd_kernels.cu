@@ -425,10 +425,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // into registers and release them at once, so S/dP of the next chunk run
 // on the tensor core while this chunk's dS is computed; dQ += dS K reads
 // dS from TMEM. MMA order: S/dP(c), dQ(c-1), S/dP(c+1), dQ(c), ...
+// K chunks stay until dQ += dS K has read them, one chunk after S, so K
+// has three stages; V is free right after dP and has one.
 // TMEM columns: S [0,128), dP [128,256), dQ [256,384), dS buffers
 // [384,448) and [448,512).
-constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = 4 * kTile;
-constexpr int kDqOffCtl = 6 * kTile;
+constexpr int kDqKStages = 3;
+constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = (2 + kDqKStages) * kTile;
+constexpr int kDqOffCtl = kDqOffV + kTile;
 constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks * 6;
 
 template <typename T>
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
-    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 3, *b_vf = bars + 5, *b_ve = bars + 7;
+    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 8;
     uint64_t *b_sf = bars + 9, *b_sfree = bars + 10, *b_dsf = bars + 11, *b_dq = bars + 12, *b_fin = bars + 14;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
@@ -470,13 +473,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kDqKStages; ++s) {
             mbar_init(b_kf + s, 1);
             mbar_init(b_ke + s, 1);
-            mbar_init(b_vf + s, 1);
-            mbar_init(b_ve + s, 1);
-            mbar_init(b_dq + s, 1);
         }
+        mbar_init(b_vf, 1);
+        mbar_init(b_ve, 1);
+        for (int s = 0; s < 2; ++s) mbar_init(b_dq + s, 1);
         mbar_init(b_sf, 1);
         mbar_init(b_sfree, 256);
         mbar_init(b_dsf, 256);
@@ -524,7 +527,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int N = *s_nchunk;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_q = 0, issued_k[2] = {0, 0}, issued_v[2] = {0, 0}, mma_started = 0;
+    int issued_q = 0, issued_k[kDqKStages] = {0, 0, 0}, issued_v = 0, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && N > 0) {
         mbar_expect_tx(b_q, 2 * kTile);
@@ -534,18 +537,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
-            const int s = c & 1;
+            const int sk = c % kDqKStages;
             const int kr = kvb + s_crow[c];
-            if (c >= 2 && !mbar_wait(b_ve + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
-            mbar_expect_tx(b_vf + s, kTile);
-            tma_load_4d(sV + s * kTile, &tv, b_vf + s, 0, kr, hk, bc);
-            tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
-            issued_v[s]++;
-            if (c >= 2 && !mbar_wait(b_ke + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
-            mbar_expect_tx(b_kf + s, kTile);
-            tma_load_4d(sK + s * kTile, &tk, b_kf + s, 0, kr, hk, bc);
-            tma_load_4d(sK + s * kTile + kBox, &tk, b_kf + s, 64, kr, hk, bc);
-            issued_k[s]++;
+            if (c >= kDqKStages && !mbar_wait(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
+                break;
+            mbar_expect_tx(b_kf + sk, kTile);
+            tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
+            tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
+            issued_k[sk]++;
+            if (c >= 1 && !mbar_wait(b_ve, (c - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
+            mbar_expect_tx(b_vf, kTile);
+            tma_load_4d(sV, &tv, b_vf, 0, kr, hk, bc);
+            tma_load_4d(sV + kBox, &tv, b_vf, 64, kr, hk, bc);
+            issued_v++;
         }
     } else if (warp == kMmaWarp && lane == 0 && N > 0) {
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
@@ -554,32 +558,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tS = tbase, tP = tbase + 128, tQ = tbase + 256, tX = tbase + 384;
         bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
-            const int s = c & 1;
-            if (!(ok = mbar_wait(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
-            if (!(ok = mbar_wait(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            const int sk = c % kDqKStages;
+            if (!(ok = mbar_wait(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (!(ok = mbar_wait(b_vf, c & 1, s_abort, a.err, kSiteDqMma))) break;
             if (c > 0 && !(ok = mbar_wait(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tS, aQ, aK + s * kTile, idS);  // S = Q K^T
-            issue_ss(tP, aO, aV + s * kTile, idS);  // dP = dO V^T
+            issue_ss(tS, aQ, aK + sk * kTile, idS);  // S = Q K^T
+            issue_ss(tP, aO, aV, idS);               // dP = dO V^T
             mma_commit(b_sf);
-            mma_commit(b_ve + s);
+            mma_commit(b_ve);
             mma_started = 1;
             if (c > 0) {
-                const int cp = c - 1, sp = cp & 1;
+                const int cp = c - 1, skp = cp % kDqKStages;
                 if (!(ok = mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma))) break;
                 tc_fence_after();
-                issue_ts(tQ, tX + sp * 64, aK + sp * kTile, idQ, cp > 0);  // dQ += dS K
-                mma_commit(b_dq + sp);
-                mma_commit(b_ke + sp);
+                issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);  // dQ += dS K
+                mma_commit(b_dq + (cp & 1));
+                mma_commit(b_ke + skp);
             }
         }
         if (ok) {
-            const int cp = N - 1, sp = cp & 1;
+            const int cp = N - 1, skp = cp % kDqKStages;
             if (mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma)) {
                 tc_fence_after();
-                issue_ts(tQ, tX + sp * 64, aK + sp * kTile, idQ, cp > 0);
-                mma_commit(b_dq + sp);
-                mma_commit(b_ke + sp);
+                issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);
+                mma_commit(b_dq + (cp & 1));
+                mma_commit(b_ke + skp);
             }
         }
     } else if (warp < 8) {
@@ -671,10 +675,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int never = 0;
         if (warp == kProdWarp && lane == 0) {
             if (issued_q) mbar_wait(b_q, 0, &never, nullptr, 0, 200000000ull);
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < kDqKStages; ++s)
                 if (issued_k[s]) mbar_wait(b_kf + s, (issued_k[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
-                if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
-            }
+            if (issued_v) mbar_wait(b_vf, (issued_v - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
         if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
