@@ -113,33 +113,23 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
         mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-// As issue_ts, with the packed A operand held in two 32-column pieces:
-// K steps 0-3 read columns [a_tmem, a_tmem+32), steps 4-7 read
-// [a_tmem+64, a_tmem+96).
-__device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_f16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
-                   (acc || kk > 0) ? 1u : 0u);
-}
-
 // ----------------------------------------------------------------- dK/dV
 // One CTA per (b, kv-head hk, 128-key chunk of KV tile j). K and V of the
 // chunk stay in shared memory. Work items are the 128-row chunks of every
 // query tile that selected j, over the query heads of hk's group, in
-// (head, ascending tile, chunk) order. Per item:
-//   S^T = K Q^T, dP^T = V dO^T            (TMEM, thread = key row)
-//   P^T = exp(scale S^T - LSE_t), dS^T = P^T (dP^T - Dvec_t)
-//                                         (packed 16-bit, written back over
-//                                          the consumed S^T / dP^T columns)
-//   dV += P^T dO, dK += dS^T Q            (A operands read from TMEM)
-// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and query columns
-// 64*(w/4)..+63, and writes its packed results into the first 32 of its
-// own 64 columns, 32-column slice by slice, so no warp overwrites columns
-// another warp still reads.
-// TMEM columns: S^T [0,128) (P^T packed in [0,32) and [64,96)), dP^T
-// [128,256) (dS^T packed in [128,160) and [192,224)), dV [256,384),
-// dK [384,512).
+// (head, ascending tile, chunk) order. Per item m:
+//   S^T = K Q^T into TMEM region X; the softmax reads it, frees X and
+//   computes P^T = exp(scale S^T - LSE_t) while dP^T = V dO^T runs into X;
+//   it then reads dP^T, frees X (S^T of item m+1 starts) and computes
+//   dS^T = P^T (dP^T - Dvec_t); P^T and dS^T go, packed to 16 bits, into
+//   their own TMEM regions, from which dV += P^T dO and dK += dS^T Q read
+//   their A operands.
+// MMA order: dV/dK(m-1), dP^T(m), S^T(m+1), so the tensor core always has
+// one MMA group queued while the softmax works on the other.
+// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. (key rows) and
+// query columns 64*(w/4)..+63.
+// TMEM columns: X [0,128), P^T packed [128,192), dS^T packed [192,256),
+// dV [256,384), dK [384,512).
 constexpr int kDkStages = 2;
 constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
 constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: lse2[128], dvec[128]
@@ -191,9 +181,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
-    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_pd = bars + 6;
-    uint64_t *b_acc = bars + 7, *b_fin = bars + 8;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 9);
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3;
+    uint64_t *b_s = bars + 5, *b_d = bars + 6, *b_xs = bars + 7, *b_xd = bars + 8, *b_pd = bars + 9;
+    uint64_t *b_pdfree = bars + 10, *b_acc = bars + 11, *b_fin = bars + 12;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 13);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -216,8 +207,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b_qf + s, 1);
             mbar_init(b_qe + s, 1);
         }
-        mbar_init(b_sf, 1);
+        mbar_init(b_s, 1);
+        mbar_init(b_d, 1);
+        mbar_init(b_xs, 256);
+        mbar_init(b_xd, 256);
         mbar_init(b_pd, 256);
+        mbar_init(b_pdfree, 1);
         mbar_init(b_acc, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -279,32 +274,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
-        const uint32_t tS = tbase, tP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
-        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma);
+        const uint32_t tX = tbase, tPt = tbase + 128, tDt = tbase + 192, tdV = tbase + 256, tdK = tbase + 384;
+        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma) && mbar_wait(b_qf, 0, s_abort, a.err, kSiteDkMma);
+        if (ok) {
+            tc_fence_after();
+            issue_ss(tX, aK, aQ, idS);  // S^T(0) = K Q^T
+            mma_commit(b_s);
+            mma_started = 1;
+        }
         for (int m = 0; ok && m < M; ++m) {
             const int st = m % kDkStages;
-            if (!(ok = mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
             if (m > 0) {
-                // finish item m-1 first: its P^T / dS^T live in the columns S/dP(m) overwrite
                 const int mp = m - 1, sp = mp % kDkStages;
                 if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
-                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
+                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
+                issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
+                mma_commit(b_pdfree);
                 mma_commit(b_qe + sp);
             }
+            if (!(ok = mbar_wait(b_xs, m & 1, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
-            issue_ss(tS, aK, aQ + st * kTile, idS);  // S^T = K Q^T
-            issue_ss(tP, aV, aO + st * kTile, idS);  // dP^T = V dO^T
-            mma_commit(b_sf);
-            mma_started = 1;
+            issue_ss(tX, aV, aO + st * kTile, idS);  // dP^T(m) = V dO^T
+            mma_commit(b_d);
+            if (m + 1 < M) {
+                const int sn = (m + 1) % kDkStages;
+                if (!(ok = mbar_wait(b_qf + sn, ((m + 1) / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
+                if (!(ok = mbar_wait(b_xd, m & 1, s_abort, a.err, kSiteDkMma))) break;
+                tc_fence_after();
+                issue_ss(tX, aK, aQ + sn * kTile, idS);  // S^T(m+1)
+                mma_commit(b_s);
+            }
         }
         if (ok) {
             const int mp = M - 1, sp = mp % kDkStages;
             if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
-                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);
-                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);
+                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);
+                issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);
+                mma_commit(b_pdfree);
                 mma_commit(b_qe + sp);
                 mma_commit(b_acc);
             }
@@ -319,39 +327,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int m = 0; m < M; ++m) {
             const int st = m % kDkStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(b_s, m & 1, s_abort, a.err, kSiteDkSoft) &&
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
-            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
-                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
+            // S^T -> P^T (fp32 kept for dS^T)
+            float pf[64];
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tl + ch * 64, r0);
+                tmem_ld32(tl + ch * 64 + 32, r1);
                 tmem_wait_ld();
-                uint32_t pw[16], dw[16];
+                tc_fence_before();
+                mbar_arrive(b_xs);  // X may take dP^T now
+                const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
 #pragma unroll
-                for (int t4 = 0; t4 < 8; ++t4) {
-                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pp[4], dd[4];
+                for (int t4 = 0; t4 < 16; ++t4) {
+                    const float4 l4 = sl4[t4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
-                        pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
+                        const int t = t4 * 4 + e;
+                        const float sv = __uint_as_float(t < 32 ? r0[t] : r1[t - 32]);
+                        pf[t] = key_ok ? ex2(fmaf(sv, sl2, -lv[e])) : 0.f;
                     }
-                    pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
-                    pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
+                }
+            }
+            uint32_t pw[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) pw[t] = pack2<T>(pf[2 * t], pf[2 * t + 1]);
+            if (m > 0) {  // P^T / dS^T regions were read by dV/dK(m-1)
+                ok = __all_sync(0xffffffffu, mbar_wait(b_pdfree, (m - 1) & 1, s_abort, a.err, kSiteDkSoft));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st32(tl + 128 + ch * 32, pw);
+            // dP^T -> dS^T
+            ok = __all_sync(0xffffffffu, mbar_wait(b_d, m & 1, s_abort, a.err, kSiteDkSoft));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t dw[32];
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tl + ch * 64, r0);
+                tmem_ld32(tl + ch * 64 + 32, r1);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(b_xd);  // X may take S^T of the next item now
+                const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
+#pragma unroll
+                for (int t4 = 0; t4 < 16; ++t4) {
+                    const float4 d4 = sd4[t4];
+                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float dd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = t4 * 4 + e;
+                        dd[e] = pf[t] * (__uint_as_float(t < 32 ? r0[t] : r1[t - 32]) - dvv[e]);
+                    }
                     dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
                     dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
-                // into this warp's own, already read columns
-                tmem_st16(tl + ch * 64 + q2 * 16, pw);
-                tmem_st16(tl + 128 + ch * 64 + q2 * 16, dw);
             }
+            tmem_st32(tl + 192 + ch * 32, dw);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_pd);
