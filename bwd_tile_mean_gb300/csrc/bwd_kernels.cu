@@ -124,8 +124,11 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
 //   dS^T = P^T (dP^T - Dvec_t); P^T and dS^T go, packed to 16 bits, into
 //   their own TMEM regions, from which dV += P^T dO and dK += dS^T Q read
 //   their A operands.
-// MMA order: dV/dK(m-1), dP^T(m), S^T(m+1), so the tensor core always has
-// one MMA group queued while the softmax works on the other.
+// MMA order: dK(m-1), dV(m-1), dP^T(m), S^T(m+1), so the tensor core always
+// has one MMA group queued while the softmax works on the other. Q (with
+// the LSE row) and dO (with Dvec) of an item sit in separately released
+// halves of a stage: Q is free once dK has read it, which lets the next
+// item's Q load start a whole dV + dP^T earlier than a joint release.
 // Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. (key rows) and
 // query columns 64*(w/4)..+63.
 // TMEM columns: X [0,128), P^T packed [128,192), dS^T packed [192,256),
@@ -181,10 +184,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
-    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3;
-    uint64_t *b_s = bars + 5, *b_d = bars + 6, *b_xs = bars + 7, *b_xd = bars + 8, *b_pd = bars + 9;
-    uint64_t *b_pdfree = bars + 10, *b_acc = bars + 11, *b_fin = bars + 12;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 13);
+    // b_qf / b_qe: Q halves of the stages; b_of / b_oe: dO halves
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_of = bars + 5, *b_oe = bars + 7;
+    uint64_t *b_s = bars + 9, *b_d = bars + 10, *b_xs = bars + 11, *b_xd = bars + 12, *b_pd = bars + 13;
+    uint64_t *b_pdfree = bars + 14, *b_acc = bars + 15, *b_fin = bars + 16;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 17);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -206,6 +210,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int s = 0; s < kDkStages; ++s) {
             mbar_init(b_qf + s, 1);
             mbar_init(b_qe + s, 1);
+            mbar_init(b_of + s, 1);
+            mbar_init(b_oe + s, 1);
         }
         mbar_init(b_s, 1);
         mbar_init(b_d, 1);
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int M = *s_nwork;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_kv = 0, issued[kDkStages] = {0, 0}, mma_started = 0;
+    int issued_kv = 0, issued[kDkStages] = {0, 0}, issued_o[kDkStages] = {0, 0}, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && M > 0) {
         // ------------------------------------------------------ producer
@@ -255,18 +261,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool more = work_first(p, a, b, h0, h_end, j, w);
         for (int m = 0; more && m < M; ++m) {
             const int st = m % kDkStages;
-            if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
-                break;
             const int row = qb + w.i * p.tile_q + w.sub * 128;
             const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
-            mbar_expect_tx(b_qf + st, 2 * kTile + 1024);
+            if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
+                break;
+            mbar_expect_tx(b_qf + st, kTile + 512);
             tma_load_4d(sQ + st * kTile, &tq, b_qf + st, 0, row, w.h, bc);
             tma_load_4d(sQ + st * kTile + kBox, &tq, b_qf + st, 64, row, w.h, bc);
-            tma_load_4d(sO + st * kTile, &tdo, b_qf + st, 0, row, w.h, bc);
-            tma_load_4d(sO + st * kTile + kBox, &tdo, b_qf + st, 64, row, w.h, bc);
             bulk_load(sLd + st * 1024, a.lse2 + slot, 512, b_qf + st);
-            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_qf + st);
             issued[st]++;
+            if (m >= kDkStages && !mbar_wait(b_oe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
+                break;
+            mbar_expect_tx(b_of + st, kTile + 512);
+            tma_load_4d(sO + st * kTile, &tdo, b_of + st, 0, row, w.h, bc);
+            tma_load_4d(sO + st * kTile + kBox, &tdo, b_of + st, 64, row, w.h, bc);
+            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_of + st);
+            issued_o[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
     } else if (warp == kMmaWarp && lane == 0 && M > 0) {
@@ -288,12 +298,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int mp = m - 1, sp = mp % kDkStages;
                 if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
                 issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
-                mma_commit(b_pdfree);
                 mma_commit(b_qe + sp);
+                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
+                mma_commit(b_pdfree);
+                mma_commit(b_oe + sp);
             }
             if (!(ok = mbar_wait(b_xs, m & 1, s_abort, a.err, kSiteDkMma))) break;
+            if (!(ok = mbar_wait(b_of + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
             issue_ss(tX, aV, aO + st * kTile, idS);  // dP^T(m) = V dO^T
             mma_commit(b_d);
@@ -310,10 +322,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int mp = M - 1, sp = mp % kDkStages;
             if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
-                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);
                 issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);
-                mma_commit(b_pdfree);
                 mma_commit(b_qe + sp);
+                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);
+                mma_commit(b_pdfree);
+                mma_commit(b_oe + sp);
                 mma_commit(b_acc);
             }
         }
@@ -331,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            // S^T -> P^T (fp32 kept for dS^T)
+            // S^T -> P^T (fp32 kept for dS^T); the LSE row came with Q
             float pf[64];
             {
                 uint32_t r0[32], r1[32];
@@ -362,8 +375,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
             }
             tmem_st32(tl + 128 + ch * 32, pw);
-            // dP^T -> dS^T
-            ok = __all_sync(0xffffffffu, mbar_wait(b_d, m & 1, s_abort, a.err, kSiteDkSoft));
+            // dP^T -> dS^T; Dvec came with dO
+            ok = __all_sync(0xffffffffu, mbar_wait(b_d, m & 1, s_abort, a.err, kSiteDkSoft) &&
+                                             mbar_wait(b_of + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
             uint32_t dw[32];
@@ -438,8 +452,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int never = 0;
         if (warp == kProdWarp && lane == 0) {
             if (issued_kv) mbar_wait(b_kv, 0, &never, nullptr, 0, 200000000ull);
-            for (int s = 0; s < kDkStages; ++s)
+            for (int s = 0; s < kDkStages; ++s) {
                 if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+                if (issued_o[s]) mbar_wait(b_of + s, (issued_o[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+            }
         }
         if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
