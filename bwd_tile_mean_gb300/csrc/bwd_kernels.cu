@@ -113,26 +113,33 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
         mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
+// As issue_ts, with the packed A operand held in two 32-column pieces:
+// K steps 0-3 read columns [a_tmem, a_tmem+32), steps 4-7 read
+// [a_tmem+64, a_tmem+96).
+__device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_f16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
+                   (acc || kk > 0) ? 1u : 0u);
+}
+
 // ----------------------------------------------------------------- dK/dV
 // One CTA per (b, kv-head hk, 128-key chunk of KV tile j). K and V of the
 // chunk stay in shared memory. Work items are the 128-row chunks of every
 // query tile that selected j, over the query heads of hk's group, in
-// (head, ascending tile, chunk) order. Per item m:
-//   S^T = K Q^T into TMEM region X; the softmax reads it, frees X and
-//   computes P^T = exp(scale S^T - LSE_t) while dP^T = V dO^T runs into X;
-//   it then reads dP^T, frees X (S^T of item m+1 starts) and computes
-//   dS^T = P^T (dP^T - Dvec_t); P^T and dS^T go, packed to 16 bits, into
-//   their own TMEM regions, from which dV += P^T dO and dK += dS^T Q read
-//   their A operands.
-// MMA order: dK(m-1), dV(m-1), dP^T(m), S^T(m+1), so the tensor core always
-// has one MMA group queued while the softmax works on the other. Q (with
-// the LSE row) and dO (with Dvec) of an item sit in separately released
-// halves of a stage: Q is free once dK has read it, which lets the next
-// item's Q load start a whole dV + dP^T earlier than a joint release.
-// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. (key rows) and
-// query columns 64*(w/4)..+63.
-// TMEM columns: X [0,128), P^T packed [128,192), dS^T packed [192,256),
-// dV [256,384), dK [384,512).
+// (head, ascending tile, chunk) order. Per item:
+//   S^T = K Q^T, dP^T = V dO^T            (TMEM, thread = key row)
+//   P^T = exp(scale S^T - LSE_t), dS^T = P^T (dP^T - Dvec_t)
+//                                         (packed 16-bit, written back over
+//                                          the consumed S^T / dP^T columns)
+//   dV += P^T dO, dK += dS^T Q            (A operands read from TMEM)
+// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and query columns
+// 64*(w/4)..+63, and writes its packed results into the first 32 of its
+// own 64 columns, 32-column slice by slice, so no warp overwrites columns
+// another warp still reads.
+// TMEM columns: S^T [0,128) (P^T packed in [0,32) and [64,96)), dP^T
+// [128,256) (dS^T packed in [128,160) and [192,224)), dV [256,384),
+// dK [384,512).
 constexpr int kDkStages = 2;
 constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
 constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: lse2[128], dvec[128]
@@ -184,11 +191,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
-    // b_qf / b_qe: Q halves of the stages; b_of / b_oe: dO halves
-    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_of = bars + 5, *b_oe = bars + 7;
-    uint64_t *b_s = bars + 9, *b_d = bars + 10, *b_xs = bars + 11, *b_xd = bars + 12, *b_pd = bars + 13;
-    uint64_t *b_pdfree = bars + 14, *b_acc = bars + 15, *b_fin = bars + 16;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 17);
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_pd = bars + 6;
+    uint64_t *b_acc = bars + 7, *b_fin = bars + 8;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 9);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -210,15 +215,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int s = 0; s < kDkStages; ++s) {
             mbar_init(b_qf + s, 1);
             mbar_init(b_qe + s, 1);
-            mbar_init(b_of + s, 1);
-            mbar_init(b_oe + s, 1);
         }
-        mbar_init(b_s, 1);
-        mbar_init(b_d, 1);
-        mbar_init(b_xs, 256);
-        mbar_init(b_xd, 256);
+        mbar_init(b_sf, 1);
         mbar_init(b_pd, 256);
-        mbar_init(b_pdfree, 1);
         mbar_init(b_acc, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -247,7 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int M = *s_nwork;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_kv = 0, issued[kDkStages] = {0, 0}, issued_o[kDkStages] = {0, 0}, mma_started = 0;
+    int issued_kv = 0, issued[kDkStages] = {0, 0}, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && M > 0) {
         // ------------------------------------------------------ producer
@@ -261,22 +260,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool more = work_first(p, a, b, h0, h_end, j, w);
         for (int m = 0; more && m < M; ++m) {
             const int st = m % kDkStages;
-            const int row = qb + w.i * p.tile_q + w.sub * 128;
-            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
             if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
                 break;
-            mbar_expect_tx(b_qf + st, kTile + 512);
+            const int row = qb + w.i * p.tile_q + w.sub * 128;
+            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
+            mbar_expect_tx(b_qf + st, 2 * kTile + 1024);
             tma_load_4d(sQ + st * kTile, &tq, b_qf + st, 0, row, w.h, bc);
             tma_load_4d(sQ + st * kTile + kBox, &tq, b_qf + st, 64, row, w.h, bc);
+            tma_load_4d(sO + st * kTile, &tdo, b_qf + st, 0, row, w.h, bc);
+            tma_load_4d(sO + st * kTile + kBox, &tdo, b_qf + st, 64, row, w.h, bc);
             bulk_load(sLd + st * 1024, a.lse2 + slot, 512, b_qf + st);
+            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_qf + st);
             issued[st]++;
-            if (m >= kDkStages && !mbar_wait(b_oe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
-                break;
-            mbar_expect_tx(b_of + st, kTile + 512);
-            tma_load_4d(sO + st * kTile, &tdo, b_of + st, 0, row, w.h, bc);
-            tma_load_4d(sO + st * kTile + kBox, &tdo, b_of + st, 64, row, w.h, bc);
-            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_of + st);
-            issued_o[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
     } else if (warp == kMmaWarp && lane == 0 && M > 0) {
@@ -284,49 +279,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
-        const uint32_t tX = tbase, tPt = tbase + 128, tDt = tbase + 192, tdV = tbase + 256, tdK = tbase + 384;
-        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma) && mbar_wait(b_qf, 0, s_abort, a.err, kSiteDkMma);
-        if (ok) {
-            tc_fence_after();
-            issue_ss(tX, aK, aQ, idS);  // S^T(0) = K Q^T
-            mma_commit(b_s);
-            mma_started = 1;
-        }
+        const uint32_t tS = tbase, tP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
+        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma);
         for (int m = 0; ok && m < M; ++m) {
             const int st = m % kDkStages;
+            if (!(ok = mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
             if (m > 0) {
+                // finish item m-1 first: its P^T / dS^T live in the columns S/dP(m) overwrite
                 const int mp = m - 1, sp = mp % kDkStages;
                 if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
+                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
+                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
                 mma_commit(b_qe + sp);
-                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
-                mma_commit(b_pdfree);
-                mma_commit(b_oe + sp);
             }
-            if (!(ok = mbar_wait(b_xs, m & 1, s_abort, a.err, kSiteDkMma))) break;
-            if (!(ok = mbar_wait(b_of + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
-            issue_ss(tX, aV, aO + st * kTile, idS);  // dP^T(m) = V dO^T
-            mma_commit(b_d);
-            if (m + 1 < M) {
-                const int sn = (m + 1) % kDkStages;
-                if (!(ok = mbar_wait(b_qf + sn, ((m + 1) / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
-                if (!(ok = mbar_wait(b_xd, m & 1, s_abort, a.err, kSiteDkMma))) break;
-                tc_fence_after();
-                issue_ss(tX, aK, aQ + sn * kTile, idS);  // S^T(m+1)
-                mma_commit(b_s);
-            }
+            issue_ss(tS, aK, aQ + st * kTile, idS);  // S^T = K Q^T
+            issue_ss(tP, aV, aO + st * kTile, idS);  // dP^T = V dO^T
+            mma_commit(b_sf);
+            mma_started = 1;
         }
         if (ok) {
             const int mp = M - 1, sp = mp % kDkStages;
             if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
-                issue_ts(tdK, tDt, aQ + sp * kTile, idA, mp > 0);
+                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);
+                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);
                 mma_commit(b_qe + sp);
-                issue_ts(tdV, tPt, aO + sp * kTile, idA, mp > 0);
-                mma_commit(b_pdfree);
-                mma_commit(b_oe + sp);
                 mma_commit(b_acc);
             }
         }
@@ -340,70 +319,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int m = 0; m < M; ++m) {
             const int st = m % kDkStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(b_s, m & 1, s_abort, a.err, kSiteDkSoft) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            // S^T -> P^T (fp32 kept for dS^T); the LSE row came with Q
-            float pf[64];
-            {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tl + ch * 64, r0);
-                tmem_ld32(tl + ch * 64 + 32, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(b_xs);  // X may take dP^T now
-                const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
+            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
+            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
 #pragma unroll
-                for (int t4 = 0; t4 < 16; ++t4) {
-                    const float4 l4 = sl4[t4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
+                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
+                tmem_wait_ld();
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pp[4], dd[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int t = t4 * 4 + e;
-                        const float sv = __uint_as_float(t < 32 ? r0[t] : r1[t - 32]);
-                        pf[t] = key_ok ? ex2(fmaf(sv, sl2, -lv[e])) : 0.f;
+                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
+                        pp[e] = pr;
+                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
                     }
-                }
-            }
-            uint32_t pw[32];
-#pragma unroll
-            for (int t = 0; t < 32; ++t) pw[t] = pack2<T>(pf[2 * t], pf[2 * t + 1]);
-            if (m > 0) {  // P^T / dS^T regions were read by dV/dK(m-1)
-                ok = __all_sync(0xffffffffu, mbar_wait(b_pdfree, (m - 1) & 1, s_abort, a.err, kSiteDkSoft));
-                if (!ok) break;
-                tc_fence_after();
-            }
-            tmem_st32(tl + 128 + ch * 32, pw);
-            // dP^T -> dS^T; Dvec came with dO
-            ok = __all_sync(0xffffffffu, mbar_wait(b_d, m & 1, s_abort, a.err, kSiteDkSoft) &&
-                                             mbar_wait(b_of + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t dw[32];
-            {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tl + ch * 64, r0);
-                tmem_ld32(tl + ch * 64 + 32, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(b_xd);  // X may take S^T of the next item now
-                const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
-#pragma unroll
-                for (int t4 = 0; t4 < 16; ++t4) {
-                    const float4 d4 = sd4[t4];
-                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float dd[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int t = t4 * 4 + e;
-                        dd[e] = pf[t] * (__uint_as_float(t < 32 ? r0[t] : r1[t - 32]) - dvv[e]);
-                    }
+                    pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
+                    pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
                     dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
                     dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
+                // into this warp's own, already read columns
+                tmem_st16(tl + ch * 64 + q2 * 16, pw);
+                tmem_st16(tl + 128 + ch * 64 + q2 * 16, dw);
             }
-            tmem_st32(tl + 192 + ch * 32, dw);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_pd);
@@ -452,10 +400,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int never = 0;
         if (warp == kProdWarp && lane == 0) {
             if (issued_kv) mbar_wait(b_kv, 0, &never, nullptr, 0, 200000000ull);
-            for (int s = 0; s < kDkStages; ++s) {
+            for (int s = 0; s < kDkStages; ++s)
                 if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
-                if (issued_o[s]) mbar_wait(b_of + s, (issued_o[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
-            }
         }
         if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);
@@ -480,13 +426,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // on the tensor core while this chunk's dS is computed; dQ += dS K reads
 // dS from TMEM. MMA order: S/dP(c), dQ(c-1), S/dP(c+1), dQ(c), ...
 // K chunks stay until dQ += dS K has read them, one chunk after S, so K
-// has three stages; V is free right after dP and has one.
+// has three stages; V, free right after dP, has two. The chunk sequence
+// (selected tiles in ascending order, each cut into 128-key chunks with
+// valid keys) is walked from the index by each role, not stored.
 // TMEM columns: S [0,128), dP [128,256), dQ [256,384), dS buffers
 // [384,448) and [448,512).
-constexpr int kDqKStages = 3;
+constexpr int kDqKStages = 3, kDqVStages = 2;
 constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = (2 + kDqKStages) * kTile;
-constexpr int kDqOffCtl = kDqOffV + kTile;
-constexpr size_t kDqSmem = kDqOffCtl + 256 + kMaxChunks * 6;
+constexpr int kDqOffCtl = kDqOffV + kDqVStages * kTile;
+constexpr size_t kDqSmem = kDqOffCtl + 256;
+
+// Walks the 128-key chunks of a query tile's selected KV tiles.
+struct ChunkIter {
+    const int *idx;
+    int cnt, per, n, sub, j, kvv;
+};
+__device__ __forceinline__ bool chunk_next(const Prob &p, int b, ChunkIter &it, int &row, int &valid) {
+    while (it.n < it.cnt) {
+        if (it.sub == 0) {
+            it.j = it.idx[it.n];
+            it.kvv = kv_valid(p, b, it.j);
+        }
+        const int v = it.kvv - it.sub * 128;
+        if (it.sub < it.per && v > 0) {
+            row = it.j * p.tile_kv + it.sub * 128;
+            valid = v < 128 ? v : 128;
+            ++it.sub;
+            return true;
+        }
+        ++it.n;
+        it.sub = 0;
+    }
+    return false;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -501,13 +473,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
-    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 8;
-    uint64_t *b_sf = bars + 9, *b_sfree = bars + 10, *b_dsf = bars + 11, *b_dq = bars + 12, *b_fin = bars + 14;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 15);
+    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 9;
+    uint64_t *b_sf = bars + 11, *b_sfree = bars + 12, *b_dsf = bars + 13, *b_dq = bars + 14, *b_fin = bars + 16;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 17);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
-    int *s_crow = reinterpret_cast<int *>(sm + kDqOffCtl + 256);
-    short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int subs = p.tile_q >> 7;
@@ -531,8 +501,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b_kf + s, 1);
             mbar_init(b_ke + s, 1);
         }
-        mbar_init(b_vf, 1);
-        mbar_init(b_ve, 1);
+        for (int s = 0; s < kDqVStages; ++s) {
+            mbar_init(b_vf + s, 1);
+            mbar_init(b_ve + s, 1);
+        }
         for (int s = 0; s < 2; ++s) mbar_init(b_dq + s, 1);
         mbar_init(b_sf, 1);
         mbar_init(b_sfree, 256);
@@ -542,34 +514,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_mbar_init();
     }
     if (warp == kProdWarp) {
+        // number of 128-key chunks with valid keys
         const int cnt = a.q_cnt[qrow];
         const int *idx = a.q_idx + qrow * a.cap;
         const int per = p.tile_kv >> 7;
         int total = 0;
-        for (int n0 = 0; n0 < cnt; n0 += 32) {
-            const int n = n0 + lane;
-            int jj = 0, kvv = 0, nc = 0;
-            if (n < cnt) {
-                jj = idx[n];
-                kvv = kv_valid(p, b, jj);
-                nc = min(per, (kvv + 127) >> 7);
-            }
-            int inc = nc;
+        for (int n = lane; n < cnt; n += 32) total += min(per, (kv_valid(p, b, idx[n]) + 127) >> 7);
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, inc, off);
-                if (lane >= off) inc += y;
-            }
-            const int base = total + inc - nc;
-            for (int c = 0; c < nc; ++c) {
-                const int pos = base + c;
-                if (pos < kMaxChunks) {
-                    s_crow[pos] = jj * p.tile_kv + c * 128;
-                    s_cval[pos] = (short)min(128, kvv - c * 128);
-                }
-            }
-            total += __shfl_sync(0xffffffffu, inc, 31);
-        }
+        for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
     } else if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
@@ -581,7 +533,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int N = *s_nchunk;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_q = 0, issued_k[kDqKStages] = {0, 0, 0}, issued_v = 0, mma_started = 0;
+    int issued_q = 0, issued_k[kDqKStages] = {0, 0, 0}, issued_v[kDqVStages] = {0, 0}, mma_started = 0;
+    ChunkIter cit{a.q_idx + qrow * a.cap, a.q_cnt[qrow], p.tile_kv >> 7, 0, 0, 0, 0};
 
     if (warp == kProdWarp && lane == 0 && N > 0) {
         mbar_expect_tx(b_q, 2 * kTile);
@@ -591,19 +544,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
-            const int sk = c % kDqKStages;
-            const int kr = kvb + s_crow[c];
+            int crow = 0, cval = 0;
+            if (!chunk_next(p, b, cit, crow, cval)) break;
+            const int sk = c % kDqKStages, sv = c % kDqVStages;
+            const int kr = kvb + crow;
             if (c >= kDqKStages && !mbar_wait(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
                 break;
             mbar_expect_tx(b_kf + sk, kTile);
             tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
             tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
             issued_k[sk]++;
-            if (c >= 1 && !mbar_wait(b_ve, (c - 1) & 1, s_abort, a.err, kSiteDqProd)) break;
-            mbar_expect_tx(b_vf, kTile);
-            tma_load_4d(sV, &tv, b_vf, 0, kr, hk, bc);
-            tma_load_4d(sV + kBox, &tv, b_vf, 64, kr, hk, bc);
-            issued_v++;
+            if (c >= kDqVStages && !mbar_wait(b_ve + sv, ((c / kDqVStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
+                break;
+            mbar_expect_tx(b_vf + sv, kTile);
+            tma_load_4d(sV + sv * kTile, &tv, b_vf + sv, 0, kr, hk, bc);
+            tma_load_4d(sV + sv * kTile + kBox, &tv, b_vf + sv, 64, kr, hk, bc);
+            issued_v[sv]++;
         }
     } else if (warp == kMmaWarp && lane == 0 && N > 0) {
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
@@ -614,13 +570,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; ok && c < N; ++c) {
             const int sk = c % kDqKStages;
             if (!(ok = mbar_wait(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
-            if (!(ok = mbar_wait(b_vf, c & 1, s_abort, a.err, kSiteDqMma))) break;
+            const int sv = c % kDqVStages;
+            if (!(ok = mbar_wait(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
             if (c > 0 && !(ok = mbar_wait(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tS, aQ, aK + sk * kTile, idS);  // S = Q K^T
-            issue_ss(tP, aO, aV, idS);               // dP = dO V^T
+            issue_ss(tS, aQ, aK + sk * kTile, idS);          // S = Q K^T
+            issue_ss(tP, aO, aV + sv * kTile, idS);          // dP = dO V^T
             mma_commit(b_sf);
-            mma_commit(b_ve);
+            mma_commit(b_ve + sv);
             mma_started = 1;
             if (c > 0) {
                 const int cp = c - 1, skp = cp % kDqKStages;
@@ -662,7 +619,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(b_sfree);  // S and dP of this chunk are in registers
-            const int valid = s_cval[c] - ch * 64;
+            int crow = 0, cval = 0;
+            chunk_next(p, b, cit, crow, cval);
+            const int valid = cval - ch * 64;
             uint32_t dw[32];
 #pragma unroll
             for (int t2 = 0; t2 < 32; ++t2) {
@@ -731,7 +690,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (issued_q) mbar_wait(b_q, 0, &never, nullptr, 0, 200000000ull);
             for (int s = 0; s < kDqKStages; ++s)
                 if (issued_k[s]) mbar_wait(b_kf + s, (issued_k[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
-            if (issued_v) mbar_wait(b_vf, (issued_v - 1) & 1, &never, nullptr, 0, 200000000ull);
+            for (int s = 0; s < kDqVStages; ++s)
+                if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
         if (warp == kMmaWarp && lane == 0 && mma_started) {
             mma_commit(b_fin);

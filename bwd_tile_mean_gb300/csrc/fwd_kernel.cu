@@ -23,11 +23,11 @@
 // Per chunk c the MMAs go S_A(c) = Q_A K_c^T, O_B += P_B(c-1) V_(c-1),
 // S_B(c) = Q_B K_c^T, O_A += P_A(c) V_c, so each group's softmax runs while
 // the tensor core works for the other group. The softmax reads S from
-// TMEM twice (row max, then probabilities), masks keys past the chunk's
-// valid count, keeps a running max in the exp2 domain (rescaling O in TMEM
-// only when the max grows by more than 2^8), and writes P back into the
-// first 64 columns of its S buffer as packed 16-bit pairs; the PV MMA reads
-// P from TMEM as its A operand. The epilogue normalises O, adds gate * c
+// TMEM once, computing probabilities against the running max in the exp2
+// domain (keys past the chunk's valid count masked); only rows whose max
+// grows by more than 2^8 (and the first chunk) read S again with the new
+// max and rescale O in TMEM. P goes back into the first 64 columns of the S
+// buffer as packed 16-bit pairs; the PV MMA reads it as its A operand. The epilogue normalises O, adds gate * c
 // when gated, and writes O and the LSE.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "sm103_ptx.cuh"
@@ -250,53 +250,64 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int valid = s_cval[c];
-            // pass 1: row max of the (masked) scaled scores
-            float mx = -INFINITY;
+            // One read of S: probabilities against the running max, packed
+            // in registers; rows whose max grew by more than 2^8 (always the
+            // first chunk) recompute from S with the new max.
+            uint32_t w[64];
+            float mx = -INFINITY, ls = 0.f;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t rr[32];
                 tmem_ld32(tl + cS + q4 * 32, rr);
                 tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (valid >= 128 || q4 * 32 + j < valid) mx = fmaxf(mx, __uint_as_float(rr[j]));
-            }
-            mx *= sl2;
-            float alpha = 1.f;
-            bool resc = false;
-            if (c == 0) {
-                m_ref = mx;
-            } else if (mx > m_ref + 8.f) {
-                alpha = ex2(m_ref - mx);
-                m_ref = mx;
-                resc = true;
-            }
-            // pass 2: probabilities, packed to 16 bits into S's first 64 columns
-            float ls = 0.f;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t rr[32];
-                tmem_ld32(tl + cS + q4 * 32, rr);
-                tmem_wait_ld();
-                uint32_t w[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int c0 = q4 * 32 + 2 * j;
                     const bool v0 = valid >= 128 || c0 < valid, v1 = valid >= 128 || c0 + 1 < valid;
-                    const float p0 = v0 ? ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -m_ref)) : 0.f;
-                    const float p1 = v1 ? ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -m_ref)) : 0.f;
+                    const float x0 = __uint_as_float(rr[2 * j]) * sl2, x1 = __uint_as_float(rr[2 * j + 1]) * sl2;
+                    if (v0) mx = fmaxf(mx, x0);
+                    if (v1) mx = fmaxf(mx, x1);
+                    const float p0 = v0 ? ex2(x0 - m_ref) : 0.f;
+                    const float p1 = v1 ? ex2(x1 - m_ref) : 0.f;
                     ls += p0 + p1;
-                    w[j] = pack2<T>(p0, p1);
+                    w[q4 * 16 + j] = pack2<T>(p0, p1);
                 }
-                tmem_st16(tl + cS + q4 * 16, w);
             }
+            float alpha = 1.f;
+            const bool resc = (c == 0) || (mx > m_ref + 8.f);
+            if (__any_sync(0xffffffffu, resc)) {
+                if (resc) {
+                    alpha = (c == 0) ? 0.f : ex2(m_ref - mx);
+                    m_ref = mx;
+                    ls = 0.f;
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t rr[32];
+                    tmem_ld32(tl + cS + q4 * 32, rr);
+                    tmem_wait_ld();
+                    if (!resc) continue;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c0 = q4 * 32 + 2 * j;
+                        const bool v0 = valid >= 128 || c0 < valid, v1 = valid >= 128 || c0 + 1 < valid;
+                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -m_ref)) : 0.f;
+                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -m_ref)) : 0.f;
+                        ls += p0 + p1;
+                        w[q4 * 16 + j] = pack2<T>(p0, p1);
+                    }
+                }
+            }
+            // P over S's first 64 columns (all of S has been read)
+            tmem_st32(tl + cS, *reinterpret_cast<uint32_t(*)[32]>(w));
+            tmem_st32(tl + cS + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
             l = l * alpha + ls;
             if (c > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (c - 1) & 1, s_abort, a.err, kSiteSoft));
                 if (!ok) break;
                 tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            if (c > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t o[32];
