@@ -250,57 +250,91 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int valid = s_cval[c];
-            // One read of S: probabilities against the running max, packed
-            // in registers; rows whose max grew by more than 2^8 (always the
-            // first chunk) recompute from S with the new max.
-            uint32_t w[64];
-            float mx = -INFINITY, ls = 0.f;
+            // One pipelined pass over S (32-column slices, the next slice's
+            // TMEM load in flight while this one is computed). Probabilities
+            // use the running max as it stands; a row whose slice max exceeds
+            // it by more than 2^8 (always the first slice of the first chunk)
+            // raises it, recomputes that slice from the scores still in
+            // registers, and rescales the P slices already written and, once
+            // per chunk, l and O. P goes to S's first 64 columns, slice q to
+            // columns [16q, 16q + 16), which slice q/2 has already vacated.
+            // The scale is positive, so the max is taken on raw scores.
+            float alpha = 1.f, ls = 0.f;
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tl + cS, ra);
+            tmem_wait_ld_regs(ra);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t rr[32];
-                tmem_ld32(tl + cS + q4 * 32, rr);
-                tmem_wait_ld();
+                uint32_t(&cur)[32] = (q4 & 1) ? rb : ra;
+                uint32_t(&nxt)[32] = (q4 & 1) ? ra : rb;
+                if (q4 < 3) tmem_ld32(tl + cS + (q4 + 1) * 32, nxt);
+                if (valid < (q4 + 1) * 32) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c0 = q4 * 32 + 2 * j;
-                    const bool v0 = valid >= 128 || c0 < valid, v1 = valid >= 128 || c0 + 1 < valid;
-                    const float x0 = __uint_as_float(rr[2 * j]) * sl2, x1 = __uint_as_float(rr[2 * j + 1]) * sl2;
-                    if (v0) mx = fmaxf(mx, x0);
-                    if (v1) mx = fmaxf(mx, x1);
-                    const float p0 = v0 ? ex2(x0 - m_ref) : 0.f;
-                    const float p1 = v1 ? ex2(x1 - m_ref) : 0.f;
-                    ls += p0 + p1;
-                    w[q4 * 16 + j] = pack2<T>(p0, p1);
+                    for (int j = 0; j < 32; ++j)
+                        if (q4 * 32 + j >= valid) cur[j] = __float_as_uint(-INFINITY);
                 }
-            }
-            float alpha = 1.f;
-            const bool resc = (c == 0) || (mx > m_ref + 8.f);
-            if (__any_sync(0xffffffffu, resc)) {
-                if (resc) {
-                    alpha = (c == 0) ? 0.f : ex2(m_ref - mx);
-                    m_ref = mx;
-                    ls = 0.f;
-                }
+                float t[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t rr[32];
-                    tmem_ld32(tl + cS + q4 * 32, rr);
-                    tmem_wait_ld();
-                    if (!resc) continue;
+                for (int j = 0; j < 16; ++j) t[j] = fmaxf(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1]));
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+                const float mxs = t[0] * sl2;
+                uint32_t w16[16];
+                float s0 = 0.f, s1 = 0.f;
+                {
+                    const float nm = -m_ref;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int c0 = q4 * 32 + 2 * j;
-                        const bool v0 = valid >= 128 || c0 < valid, v1 = valid >= 128 || c0 + 1 < valid;
-                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(rr[2 * j]), sl2, -m_ref)) : 0.f;
-                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(rr[2 * j + 1]), sl2, -m_ref)) : 0.f;
-                        ls += p0 + p1;
-                        w[q4 * 16 + j] = pack2<T>(p0, p1);
+                        const float p0 = ex2(fmaf(__uint_as_float(cur[2 * j]), sl2, nm));
+                        const float p1 = ex2(fmaf(__uint_as_float(cur[2 * j + 1]), sl2, nm));
+                        s0 += p0;
+                        s1 += p1;
+                        w16[j] = pack2<T>(p0, p1);
                     }
                 }
+                const bool grow = mxs > m_ref + 8.f;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float a2 = grow ? ex2(m_ref - mxs) : 1.f;
+                    if (grow) {
+                        m_ref = mxs;
+                        ls *= a2;
+                        alpha *= a2;
+                        s0 = s1 = 0.f;
+                        const float nm = -m_ref;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = ex2(fmaf(__uint_as_float(cur[2 * j]), sl2, nm));
+                            const float p1 = ex2(fmaf(__uint_as_float(cur[2 * j + 1]), sl2, nm));
+                            s0 += p0;
+                            s1 += p1;
+                            w16[j] = pack2<T>(p0, p1);
+                        }
+                    }
+                    if (q4 > 0) {  // rescale the P slices written so far (rare)
+#pragma unroll 1
+                        for (int qq = 0; qq < q4; ++qq) {
+                            uint32_t pr[32];
+                            tmem_wait_st();
+                            tmem_ld32(tl + cS + qq * 16 - (qq & 1) * 16, pr);  // 32 columns covering slice qq
+                            tmem_wait_ld_regs(pr);
+                            uint32_t r16[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 f = unpack2<T>(pr[(qq & 1) * 16 + e]);
+                                r16[e] = pack2<T>(f.x * a2, f.y * a2);
+                            }
+                            tmem_st16(tl + cS + qq * 16, r16);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                ls += s0 + s1;
+                tmem_st16(tl + cS + q4 * 16, w16);
+                if (q4 < 3) tmem_wait_ld_regs(nxt);
             }
-            // P over S's first 64 columns (all of S has been read)
-            tmem_st32(tl + cS, *reinterpret_cast<uint32_t(*)[32]>(w));
-            tmem_st32(tl + cS + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
+            const bool resc = alpha != 1.f;
             l = l * alpha + ls;
             if (c > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (c - 1) & 1, s_abort, a.err, kSiteSoft));
