@@ -23,11 +23,13 @@
 // Per chunk c the MMAs go S_A(c) = Q_A K_c^T, O_B += P_B(c-1) V_(c-1),
 // S_B(c) = Q_B K_c^T, O_A += P_A(c) V_c, so each group's softmax runs while
 // the tensor core works for the other group. The softmax reads S from
-// TMEM once, computing probabilities against the running max in the exp2
-// domain (keys past the chunk's valid count masked); only rows whose max
-// grows by more than 2^8 (and the first chunk) read S again with the new
-// max and rescale O in TMEM. P goes back into the first 64 columns of the S
-// buffer as packed 16-bit pairs; the PV MMA reads it as its A operand. The epilogue normalises O, adds gate * c
+// TMEM once, in 32-column slices with the next slice's load in flight,
+// computing probabilities against the running max in the exp2 domain (keys
+// past the chunk's valid count masked); only rows whose max grows by more
+// than 2^8 (always the first slice of the first chunk) recompute the slice
+// with the new max and rescale the P already written and O in TMEM. P goes
+// back into the first 64 columns of the S buffer as packed 16-bit pairs; the
+// PV MMA reads it as its A operand. The epilogue normalises O, adds gate * c
 // when gated, and writes O and the LSE.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "sm103_ptx.cuh"
