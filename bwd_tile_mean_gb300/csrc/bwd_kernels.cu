@@ -101,7 +101,7 @@ __device__ __forceinline__ void issue_ss(uint32_t d, uint32_t aA, uint32_t aB, u
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t o = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_f16_ss(d, sdesc_sw128(aA + o, 16, 1024), sdesc_sw128(aB + o, 16, 1024), idesc, kk > 0);
+        mma_f16_ss_w(d, sdesc_sw128(aA + o, 16, 1024), sdesc_sw128(aB + o, 16, 1024), idesc, kk > 0);
     }
 }
 // D (+)= A B with A [128 x 128] in TMEM (packed 16-bit pairs, 8 columns per
@@ -110,7 +110,7 @@ __device__ __forceinline__ void issue_ss(uint32_t d, uint32_t aA, uint32_t aB, u
 __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_f16_ts(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ts_w(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 // As issue_ts, with the packed A operand held in two 32-column pieces:
@@ -119,7 +119,7 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
 __device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_f16_ts(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
+        mma_f16_ts_w(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
                    (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -274,39 +274,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issued[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
-    } else if (warp == kMmaWarp && lane == 0 && M > 0) {
-        // ---------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp && M > 0) {
+        // ------------------------------------- MMA issuer (whole warp, lane 0 issues)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
         const uint32_t tS = tbase, tP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
-        bool ok = mbar_wait(b_kv, 0, s_abort, a.err, kSiteDkMma);
+        bool ok = mbar_wait_warp(b_kv, 0, s_abort, a.err, kSiteDkMma);
         for (int m = 0; ok && m < M; ++m) {
             const int st = m % kDkStages;
-            if (!(ok = mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
+            if (!(ok = mbar_wait_warp(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
             if (m > 0) {
                 // finish item m-1 first: its P^T / dS^T live in the columns S/dP(m) overwrite
                 const int mp = m - 1, sp = mp % kDkStages;
-                if (!(ok = mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
+                if (!(ok = mbar_wait_warp(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
                 issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
                 issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
-                mma_commit(b_qe + sp);
+                mma_commit_w(b_qe + sp);
             }
             tc_fence_after();
             issue_ss(tS, aK, aQ + st * kTile, idS);  // S^T = K Q^T
             issue_ss(tP, aV, aO + st * kTile, idS);  // dP^T = V dO^T
-            mma_commit(b_sf);
+            mma_commit_w(b_sf);
             mma_started = 1;
         }
         if (ok) {
             const int mp = M - 1, sp = mp % kDkStages;
-            if (mbar_wait(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
+            if (mbar_wait_warp(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
                 tc_fence_after();
                 issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);
                 issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);
-                mma_commit(b_qe + sp);
-                mma_commit(b_acc);
+                mma_commit_w(b_qe + sp);
+                mma_commit_w(b_acc);
             }
         }
     } else if (warp < 8) {
@@ -561,40 +561,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_4d(sV + sv * kTile + kBox, &tv, b_vf + sv, 64, kr, hk, bc);
             issued_v[sv]++;
         }
-    } else if (warp == kMmaWarp && lane == 0 && N > 0) {
+    } else if (warp == kMmaWarp && N > 0) {
+        // ------------------------------------- MMA issuer (whole warp, lane 0 issues)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idQ = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV);
         const uint32_t tS = tbase, tP = tbase + 128, tQ = tbase + 256, tX = tbase + 384;
-        bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteDqMma);
+        bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
             const int sk = c % kDqKStages;
-            if (!(ok = mbar_wait(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (!(ok = mbar_wait_warp(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
             const int sv = c % kDqVStages;
-            if (!(ok = mbar_wait(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
-            if (c > 0 && !(ok = mbar_wait(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (!(ok = mbar_wait_warp(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (c > 0 && !(ok = mbar_wait_warp(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
             issue_ss(tS, aQ, aK + sk * kTile, idS);          // S = Q K^T
             issue_ss(tP, aO, aV + sv * kTile, idS);          // dP = dO V^T
-            mma_commit(b_sf);
-            mma_commit(b_ve + sv);
+            mma_commit_w(b_sf);
+            mma_commit_w(b_ve + sv);
             mma_started = 1;
             if (c > 0) {
                 const int cp = c - 1, skp = cp % kDqKStages;
-                if (!(ok = mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma))) break;
+                if (!(ok = mbar_wait_warp(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma))) break;
                 tc_fence_after();
                 issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);  // dQ += dS K
-                mma_commit(b_dq + (cp & 1));
-                mma_commit(b_ke + skp);
+                mma_commit_w(b_dq + (cp & 1));
+                mma_commit_w(b_ke + skp);
             }
         }
         if (ok) {
             const int cp = N - 1, skp = cp % kDqKStages;
-            if (mbar_wait(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma)) {
+            if (mbar_wait_warp(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma)) {
                 tc_fence_after();
                 issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);
-                mma_commit(b_dq + (cp & 1));
-                mma_commit(b_ke + skp);
+                mma_commit_w(b_dq + (cp & 1));
+                mma_commit_w(b_ke + skp);
             }
         }
     } else if (warp < 8) {

@@ -60,7 +60,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t aQ, uint32_t aK, u
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_f16_ss(d, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), idesc, kk > 0);
+        mma_f16_ss_w(d, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), idesc, kk > 0);
     }
 }
 // O += P V: A = P in TMEM (128 keys = 64 packed columns, 8 per K = 16
@@ -70,7 +70,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t aQ, uint32_t aK, u
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t aV, uint32_t idesc, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_f16_ts(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ts_w(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 template <typename T>
@@ -196,46 +196,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
             issued_v[s]++;
         }
-    } else if (warp == kFwdMmaWarp && lane == 0 && N > 0) {
-        // ----------------------------------------------------- MMA issuer
+    } else if (warp == kFwdMmaWarp && N > 0) {
+        // ------------------------------------- MMA issuer (whole warp, lane 0 issues)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
         const uint32_t idO = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
         const uint32_t tS[2] = {tbase, tbase + 128}, tO[2] = {tbase + 256, tbase + 384};
-        bool ok = mbar_wait(b_q, 0, s_abort, a.err, kSiteMma);
+        bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteMma);
         for (int c = 0; ok && c < N; ++c) {
             const int s = c & 1, sp = (c - 1) & 1;
-            if (!(ok = mbar_wait(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
+            if (!(ok = mbar_wait_warp(b_kf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
             tc_fence_after();
             issue_qk(tS[0], aQ, aK + s * kTile, idS);  // S_A(c); P_A(c-1) was consumed by PV_A(c-1)
-            mma_commit(b_sf + 0);
+            mma_commit_w(b_sf + 0);
             mma_started = 1;
             if (has_b) {
                 if (c > 0) {
-                    if (!(ok = mbar_wait(b_pf + 1, (c - 1) & 1, s_abort, a.err, kSiteMma))) break;
+                    if (!(ok = mbar_wait_warp(b_pf + 1, (c - 1) & 1, s_abort, a.err, kSiteMma))) break;
                     tc_fence_after();
                     issue_pv(tO[1], tS[1], aV + sp * kTile, idO, c - 1 > 0);  // O_B += P_B(c-1) V_(c-1)
-                    mma_commit(b_od + 1);
-                    mma_commit(b_ve + sp);
+                    mma_commit_w(b_od + 1);
+                    mma_commit_w(b_ve + sp);
                 }
                 issue_qk(tS[1], aQ + kTile, aK + s * kTile, idS);  // S_B(c)
-                mma_commit(b_sf + 1);
+                mma_commit_w(b_sf + 1);
             }
-            mma_commit(b_ke + s);  // K_c is read by the S MMAs only
-            if (!(ok = mbar_wait(b_pf + 0, c & 1, s_abort, a.err, kSiteMma))) break;
-            if (!(ok = mbar_wait(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
+            mma_commit_w(b_ke + s);  // K_c is read by the S MMAs only
+            if (!(ok = mbar_wait_warp(b_pf + 0, c & 1, s_abort, a.err, kSiteMma))) break;
+            if (!(ok = mbar_wait_warp(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
             tc_fence_after();
             issue_pv(tO[0], tS[0], aV + s * kTile, idO, c > 0);  // O_A += P_A(c) V_c
-            mma_commit(b_od + 0);
-            if (!has_b) mma_commit(b_ve + s);
+            mma_commit_w(b_od + 0);
+            if (!has_b) mma_commit_w(b_ve + s);
         }
         if (ok && has_b) {
             const int sp = (N - 1) & 1;
-            if (mbar_wait(b_pf + 1, (N - 1) & 1, s_abort, a.err, kSiteMma)) {
+            if (mbar_wait_warp(b_pf + 1, (N - 1) & 1, s_abort, a.err, kSiteMma)) {
                 tc_fence_after();
                 issue_pv(tO[1], tS[1], aV + sp * kTile, idO, N - 1 > 0);
-                mma_commit(b_od + 1);
-                mma_commit(b_ve + sp);
+                mma_commit_w(b_od + 1);
+                mma_commit_w(b_ve + sp);
             }
         }
     } else if (warp < 8 && (warp < 4 || has_b)) {
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             uint32_t r16[16];
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
-                                const float2 f = unpack2<T>(pr[(qq & 1) * 16 + e]);
+                                const float2 f = unpack2<T>((qq & 1) ? pr[16 + e] : pr[e]);
                                 r16[e] = pack2<T>(f.x * a2, f.y * a2);
                             }
                             tmem_st16(tl + cS + qq * 16, r16);

@@ -51,9 +51,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // device status word records a failure anywhere in the grid; on a timeout
 // it raises *abort and records `site` in the device status word.
 // Returns false when the wait did not complete.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                       unsigned *err, unsigned site,
-                                       uint64_t limit_ns = 2000000000ull) {
+static __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                 unsigned *err, unsigned site,
+                                                 uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -166,6 +166,47 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Warp-wide forms of the two MMAs and the commit: the whole warp executes
+// them with the same operands (kept warp-uniform) and lane 0 alone issues,
+// by predicate rather than by branch. Issuing from a warp whose control flow
+// stays uniform keeps the MMA stream dense; lane 0 must also be the lane
+// that commits (mma_commit_w, or mma_commit from lane 0).
+__device__ __forceinline__ void mma_f16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
+        : "memory");
+}
+// Bounded wait taken by a whole warp; true only if every lane saw the phase.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, unsigned *err,
+                                               unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, site));
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 ops of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
