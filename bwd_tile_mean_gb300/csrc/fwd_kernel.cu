@@ -22,14 +22,14 @@
 //   warp 9      allocates TMEM, then one lane issues the MMAs.
 // Per chunk c the MMAs go S_A(c) = Q_A K_c^T, O_B += P_B(c-1) V_(c-1),
 // S_B(c) = Q_B K_c^T, O_A += P_A(c) V_c, so each group's softmax runs while
-// the tensor core works for the other group. The softmax reads S from
-// TMEM once, in 32-column slices with the next slice's load in flight,
-// computing probabilities against the running max in the exp2 domain (keys
-// past the chunk's valid count masked); only rows whose max grows by more
-// than 2^8 (always the first slice of the first chunk) recompute the slice
-// with the new max and rescale the P already written and O in TMEM. P goes
-// back into the first 64 columns of the S buffer as packed 16-bit pairs; the
-// PV MMA reads it as its A operand. The epilogue normalises O, adds gate * c
+// the tensor core works for the other group. The softmax loads a whole row
+// of S (128 scores) from TMEM with one wait, takes its max, and computes
+// probabilities in the exp2 domain against the running max (keys past the
+// chunk's valid count masked; scale-and-subtract and the row sum on paired
+// f32 instructions); only rows whose max grows by more than 2^8 (always the
+// first chunk) move the running max and rescale l and O in TMEM. P goes back
+// into the first 64 columns of the S buffer as packed 16-bit pairs; the PV
+// MMA reads it as its A operand. The epilogue normalises O, adds gate * c
 // when gated, and writes O and the LSE.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "sm103_ptx.cuh"
@@ -252,90 +252,62 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int valid = s_cval[c];
-            // One pipelined pass over S (32-column slices, the next slice's
-            // TMEM load in flight while this one is computed). Probabilities
-            // use the running max as it stands; a row whose slice max exceeds
-            // it by more than 2^8 (always the first slice of the first chunk)
-            // raises it, recomputes that slice from the scores still in
-            // registers, and rescales the P slices already written and, once
-            // per chunk, l and O. P goes to S's first 64 columns, slice q to
-            // columns [16q, 16q + 16), which slice q/2 has already vacated.
-            // The scale is positive, so the max is taken on raw scores.
-            float alpha = 1.f, ls = 0.f;
-            uint32_t ra[32], rb[32];
-            tmem_ld32(tl + cS, ra);
-            tmem_wait_ld_regs(ra);
+            // The whole row of S (128 scores) comes into registers with one
+            // wait; its max is taken first (the scale is positive, so on raw
+            // scores). A row whose max exceeds the running max by more than
+            // 2^8 (always the first chunk) raises it and rescales l and O;
+            // otherwise probabilities stay relative to the running max. P
+            // goes, packed, to the first 64 columns of the S buffer.
+            uint32_t sr[128];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tl + cS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + q4 * 32));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(sr + q4 * 32));
+            if (valid < 128) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+            }
+            float mx;
+            {
+                float u[43], v[15], w5[5];
+#pragma unroll
+                for (int k = 0; k < 42; ++k)
+                    u[k] = fmax3(__uint_as_float(sr[3 * k]), __uint_as_float(sr[3 * k + 1]), __uint_as_float(sr[3 * k + 2]));
+                u[42] = fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127]));
+#pragma unroll
+                for (int k = 0; k < 14; ++k) v[k] = fmax3(u[3 * k], u[3 * k + 1], u[3 * k + 2]);
+                v[14] = u[42];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) w5[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+                mx = fmaxf(fmax3(w5[0], w5[1], w5[2]), fmaxf(w5[3], w5[4])) * sl2;
+            }
+            float alpha = 1.f;
+            if (mx > m_ref + 8.f) {
+                alpha = ex2(m_ref - mx);  // 0 on the first chunk
+                m_ref = mx;
+            }
+            const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_ref, -m_ref);
+            uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t(&cur)[32] = (q4 & 1) ? rb : ra;
-                uint32_t(&nxt)[32] = (q4 & 1) ? ra : rb;
-                if (q4 < 3) tmem_ld32(tl + cS + (q4 + 1) * 32, nxt);
-                if (valid < (q4 + 1) * 32) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (q4 * 32 + j >= valid) cur[j] = __float_as_uint(-INFINITY);
-                }
-                float t[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) t[j] = fmaxf(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1]));
-#pragma unroll
-                for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
-                const float mxs = t[0] * sl2;
                 uint32_t w16[16];
-                float s0 = 0.f, s1 = 0.f;
-                {
-                    const float nm = -m_ref;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2(fmaf(__uint_as_float(cur[2 * j]), sl2, nm));
-                        const float p1 = ex2(fmaf(__uint_as_float(cur[2 * j + 1]), sl2, nm));
-                        s0 += p0;
-                        s1 += p1;
-                        w16[j] = pack2<T>(p0, p1);
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    const int e = q4 * 32 + 2 * j;
+                    const float2 x = f32x2_split(
+                        ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nm2));
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    if (j & 1)
+                        acc1 = fadd_x2(acc1, f32x2(p0, p1));
+                    else
+                        acc0 = fadd_x2(acc0, f32x2(p0, p1));
+                    w16[j] = pack2<T>(p0, p1);
                 }
-                const bool grow = mxs > m_ref + 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float a2 = grow ? ex2(m_ref - mxs) : 1.f;
-                    if (grow) {
-                        m_ref = mxs;
-                        ls *= a2;
-                        alpha *= a2;
-                        s0 = s1 = 0.f;
-                        const float nm = -m_ref;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2(fmaf(__uint_as_float(cur[2 * j]), sl2, nm));
-                            const float p1 = ex2(fmaf(__uint_as_float(cur[2 * j + 1]), sl2, nm));
-                            s0 += p0;
-                            s1 += p1;
-                            w16[j] = pack2<T>(p0, p1);
-                        }
-                    }
-                    if (q4 > 0) {  // rescale the P slices written so far (rare)
-#pragma unroll 1
-                        for (int qq = 0; qq < q4; ++qq) {
-                            uint32_t pr[32];
-                            tmem_wait_st();
-                            tmem_ld32(tl + cS + qq * 16 - (qq & 1) * 16, pr);  // 32 columns covering slice qq
-                            tmem_wait_ld_regs(pr);
-                            uint32_t r16[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float2 f = unpack2<T>((qq & 1) ? pr[16 + e] : pr[e]);
-                                r16[e] = pack2<T>(f.x * a2, f.y * a2);
-                            }
-                            tmem_st16(tl + cS + qq * 16, r16);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-                ls += s0 + s1;
                 tmem_st16(tl + cS + q4 * 16, w16);
-                if (q4 < 3) tmem_wait_ld_regs(nxt);
             }
+            const float2 s0 = f32x2_split(acc0), s1 = f32x2_split(acc1);
+            const float ls = (s0.x + s0.y) + (s1.x + s1.y);
             const bool resc = alpha != 1.f;
             l = l * alpha + ls;
             if (c > 0) {
