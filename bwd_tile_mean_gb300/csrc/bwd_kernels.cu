@@ -609,6 +609,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float dvv = N > 0 ? a.dvec[slot] : 0.f;
         bool ok = true;
         for (int c = 0; c < N; ++c) {
+            // the chunk's valid key count (index reads overlap the wait for S)
+            int crow = 0, cval = 0;
+            chunk_next(p, b, cit, crow, cval);
+            const int valid = cval - ch * 64;
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;
             tc_fence_after();
@@ -620,20 +624,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(b_sfree);  // S and dP of this chunk are in registers
-            int crow = 0, cval = 0;
-            chunk_next(p, b, cit, crow, cval);
-            const int valid = cval - ch * 64;
+            if (valid < 64) {  // keys past the valid count: P = 0
+#pragma unroll
+                for (int kk = 0; kk < 64; ++kk)
+                    if (kk >= valid) sr[kk] = __float_as_uint(-INFINITY);
+            }
+            // P = 2^(S scale log2e - LSE log2e), dS = P (dP - Dvec), on pairs
+            const uint64_t sc2 = f32x2(sl2, sl2), nl2 = f32x2(-l2, -l2), nd2 = f32x2(-dvv, -dvv);
             uint32_t dw[32];
 #pragma unroll
             for (int t2 = 0; t2 < 32; ++t2) {
-                float dd[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int kk = t2 * 2 + e;
-                    const float pr = kk < valid ? ex2(fmaf(__uint_as_float(sr[kk]), sl2, -l2)) : 0.f;
-                    dd[e] = pr * (__uint_as_float(dr[kk]) - dvv);
-                }
-                dw[t2] = pack2<T>(dd[0], dd[1]);
+                const float2 x = f32x2_split(
+                    ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2));
+                const uint64_t pp = f32x2(ex2(x.x), ex2(x.y));
+                const uint64_t dd = fmul_x2(pp, fadd_x2(f32x2(__uint_as_float(dr[2 * t2]), __uint_as_float(dr[2 * t2 + 1])), nd2));
+                const float2 d2 = f32x2_split(dd);
+                dw[t2] = pack2<T>(d2.x, d2.y);
             }
             if (c >= 2) {  // dS buffer c&1 was read by dQ(c-2)
                 ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (c & 1), ((c >> 1) - 1) & 1, s_abort, a.err,
