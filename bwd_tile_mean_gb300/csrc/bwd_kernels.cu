@@ -403,10 +403,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < kDkStages; ++s)
                 if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
-        if (warp == kMmaWarp && lane == 0 && mma_started) {
-            mma_commit(b_fin);
-            mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
-        }
+    }
+    if (warp == kMmaWarp && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+        // the MMAs this warp issued finish before TMEM is released
+        int never = 0;
+        mma_commit_w(b_fin);
+        __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
     __syncthreads();
@@ -436,28 +438,60 @@ constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = (2 + 
 constexpr int kDqOffCtl = kDqOffV + kDqVStages * kTile;
 constexpr size_t kDqSmem = kDqOffCtl + 256;
 
-// Walks the 128-key chunks of a query tile's selected KV tiles.
-struct ChunkIter {
+// The 128-key chunks of a query tile's selected KV tiles, walked by a whole
+// warp: a window of up to 32 selected tiles sits one tile per lane (tile
+// id, valid key count, chunk count and first chunk within the window), so
+// the index is read once per 32 tiles rather than once per chunk, and a
+// chunk's tile is found with a ballot. All lanes call with the same c.
+struct ChunkWin {
     const int *idx;
-    int cnt, per, n, sub, j, kvv;
+    int cnt, per;
+    int n0, c0, chunks;  // first tile and first chunk of the window; chunks in it
+    int j, kvv, nch, first;  // this lane's tile
 };
-__device__ __forceinline__ bool chunk_next(const Prob &p, int b, ChunkIter &it, int &row, int &valid) {
-    while (it.n < it.cnt) {
-        if (it.sub == 0) {
-            it.j = it.idx[it.n];
-            it.kvv = kv_valid(p, b, it.j);
-        }
-        const int v = it.kvv - it.sub * 128;
-        if (it.sub < it.per && v > 0) {
-            row = it.j * p.tile_kv + it.sub * 128;
-            valid = v < 128 ? v : 128;
-            ++it.sub;
-            return true;
-        }
-        ++it.n;
-        it.sub = 0;
+__device__ __forceinline__ void win_load(const Prob &p, int b, ChunkWin &w, int lane) {
+    const int n = w.n0 + lane;
+    w.j = n < w.cnt ? w.idx[n] : 0;
+    w.kvv = n < w.cnt ? kv_valid(p, b, w.j) : 0;
+    w.nch = min(w.per, (w.kvv + 127) >> 7);
+    int inc = w.nch;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
     }
-    return false;
+    w.first = inc - w.nch;
+    w.chunks = __shfl_sync(0xffffffffu, inc, 31);
+}
+__device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *idx, int cnt, int lane) {
+    ChunkWin w;
+    w.idx = idx;
+    w.cnt = cnt;
+    w.per = p.tile_kv >> 7;
+    w.n0 = 0;
+    w.c0 = 0;
+    win_load(p, b, w, lane);
+    return w;
+}
+// Row (of the KV tile's first key, within the batch entry) and valid key
+// count of chunk c; chunks are visited in increasing order.
+__device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int c, int lane, int &row, int &valid) {
+    while (c >= w.c0 + w.chunks) {
+        if (w.n0 + 32 >= w.cnt) return false;
+        w.c0 += w.chunks;
+        w.n0 += 32;
+        win_load(p, b, w, lane);
+    }
+    const int cw = c - w.c0;
+    const unsigned m = __ballot_sync(0xffffffffu, w.nch > 0 && w.first <= cw);
+    const int L = 31 - __clz(m);
+    const int first = __shfl_sync(0xffffffffu, w.first, L);
+    const int kvv = __shfl_sync(0xffffffffu, w.kvv, L);
+    const int j = __shfl_sync(0xffffffffu, w.j, L);
+    const int sub = cw - first;
+    row = j * p.tile_kv + sub * 128;
+    valid = min(128, kvv - sub * 128);
+    return true;
 }
 
 template <typename T>
@@ -534,31 +568,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int N = *s_nchunk;
     const bool bf16 = (p.dtype == T_BF16);
     int issued_q = 0, issued_k[kDqKStages] = {0, 0, 0}, issued_v[kDqVStages] = {0, 0}, mma_started = 0;
-    ChunkIter cit{a.q_idx + qrow * a.cap, a.q_cnt[qrow], p.tile_kv >> 7, 0, 0, 0, 0};
 
-    if (warp == kProdWarp && lane == 0 && N > 0) {
-        mbar_expect_tx(b_q, 2 * kTile);
-        tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
-        tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
-        tma_load_4d(sO, &tdo, b_q, 0, qrc, h, bc);
-        tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
+    if (warp == kProdWarp && N > 0) {
+        // ------------------------------------ TMA producer (whole warp, lane 0 issues)
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_cnt[qrow], lane);
+        if (lane == 0) {
+            mbar_expect_tx(b_q, 2 * kTile);
+            tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
+            tma_load_4d(sQ + kBox, &tq, b_q, 64, qrc, h, bc);
+            tma_load_4d(sO, &tdo, b_q, 0, qrc, h, bc);
+            tma_load_4d(sO + kBox, &tdo, b_q, 64, qrc, h, bc);
+        }
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
             int crow = 0, cval = 0;
-            if (!chunk_next(p, b, cit, crow, cval)) break;
+            if (!win_chunk(p, b, cw, c, lane, crow, cval)) break;
             const int sk = c % kDqKStages, sv = c % kDqVStages;
             const int kr = kvb + crow;
-            if (c >= kDqKStages && !mbar_wait(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
+            if (c >= kDqKStages &&
+                !mbar_wait_warp(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
                 break;
-            mbar_expect_tx(b_kf + sk, kTile);
-            tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
-            tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
+            if (lane == 0) {
+                mbar_expect_tx(b_kf + sk, kTile);
+                tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
+                tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
+            }
             issued_k[sk]++;
-            if (c >= kDqVStages && !mbar_wait(b_ve + sv, ((c / kDqVStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
+            if (c >= kDqVStages &&
+                !mbar_wait_warp(b_ve + sv, ((c / kDqVStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
                 break;
-            mbar_expect_tx(b_vf + sv, kTile);
-            tma_load_4d(sV + sv * kTile, &tv, b_vf + sv, 0, kr, hk, bc);
-            tma_load_4d(sV + sv * kTile + kBox, &tv, b_vf + sv, 64, kr, hk, bc);
+            if (lane == 0) {
+                mbar_expect_tx(b_vf + sv, kTile);
+                tma_load_4d(sV + sv * kTile, &tv, b_vf + sv, 0, kr, hk, bc);
+                tma_load_4d(sV + sv * kTile + kBox, &tv, b_vf + sv, 64, kr, hk, bc);
+            }
             issued_v[sv]++;
         }
     } else if (warp == kMmaWarp && N > 0) {
@@ -608,10 +651,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float l2 = N > 0 ? a.lse2[slot] : INFINITY;
         const float dvv = N > 0 ? a.dvec[slot] : 0.f;
         bool ok = true;
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_cnt[qrow], lane);
         for (int c = 0; c < N; ++c) {
-            // the chunk's valid key count (index reads overlap the wait for S)
             int crow = 0, cval = 0;
-            chunk_next(p, b, cit, crow, cval);
+            win_chunk(p, b, cw, c, lane, crow, cval);
             const int valid = cval - ch * 64;
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;
@@ -700,10 +743,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < kDqVStages; ++s)
                 if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
-        if (warp == kMmaWarp && lane == 0 && mma_started) {
-            mma_commit(b_fin);
-            mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
-        }
+    }
+    if (warp == kMmaWarp && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+        // the MMAs this warp issued finish before TMEM is released
+        int never = 0;
+        mma_commit_w(b_fin);
+        __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
     __syncthreads();

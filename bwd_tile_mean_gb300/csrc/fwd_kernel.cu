@@ -402,10 +402,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
             }
         }
-        if (warp == kFwdMmaWarp && lane == 0 && mma_started) {
-            mma_commit(b_fin);
-            mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull);
-        }
+    }
+    if (warp == kFwdMmaWarp && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+        // the MMAs this warp issued finish before TMEM is released
+        int never = 0;
+        mma_commit_w(b_fin);
+        __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
     __syncthreads();

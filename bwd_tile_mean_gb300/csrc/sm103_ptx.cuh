@@ -167,16 +167,15 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 // Warp-wide forms of the two MMAs and the commit: the whole warp executes
-// them with the same operands (kept warp-uniform) and lane 0 alone issues,
-// by predicate rather than by branch. Issuing from a warp whose control flow
-// stays uniform keeps the MMA stream dense; lane 0 must also be the lane
-// that commits (mma_commit_w, or mma_commit from lane 0).
+// them with the same operands (kept warp-uniform) and one lane, chosen by
+// elect.sync over the full warp, issues. Issuing from a warp whose control
+// flow stays uniform keeps the MMA stream dense. The warp that issued the
+// MMAs must also commit them with mma_commit_w (same election).
 __device__ __forceinline__ void mma_f16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
-        "mov.u32 l, %%laneid;\n\t"
-        "setp.eq.u32 e, l, 0;\n\t"
+        "elect.sync l|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
@@ -186,8 +185,7 @@ __device__ __forceinline__ void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, u
                                              uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
-        "mov.u32 l, %%laneid;\n\t"
-        "setp.eq.u32 e, l, 0;\n\t"
+        "elect.sync l|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
@@ -196,8 +194,7 @@ __device__ __forceinline__ void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, u
 __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
-        "mov.u32 l, %%laneid;\n\t"
-        "setp.eq.u32 e, l, 0;\n\t"
+        "elect.sync l|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
         : "memory");
 }
