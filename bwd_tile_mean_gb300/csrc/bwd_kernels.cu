@@ -31,6 +31,7 @@ enum : unsigned { kSiteDkProd = 0x201, kSiteDkMma = 0x202, kSiteDkSoft = 0x203,
 // groups (warp w owns TMEM lanes 32*(w%4)..+31); warp 8 issues TMA copies;
 // warp 9 owns TMEM and issues the MMAs.
 constexpr int kBwdThreads = 320;
+constexpr int kDqThreads = 352, kDqMmaWarp = 10;  // dQ: a second MMA-issuing warp
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 
 // ------------------------------------------------------------------ prep
@@ -426,11 +427,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // The eight softmax warps (lane quarter x key-column half) read S and dP
 // into registers and release them at once, so S/dP of the next chunk run
 // on the tensor core while this chunk's dS is computed; dQ += dS K reads
-// dS from TMEM. MMA order: S/dP(c), dQ(c-1), S/dP(c+1), dQ(c), ...
-// K chunks stay until dQ += dS K has read them, one chunk after S, so K
-// has three stages; V, free right after dP, has two. The chunk sequence
-// (selected tiles in ascending order, each cut into 128-key chunks with
-// valid keys) is walked from the index by each role, not stored.
+// dS from TMEM. Two warps issue MMAs: one S/dP(c) for every chunk, the
+// other dQ(c) once dS(c) is written, so the synchronisation of one warp
+// overlaps the other's MMAs. K chunks stay until dQ += dS K has read them,
+// one chunk after S, so K has three stages; V, free right after dP, has
+// two. The chunk sequence (selected tiles in ascending order, each cut into
+// 128-key chunks with valid keys) is walked from a per-warp window of the
+// index, not stored.
 // TMEM columns: S [0,128), dP [128,256), dQ [256,384), dS buffers
 // [384,448) and [448,512).
 constexpr int kDqKStages = 3, kDqVStages = 2;
@@ -495,7 +498,7 @@ __device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     k_dq(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
          const BwdArgs a) {
@@ -508,8 +511,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 9;
-    uint64_t *b_sf = bars + 11, *b_sfree = bars + 12, *b_dsf = bars + 13, *b_dq = bars + 14, *b_fin = bars + 16;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 17);
+    uint64_t *b_sf = bars + 11, *b_sfree = bars + 12, *b_dsf = bars + 13, *b_dq = bars + 15, *b_fin = bars + 17;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 19);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -542,8 +545,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int s = 0; s < 2; ++s) mbar_init(b_dq + s, 1);
         mbar_init(b_sf, 1);
         mbar_init(b_sfree, 256);
-        mbar_init(b_dsf, 256);
-        mbar_init(b_fin, 1);
+        for (int s = 0; s < 2; ++s) mbar_init(b_dsf + s, 256);
+        for (int s = 0; s < 2; ++s) mbar_init(b_fin + s, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -605,11 +608,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issued_v[sv]++;
         }
     } else if (warp == kMmaWarp && N > 0) {
-        // ------------------------------------- MMA issuer (whole warp, lane 0 issues)
+        // ------------------------------------------- S / dP issuer (whole warp)
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
-        const uint32_t idQ = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV);
-        const uint32_t tS = tbase, tP = tbase + 128, tQ = tbase + 256, tX = tbase + 384;
+        const uint32_t tS = tbase, tP = tbase + 128;
         bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
             const int sk = c % kDqKStages;
@@ -618,28 +620,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!(ok = mbar_wait_warp(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
             if (c > 0 && !(ok = mbar_wait_warp(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tS, aQ, aK + sk * kTile, idS);          // S = Q K^T
-            issue_ss(tP, aO, aV + sv * kTile, idS);          // dP = dO V^T
+            issue_ss(tS, aQ, aK + sk * kTile, idS);  // S = Q K^T
+            issue_ss(tP, aO, aV + sv * kTile, idS);  // dP = dO V^T
             mma_commit_w(b_sf);
             mma_commit_w(b_ve + sv);
             mma_started = 1;
-            if (c > 0) {
-                const int cp = c - 1, skp = cp % kDqKStages;
-                if (!(ok = mbar_wait_warp(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma))) break;
-                tc_fence_after();
-                issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);  // dQ += dS K
-                mma_commit_w(b_dq + (cp & 1));
-                mma_commit_w(b_ke + skp);
-            }
         }
-        if (ok) {
-            const int cp = N - 1, skp = cp % kDqKStages;
-            if (mbar_wait_warp(b_dsf, cp & 1, s_abort, a.err, kSiteDqMma)) {
-                tc_fence_after();
-                issue_ts(tQ, tX + (cp & 1) * 64, aK + skp * kTile, idQ, cp > 0);
-                mma_commit_w(b_dq + (cp & 1));
-                mma_commit_w(b_ke + skp);
-            }
+    } else if (warp == kDqMmaWarp && N > 0) {
+        // --------------------------------------------- dQ issuer (whole warp)
+        // Its MMAs touch no TMEM columns or stages the S / dP issuer writes,
+        // so the two warps issue independently; the waits of one overlap
+        // the other's MMAs.
+        const uint32_t idQ = idesc_f16(bf16, 128, 128, false, true);
+        const uint32_t aK = smem_addr(sK);
+        const uint32_t tQ = tbase + 256, tX = tbase + 384;
+        bool ok = true;
+        for (int c = 0; ok && c < N; ++c) {
+            const int sk = c % kDqKStages;
+            if (!(ok = mbar_wait_warp(b_dsf + (c & 1), (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            tc_fence_after();
+            issue_ts(tQ, tX + (c & 1) * 64, aK + sk * kTile, idQ, c > 0);  // dQ += dS K
+            mma_commit_w(b_dq + (c & 1));
+            mma_commit_w(b_ke + sk);
+            mma_started = 1;
         }
     } else if (warp < 8) {
         const int lg = warp & 3, ch = warp >> 2;  // lane quarter, key-column half
@@ -693,7 +696,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st32(tl + 384 + (c & 1) * 64 + ch * 32, dw);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_dsf);
+            mbar_arrive(b_dsf + (c & 1));
         }
         if (ok && N > 0) {
             const int cp = N - 1;
@@ -744,11 +747,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
     }
-    if (warp == kMmaWarp && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+    if ((warp == kMmaWarp || warp == kDqMmaWarp) && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
         // the MMAs this warp issued finish before TMEM is released
         int never = 0;
-        mma_commit_w(b_fin);
-        __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
+        mma_commit_w(b_fin + (warp - kMmaWarp));
+        __all_sync(0xffffffffu, mbar_wait(b_fin + (warp - kMmaWarp), 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
     __syncthreads();
@@ -918,9 +921,9 @@ cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     }
     prof_begin("bwd_dq", s);
     if (p.dtype == T_BF16)
-        k_dq<__nv_bfloat16><<<grid, kBwdThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__nv_bfloat16><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
     else
-        k_dq<__half><<<grid, kBwdThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__half><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
     prof_end(s);
     return cudaGetLastError();
 }
