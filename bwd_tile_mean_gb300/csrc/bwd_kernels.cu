@@ -36,15 +36,16 @@ constexpr int kProdWarp = 8, kMmaWarp = 9;
 
 // ------------------------------------------------------------------ prep
 // Per query slot w of the padded tile layout [B, Hq, nQ * tile_q]:
-// lse2[w] = LSE * log2(e) and dvec[w] = sum_d dO_d O_d (rowsum(P dP) of the
-// softmax backward). Slots that are not query rows (past a varlen
-// sequence's end) get lse2 = +inf and dvec = 0, so P = 0 there. A half-warp
+// nlse2[w] = -LSE * log2(e) and ndvec[w] = -sum_d dO_d O_d (minus
+// rowsum(P dP) of the softmax backward); both are stored negated so the
+// consumers add them. Slots that are not query rows (past a varlen
+// sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there. A half-warp
 // reads one 256-byte row (16 bytes per lane); each warp keeps four row
 // pairs in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
-                                                  const float *__restrict__ lse, float *__restrict__ lse2,
-                                                  float *__restrict__ dvec) {
+                                                  const float *__restrict__ lse, float *__restrict__ nlse2,
+                                                  float *__restrict__ ndvec) {
     const int per = p.nQ * p.tile_q;
     const long long slots = (long long)p.B * p.Hq * per;
     const int half = (threadIdx.x >> 4) & 1, hl = threadIdx.x & 15;
@@ -85,8 +86,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ 
         for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         const long long w = wbase + it * 2 + half;
         if (hl == 0 && w < slots) {
-            dvec[w] = ex[it] ? acc : 0.f;
-            lse2[w] = ex[it] ? lse[lo[it]] * kLog2e : INFINITY;
+            ndvec[w] = ex[it] ? -acc : 0.f;
+            nlse2[w] = ex[it] ? -lse[lo[it]] * kLog2e : -INFINITY;
         }
     }
 }
@@ -143,7 +144,7 @@ __device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint
 // dK [384,512).
 constexpr int kDkStages = 2;
 constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
-constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: lse2[128], dvec[128]
+constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: nlse2[128], ndvec[128]
 constexpr int kDkOffCtl = kDkOffLd + kDkStages * 1024;
 constexpr size_t kDkSmem = kDkOffCtl + 256;
 
@@ -270,8 +271,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_4d(sQ + st * kTile + kBox, &tq, b_qf + st, 64, row, w.h, bc);
             tma_load_4d(sO + st * kTile, &tdo, b_qf + st, 0, row, w.h, bc);
             tma_load_4d(sO + st * kTile + kBox, &tdo, b_qf + st, 64, row, w.h, bc);
-            bulk_load(sLd + st * 1024, a.lse2 + slot, 512, b_qf + st);
-            bulk_load(sLd + st * 1024 + 512, a.dvec + slot, 512, b_qf + st);
+            bulk_load(sLd + st * 1024, a.nlse2 + slot, 512, b_qf + st);
+            bulk_load(sLd + st * 1024 + 512, a.ndvec + slot, 512, b_qf + st);
             issued[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
@@ -324,30 +325,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            const float4 *sl4 = reinterpret_cast<const float4 *>(sLd + st * 1024) + ch * 16;
-            const float4 *sd4 = reinterpret_cast<const float4 *>(sLd + st * 1024 + 512) + ch * 16;
+            // this warp's 64 query columns of S^T and dP^T, one wait
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
+            tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+            tmem_wait_ld();
+            if (!key_ok) {  // keys past the chunk's valid count: P^T = 0
+#pragma unroll
+                for (int e = 0; e < 64; ++e) sr[e] = __float_as_uint(-INFINITY);
+            }
+            // P^T = 2^(scale log2e S^T + nlse2_t), dS^T = P^T (dP^T + ndvec_t), on pairs
+            const ulonglong2 *nl = reinterpret_cast<const ulonglong2 *>(sLd + st * 1024) + ch * 16;
+            const ulonglong2 *nd = reinterpret_cast<const ulonglong2 *>(sLd + st * 1024 + 512) + ch * 16;
+            const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tl + ch * 64 + q2 * 32, sr);
-                tmem_ld32(tl + 128 + ch * 64 + q2 * 32, dr);
-                tmem_wait_ld();
                 uint32_t pw[16], dw[16];
 #pragma unroll
                 for (int t4 = 0; t4 < 8; ++t4) {
-                    const float4 l4 = sl4[q2 * 8 + t4], d4 = sd4[q2 * 8 + t4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pp[4], dd[4];
+                    const ulonglong2 l4 = nl[q2 * 8 + t4], d4 = nd[q2 * 8 + t4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pr = key_ok ? ex2(fmaf(__uint_as_float(sr[t4 * 4 + e]), sl2, -lv[e])) : 0.f;
-                        pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(dr[t4 * 4 + e]) - dvv[e]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int e = q2 * 32 + t4 * 4 + hh * 2;
+                        const float2 x = f32x2_split(ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                             sc2, hh ? l4.y : l4.x));
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        const float2 dd = f32x2_split(fmul_x2(
+                            f32x2(p0, p1),
+                            fadd_x2(f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), hh ? d4.y : d4.x)));
+                        pw[t4 * 2 + hh] = pack2<T>(p0, p1);
+                        dw[t4 * 2 + hh] = pack2<T>(dd.x, dd.y);
                     }
-                    pw[t4 * 2] = pack2<T>(pp[0], pp[1]);
-                    pw[t4 * 2 + 1] = pack2<T>(pp[2], pp[3]);
-                    dw[t4 * 2] = pack2<T>(dd[0], dd[1]);
-                    dw[t4 * 2 + 1] = pack2<T>(dd[2], dd[3]);
                 }
                 // into this warp's own, already read columns
                 tmem_st16(tl + ch * 64 + q2 * 16, pw);
@@ -651,8 +661,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const float sl2 = p.scale * kLog2e;
         const bool row_ok = r < nrows;
         const long long slot = ((long long)b * p.Hq + h) * p.nQ * p.tile_q + row0 + r;
-        const float l2 = N > 0 ? a.lse2[slot] : INFINITY;
-        const float dvv = N > 0 ? a.dvec[slot] : 0.f;
+        const float nl2 = N > 0 ? a.nlse2[slot] : -INFINITY;
+        const float ndv = N > 0 ? a.ndvec[slot] : 0.f;
         bool ok = true;
         ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_cnt[qrow], lane);
         for (int c = 0; c < N; ++c) {
@@ -676,12 +686,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     if (kk >= valid) sr[kk] = __float_as_uint(-INFINITY);
             }
             // P = 2^(S scale log2e - LSE log2e), dS = P (dP - Dvec), on pairs
-            const uint64_t sc2 = f32x2(sl2, sl2), nl2 = f32x2(-l2, -l2), nd2 = f32x2(-dvv, -dvv);
+            const uint64_t sc2 = f32x2(sl2, sl2), nl2x = f32x2(nl2, nl2), nd2 = f32x2(ndv, ndv);
             uint32_t dw[32];
 #pragma unroll
             for (int t2 = 0; t2 < 32; ++t2) {
                 const float2 x = f32x2_split(
-                    ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2));
+                    ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2x));
                 const uint64_t pp = f32x2(ex2(x.x), ex2(x.y));
                 const uint64_t dd = fmul_x2(pp, fadd_x2(f32x2(__uint_as_float(dr[2 * t2]), __uint_as_float(dr[2 * t2 + 1])), nd2));
                 const float2 d2 = f32x2_split(dd);
@@ -871,17 +881,17 @@ __global__ void __launch_bounds__(128) k_compress_cols(Prob p, const float *__re
 
 }  // namespace
 
-cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *lse2,
-                            float *dvec, cudaStream_t s) {
+cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *nlse2,
+                            float *ndvec, cudaStream_t s) {
     const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;
     if (slots == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((slots + 63) / 64);
     prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
         k_bwd_prep<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)o,
-                                                        lse, lse2, dvec);
+                                                        lse, nlse2, ndvec);
     else
-        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, lse2, dvec);
+        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, nlse2, ndvec);
     prof_end(s);
     return cudaGetLastError();
 }

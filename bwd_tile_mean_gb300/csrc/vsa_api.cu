@@ -144,7 +144,7 @@ vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var,
 }
 
 struct WsLayout {
-    size_t pq, pk, pv, c, lse2, dvec, dc, A, ds, dpq, dpk, dpv, total;
+    size_t pq, pk, pv, c, nlse2, ndvec, dc, A, ds, dpq, dpk, dpv, total;
 };
 
 WsLayout ws_layout(const Prob &p, bool gate) {
@@ -159,8 +159,8 @@ WsLayout ws_layout(const Prob &p, bool gate) {
     const size_t slots = (size_t)p.B * p.Hq * p.nQ * p.tile_q;  // padded tile layout
     L.pq = take(fq);
     L.pk = take(fk);
-    L.lse2 = take(slots * 4);
-    L.dvec = take(slots * 4);
+    L.nlse2 = take(slots * 4);
+    L.ndvec = take(slots * 4);
     if (gate) {
         L.pv = take(fk);
         L.c = take(fq);
@@ -328,10 +328,10 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
     a.dk = dk;
     a.dv = dv;
     a.err = at<unsigned>(workspace, 0);
-    float *dvec = at<float>(workspace, L.dvec), *lse2 = at<float>(workspace, L.lse2);
-    a.dvec = dvec;
-    a.lse2 = lse2;
-    VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, lse2, dvec, s));
+    float *ndvec = at<float>(workspace, L.ndvec), *nlse2 = at<float>(workspace, L.nlse2);
+    a.ndvec = ndvec;
+    a.nlse2 = nlse2;
+    VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, nlse2, ndvec, s));
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
         VSA_CUDA(launch_pool(p, true, q, pq, s));

@@ -50,13 +50,15 @@ cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk,
 
 // Backward pieces.
 // Backward preprocess: per query slot of the padded tile layout
-// [B, Hq, nQ * tile_q], lse2 = LSE * log2(e) and Dvec = dO . O (slots
-// past a varlen sequence's end get lse2 = +inf, Dvec = 0).
-cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *lse2,
-                            float *dvec, cudaStream_t s);
+// [B, Hq, nQ * tile_q], nlse2 = -LSE * log2(e) and ndvec = -Dvec with
+// Dvec = dO . O, both negated so that P = 2^(scale log2e S + nlse2) and
+// dP - Dvec = dP + ndvec are single adds (slots past a varlen sequence's
+// end get nlse2 = -inf, ndvec = 0).
+cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *nlse2,
+                            float *ndvec, cudaStream_t s);
 struct BwdArgs {
     const void *dO, *q, *k, *v;
-    const float *lse2, *dvec;   // padded tile layout, see launch_bwd_prep
+    const float *nlse2, *ndvec;   // padded tile layout, see launch_bwd_prep
     const int *q_idx, *q_cnt;
     int cap;
     const int *kv_ptr, *kv_qidx;
