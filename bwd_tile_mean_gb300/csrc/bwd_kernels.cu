@@ -115,38 +115,54 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
         mma_f16_ts_w(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-// As issue_ts, with the packed A operand held in two 32-column pieces:
-// K steps 0-3 read columns [a_tmem, a_tmem+32), steps 4-7 read
-// [a_tmem+64, a_tmem+96).
-__device__ __forceinline__ void issue_ts_split(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_f16_ts_w(d, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc,
-                   (acc || kk > 0) ? 1u : 0u);
-}
-
 // ----------------------------------------------------------------- dK/dV
 // One CTA per (b, kv-head hk, 128-key chunk of KV tile j). K and V of the
-// chunk stay in shared memory. Work items are the 128-row chunks of every
+// chunk stay in shared memory. Work items are the 64-row pieces of every
 // query tile that selected j, over the query heads of hk's group, in
-// (head, ascending tile, chunk) order. Per item:
-//   S^T = K Q^T, dP^T = V dO^T            (TMEM, thread = key row)
+// (head, ascending tile, piece) order. Per item m:
+//   S^T = K Q_m^T, dP^T = V dO_m^T        (128 keys x 64 rows, TMEM buffer m%2)
 //   P^T = exp(scale S^T - LSE_t), dS^T = P^T (dP^T - Dvec_t)
 //                                         (packed 16-bit, written back over
 //                                          the consumed S^T / dP^T columns)
-//   dV += P^T dO, dK += dS^T Q            (A operands read from TMEM)
-// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and query columns
-// 64*(w/4)..+63, and writes its packed results into the first 32 of its
-// own 64 columns, 32-column slice by slice, so no warp overwrites columns
-// another warp still reads.
-// TMEM columns: S^T [0,128) (P^T packed in [0,32) and [64,96)), dP^T
-// [128,256) (dS^T packed in [128,160) and [192,224)), dV [256,384),
-// dK [384,512).
-constexpr int kDkStages = 2;
-constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = 2 * kTile + kDkStages * kTile;
-constexpr int kDkOffLd = 2 * kTile + 2 * kDkStages * kTile;  // per stage: nlse2[128], ndvec[128]
-constexpr int kDkOffCtl = kDkOffLd + kDkStages * 1024;
+//   dV += P^T dO_m, dK += dS^T Q_m         (A operands read from TMEM)
+// Two TMEM buffers let S^T / dP^T of item m+1 run on the tensor core while
+// the softmax warps work on item m; the MMA order is S/dP(0), S/dP(1),
+// dV/dK(0), S/dP(2), dV/dK(1), S/dP(3), ... (S/dP(m+2) reuses the buffer
+// that dV/dK(m), issued just before it, reads).
+// Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and the item's
+// query columns 32*(w/4)..+31, and writes its packed results into the first
+// 16 of those 32 columns, so no warp overwrites columns another still reads.
+// TMEM columns: buffer x: S^T [128x, 128x+64) (P^T packed in [128x, +16)
+// and [128x+32, +16)), dP^T [128x+64, 128x+128) (dS^T likewise);
+// dV [256,384), dK [384,512).
+constexpr int kDkStages = 4;
+constexpr int kDkItem = 64;                // query rows per item
+constexpr int kDkQTile = kDkItem * 256;    // one [64 x 128] 16-bit tile: two 8 KB boxes
+constexpr int kDkQBox = kDkItem * 128;
+constexpr int kDkOffK = 0, kDkOffV = kTile, kDkOffQ = 2 * kTile, kDkOffO = kDkOffQ + kDkStages * kDkQTile;
+constexpr int kDkOffLd = kDkOffO + kDkStages * kDkQTile;  // per stage: nlse2[64], ndvec[64]
+constexpr int kDkOffCtl = kDkOffLd + kDkStages * 512;
 constexpr size_t kDkSmem = kDkOffCtl + 256;
+
+// S^T = K Q_m^T (or dP^T = V dO_m^T): A = the 128-key tile, B = the 64-row
+// tile, both K-major 128-byte-swizzled; N = 64.
+__device__ __forceinline__ void issue_ss_n64(uint32_t d, uint32_t aA, uint32_t aB, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t o = (kk & 3) * 32;
+        mma_f16_ss_w(d, sdesc_sw128(aA + (kk >> 2) * kBox + o, 16, 1024),
+                     sdesc_sw128(aB + (kk >> 2) * kDkQBox + o, 16, 1024), idesc, kk > 0);
+    }
+}
+// dV += P^T dO_m (or dK += dS^T Q_m): A in TMEM, K = 64 query rows packed in
+// two 16-column pieces 32 columns apart (8 columns per K = 16 step); B = the
+// 64-row tile read MN-major (D halves 8 KB apart, 8-row groups 1 KB apart).
+__device__ __forceinline__ void issue_ts_k64(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_f16_ts_w(d, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_sw128(aB + kk * 2048, kDkQBox, 1024), idesc,
+                     (acc || kk > 0) ? 1u : 0u);
+}
 
 struct WorkIter {
     int h, pos, end, sub, i, nsub;
@@ -161,7 +177,7 @@ __device__ __forceinline__ bool work_next_list(const Prob &p, const BwdArgs &a, 
         w.end = ptr[j + 1];
     }
     w.i = a.kv_qidx[((long long)b * p.Hq + w.h) * p.nQ * a.cap + w.pos];
-    w.nsub = (q_rows(p, b, w.i) + 127) >> 7;
+    w.nsub = (q_rows(p, b, w.i) + kDkItem - 1) / kDkItem;
     w.sub = 0;
     return true;
 }
@@ -193,9 +209,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
-    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 3, *b_sf = bars + 5, *b_pd = bars + 6;
-    uint64_t *b_acc = bars + 7, *b_fin = bars + 8;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 9);
+    uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 1 + kDkStages, *b_sf = bars + 1 + 2 * kDkStages;
+    uint64_t *b_pd = b_sf + 2, *b_acc = b_pd + 2, *b_fin = b_acc + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(b_fin + 1);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -218,8 +234,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(b_qf + s, 1);
             mbar_init(b_qe + s, 1);
         }
-        mbar_init(b_sf, 1);
-        mbar_init(b_pd, 256);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_sf + x, 1);
+            mbar_init(b_pd + x, 256);
+        }
         mbar_init(b_acc, 1);
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -229,11 +247,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int h = h0; h < h_end; ++h) {
                 const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
                 if (p.layout != L_TND) {  // every query tile has tile_q rows
-                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q >> 7);
+                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q / kDkItem);
                     continue;
                 }
                 const int *lst = a.kv_qidx + ((long long)b * p.Hq + h) * p.nQ * a.cap;
-                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + 127) >> 7;
+                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + kDkItem - 1) / kDkItem;
             }
         *s_nwork = n;
         fence_mbar_init();
@@ -248,7 +266,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tbase = *s_tmem;
     const int M = *s_nwork;
     const bool bf16 = (p.dtype == T_BF16);
-    int issued_kv = 0, issued[kDkStages] = {0, 0}, mma_started = 0;
+    int issued_kv = 0, issued[kDkStages] = {0, 0, 0, 0}, mma_started = 0;
 
     if (warp == kProdWarp && lane == 0 && M > 0) {
         // ------------------------------------------------------ producer
@@ -264,53 +282,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int st = m % kDkStages;
             if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
                 break;
-            const int row = qb + w.i * p.tile_q + w.sub * 128;
-            const long long slot = ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * 128;
-            mbar_expect_tx(b_qf + st, 2 * kTile + 1024);
-            tma_load_4d(sQ + st * kTile, &tq, b_qf + st, 0, row, w.h, bc);
-            tma_load_4d(sQ + st * kTile + kBox, &tq, b_qf + st, 64, row, w.h, bc);
-            tma_load_4d(sO + st * kTile, &tdo, b_qf + st, 0, row, w.h, bc);
-            tma_load_4d(sO + st * kTile + kBox, &tdo, b_qf + st, 64, row, w.h, bc);
-            bulk_load(sLd + st * 1024, a.nlse2 + slot, 512, b_qf + st);
-            bulk_load(sLd + st * 1024 + 512, a.ndvec + slot, 512, b_qf + st);
+            const int row = qb + w.i * p.tile_q + w.sub * kDkItem;
+            const long long slot =
+                ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * kDkItem;
+            mbar_expect_tx(b_qf + st, 2 * kDkQTile + 512);
+            tma_load_4d(sQ + st * kDkQTile, &tq, b_qf + st, 0, row, w.h, bc);
+            tma_load_4d(sQ + st * kDkQTile + kDkQBox, &tq, b_qf + st, 64, row, w.h, bc);
+            tma_load_4d(sO + st * kDkQTile, &tdo, b_qf + st, 0, row, w.h, bc);
+            tma_load_4d(sO + st * kDkQTile + kDkQBox, &tdo, b_qf + st, 64, row, w.h, bc);
+            bulk_load(sLd + st * 512, a.nlse2 + slot, 256, b_qf + st);
+            bulk_load(sLd + st * 512 + 256, a.ndvec + slot, 256, b_qf + st);
             issued[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
     } else if (warp == kMmaWarp && M > 0) {
-        // ------------------------------------- MMA issuer (whole warp, lane 0 issues)
-        const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
+        // ------------------------------------- MMA issuer (whole warp, one lane issues)
+        const uint32_t idS = idesc_f16(bf16, 128, 64, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
-        const uint32_t tS = tbase, tP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
+        const uint32_t tdV = tbase + 256, tdK = tbase + 384;
         bool ok = mbar_wait_warp(b_kv, 0, s_abort, a.err, kSiteDkMma);
-        for (int m = 0; ok && m < M; ++m) {
-            const int st = m % kDkStages;
-            if (!(ok = mbar_wait_warp(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
-            if (m > 0) {
-                // finish item m-1 first: its P^T / dS^T live in the columns S/dP(m) overwrite
-                const int mp = m - 1, sp = mp % kDkStages;
-                if (!(ok = mbar_wait_warp(b_pd, mp & 1, s_abort, a.err, kSiteDkMma))) break;
-                tc_fence_after();
-                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);  // dV += P^T dO
-                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);  // dK += dS^T Q
-                mma_commit_w(b_qe + sp);
-            }
+        // S^T / dP^T of items 0 and 1
+        for (int m = 0; ok && m < 2 && m < M; ++m) {
+            if (!(ok = mbar_wait_warp(b_qf + m, 0, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
-            issue_ss(tS, aK, aQ + st * kTile, idS);  // S^T = K Q^T
-            issue_ss(tP, aV, aO + st * kTile, idS);  // dP^T = V dO^T
-            mma_commit_w(b_sf);
+            issue_ss_n64(tbase + m * 128, aK, aQ + m * kDkQTile, idS);       // S^T = K Q^T
+            issue_ss_n64(tbase + m * 128 + 64, aV, aO + m * kDkQTile, idS);  // dP^T = V dO^T
+            mma_commit_w(b_sf + m);
             mma_started = 1;
         }
-        if (ok) {
-            const int mp = M - 1, sp = mp % kDkStages;
-            if (mbar_wait_warp(b_pd, mp & 1, s_abort, a.err, kSiteDkMma)) {
+        for (int m = 0; ok && m < M; ++m) {
+            const int x = m & 1, st = m % kDkStages;
+            const uint32_t tx = tbase + x * 128;
+            if (!(ok = mbar_wait_warp(b_pd + x, (m >> 1) & 1, s_abort, a.err, kSiteDkMma))) break;
+            tc_fence_after();
+            issue_ts_k64(tdV, tx, aO + st * kDkQTile, idA, m > 0);       // dV += P^T dO
+            issue_ts_k64(tdK, tx + 64, aQ + st * kDkQTile, idA, m > 0);  // dK += dS^T Q
+            mma_commit_w(b_qe + st);
+            const int n = m + 2;
+            if (n < M) {
+                const int sn = n % kDkStages;
+                if (!(ok = mbar_wait_warp(b_qf + sn, (n / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ts_split(tdV, tS, aO + sp * kTile, idA, mp > 0);
-                issue_ts_split(tdK, tP, aQ + sp * kTile, idA, mp > 0);
-                mma_commit_w(b_qe + sp);
-                mma_commit_w(b_acc);
+                issue_ss_n64(tx, aK, aQ + sn * kDkQTile, idS);
+                issue_ss_n64(tx + 64, aV, aO + sn * kDkQTile, idS);
+                mma_commit_w(b_sf + x);
             }
         }
+        if (ok) mma_commit_w(b_acc);
     } else if (warp < 8) {
         // ------------------------------------------- softmax + epilogue
         const int lg = warp & 3, ch = warp >> 2;  // lane quarter, query-column half
@@ -320,52 +339,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool key_ok = u < kvalid;
         bool ok = true;
         for (int m = 0; m < M; ++m) {
-            const int st = m % kDkStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, m & 1, s_abort, a.err, kSiteDkSoft) &&
-                                             mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
+            const int x = m & 1, st = m % kDkStages;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(b_sf + x, (m >> 1) & 1, s_abort, a.err, kSiteDkSoft) &&
+                                mbar_wait(b_qf + st, (m / kDkStages) & 1, s_abort, a.err, kSiteDkSoft));
             if (!ok) break;
             tc_fence_after();
-            // this warp's 64 query columns of S^T and dP^T, one wait
-            uint32_t sr[64], dr[64];
-            tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-            tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-            tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
-            tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+            // this warp's 32 query columns of S^T and dP^T
+            const uint32_t cs = x * 128 + ch * 32;
+            uint32_t sr[32], dr[32];
+            tmem_ld32(tl + cs, sr);
+            tmem_ld32(tl + cs + 64, dr);
             tmem_wait_ld();
             if (!key_ok) {  // keys past the chunk's valid count: P^T = 0
 #pragma unroll
-                for (int e = 0; e < 64; ++e) sr[e] = __float_as_uint(-INFINITY);
+                for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(-INFINITY);
             }
             // P^T = 2^(scale log2e S^T + nlse2_t), dS^T = P^T (dP^T + ndvec_t), on pairs
-            const ulonglong2 *nl = reinterpret_cast<const ulonglong2 *>(sLd + st * 1024) + ch * 16;
-            const ulonglong2 *nd = reinterpret_cast<const ulonglong2 *>(sLd + st * 1024 + 512) + ch * 16;
+            const ulonglong2 *nl = reinterpret_cast<const ulonglong2 *>(sLd + st * 512) + ch * 8;
+            const ulonglong2 *nd = reinterpret_cast<const ulonglong2 *>(sLd + st * 512 + 256) + ch * 8;
             const uint64_t sc2 = f32x2(sl2, sl2);
+            uint32_t pw[16], dw[16];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t pw[16], dw[16];
+            for (int t4 = 0; t4 < 8; ++t4) {
+                const ulonglong2 l4 = nl[t4], d4 = nd[t4];
 #pragma unroll
-                for (int t4 = 0; t4 < 8; ++t4) {
-                    const ulonglong2 l4 = nl[q2 * 8 + t4], d4 = nd[q2 * 8 + t4];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int e = q2 * 32 + t4 * 4 + hh * 2;
-                        const float2 x = f32x2_split(ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                                             sc2, hh ? l4.y : l4.x));
-                        const float p0 = ex2(x.x), p1 = ex2(x.y);
-                        const float2 dd = f32x2_split(fmul_x2(
-                            f32x2(p0, p1),
-                            fadd_x2(f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), hh ? d4.y : d4.x)));
-                        pw[t4 * 2 + hh] = pack2<T>(p0, p1);
-                        dw[t4 * 2 + hh] = pack2<T>(dd.x, dd.y);
-                    }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int e = t4 * 4 + hh * 2;
+                    const float2 xx = f32x2_split(
+                        ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, hh ? l4.y : l4.x));
+                    const float p0 = ex2(xx.x), p1 = ex2(xx.y);
+                    const float2 dd = f32x2_split(fmul_x2(
+                        f32x2(p0, p1), fadd_x2(f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                               hh ? d4.y : d4.x)));
+                    pw[t4 * 2 + hh] = pack2<T>(p0, p1);
+                    dw[t4 * 2 + hh] = pack2<T>(dd.x, dd.y);
                 }
-                // into this warp's own, already read columns
-                tmem_st16(tl + ch * 64 + q2 * 16, pw);
-                tmem_st16(tl + 128 + ch * 64 + q2 * 16, dw);
             }
+            // into this warp's own, already read columns
+            tmem_st16(tl + cs, pw);
+            tmem_st16(tl + cs + 64, dw);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_pd);
+            mbar_arrive(b_pd + x);
         }
         if (ok && M > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_acc, 0, s_abort, a.err, kSiteDkSoft));
@@ -898,8 +914,8 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
 
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tv, tdo;
-    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
-        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
+    if (!make_tmap_rows(&tq, p, true, a.q, p.Hq, kDkItem) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, kDkItem))
         return cudaErrorInvalidValue;
     dim3 grid(p.nKV * (p.tile_kv / 128), p.Hkv, p.B);
     static bool attr = false;
