@@ -537,8 +537,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 9;
-    uint64_t *b_sf = bars + 11, *b_sfree = bars + 12, *b_dsf = bars + 13, *b_dq = bars + 15, *b_fin = bars + 17;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 19);
+    // b_sf / b_sfree: [0] for S, [1] for dP (each computed, then read, on its own)
+    uint64_t *b_sf = bars + 11, *b_sfree = bars + 13, *b_dsf = bars + 15, *b_dq = bars + 17, *b_fin = bars + 19;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 21);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -569,8 +570,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             mbar_init(b_ve + s, 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(b_dq + s, 1);
-        mbar_init(b_sf, 1);
-        mbar_init(b_sfree, 256);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(b_sf + s, 1);
+            mbar_init(b_sfree + s, 256);
+        }
         for (int s = 0; s < 2; ++s) mbar_init(b_dsf + s, 256);
         for (int s = 0; s < 2; ++s) mbar_init(b_fin + s, 1);
         *s_abort = 0;
@@ -614,15 +617,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!win_chunk(p, b, cw, c, lane, crow, cval)) break;
             const int sk = c % kDqKStages, sv = c % kDqVStages;
             const int kr = kvb + crow;
-            if (c >= kDqKStages &&
-                !mbar_wait_warp(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
-                break;
-            if (lane == 0) {
-                mbar_expect_tx(b_kf + sk, kTile);
-                tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
-                tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
-            }
-            issued_k[sk]++;
+            // V first: its stage frees when dP(c-2) completes, which precedes
+            // dQ(c-3), the MMA that frees K's stage
             if (c >= kDqVStages &&
                 !mbar_wait_warp(b_ve + sv, ((c / kDqVStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
                 break;
@@ -632,6 +628,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 tma_load_4d(sV + sv * kTile + kBox, &tv, b_vf + sv, 64, kr, hk, bc);
             }
             issued_v[sv]++;
+            if (c >= kDqKStages &&
+                !mbar_wait_warp(b_ke + sk, ((c / kDqKStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
+                break;
+            if (lane == 0) {
+                mbar_expect_tx(b_kf + sk, kTile);
+                tma_load_4d(sK + sk * kTile, &tk, b_kf + sk, 0, kr, hk, bc);
+                tma_load_4d(sK + sk * kTile + kBox, &tk, b_kf + sk, 64, kr, hk, bc);
+            }
+            issued_k[sk]++;
         }
     } else if (warp == kMmaWarp && N > 0) {
         // ------------------------------------------- S / dP issuer (whole warp)
@@ -640,15 +645,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const uint32_t tS = tbase, tP = tbase + 128;
         bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
+            // S(c) needs only S(c-1) read out, dP(c) only dP(c-1): the read of
+            // one overlaps the other's MMAs
             const int sk = c % kDqKStages;
             if (!(ok = mbar_wait_warp(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
-            const int sv = c % kDqVStages;
-            if (!(ok = mbar_wait_warp(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
             if (c > 0 && !(ok = mbar_wait_warp(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
             issue_ss(tS, aQ, aK + sk * kTile, idS);  // S = Q K^T
-            issue_ss(tP, aO, aV + sv * kTile, idS);  // dP = dO V^T
             mma_commit_w(b_sf);
+            const int sv = c % kDqVStages;
+            if (!(ok = mbar_wait_warp(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (c > 0 && !(ok = mbar_wait_warp(b_sfree + 1, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            tc_fence_after();
+            issue_ss(tP, aO, aV + sv * kTile, idS);  // dP = dO V^T
+            mma_commit_w(b_sf + 1);
             mma_commit_w(b_ve + sv);
             mma_started = 1;
         }
@@ -685,17 +695,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             int crow = 0, cval = 0;
             win_chunk(p, b, cw, c, lane, crow, cval);
             const int valid = cval - ch * 64;
+            uint32_t sr[64], dr[64];
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[64], dr[64];
             tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
             tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(b_sfree);  // S of this chunk is in registers
+            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + 1, c & 1, s_abort, a.err, kSiteDqSoft));
+            if (!ok) break;
+            tc_fence_after();
             tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
             tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(b_sfree);  // S and dP of this chunk are in registers
+            mbar_arrive(b_sfree + 1);  // and dP
             if (valid < 64) {  // keys past the valid count: P = 0
 #pragma unroll
                 for (int kk = 0; kk < 64; ++kk)
