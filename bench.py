@@ -66,7 +66,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, bus_id=None):
-        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "50"]
         if bus_id:
             cmd.insert(1, f"--id={bus_id}")
         try:
