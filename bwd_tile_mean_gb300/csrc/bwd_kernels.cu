@@ -30,8 +30,8 @@ enum : unsigned { kSiteDkProd = 0x201, kSiteDkMma = 0x202, kSiteDkSoft = 0x203,
 // Warp roles of the backward kernels: warps 0-3 and 4-7 are two softmax
 // groups (warp w owns TMEM lanes 32*(w%4)..+31); warp 8 issues TMA copies;
 // warp 9 owns TMEM and issues the MMAs.
-constexpr int kBwdThreads = 320;
 constexpr int kDqThreads = 352, kDqMmaWarp = 10;  // dQ: a second MMA-issuing warp
+constexpr int kDkThreads = 352, kDkMma2Warp = 10;  // dK/dV: a second MMA-issuing warp
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 
 // ------------------------------------------------------------------ prep
@@ -126,9 +126,10 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t a
 //                                          the consumed S^T / dP^T columns)
 //   dV += P^T dO_m, dK += dS^T Q_m         (A operands read from TMEM)
 // Two TMEM buffers let S^T / dP^T of item m+1 run on the tensor core while
-// the softmax warps work on item m; the MMA order is S/dP(0), S/dP(1),
-// dV/dK(0), S/dP(2), dV/dK(1), S/dP(3), ... (S/dP(m+2) reuses the buffer
-// that dV/dK(m), issued just before it, reads).
+// the softmax warps work on item m; each MMA warp's order is S/dP(0),
+// S/dP(1), dV/dK(0), S/dP(2), dV/dK(1), S/dP(3), ... (S/dP(m+2) reuses the
+// buffer that dV/dK(m), issued just before it, reads). One warp issues
+// S^T and dV, another dP^T and dK.
 // Eight softmax warps: warp w owns TMEM lanes 32*(w%4).. and the item's
 // query columns 32*(w/4)..+31, and writes its packed results into the first
 // 16 of those 32 columns, so no warp overwrites columns another still reads.
@@ -197,7 +198,7 @@ __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, in
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkThreads, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
            const BwdArgs a) {
@@ -210,8 +211,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t *sK = sm + kDkOffK, *sV = sm + kDkOffV, *sQ = sm + kDkOffQ, *sO = sm + kDkOffO, *sLd = sm + kDkOffLd;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDkOffCtl);
     uint64_t *b_kv = bars + 0, *b_qf = bars + 1, *b_qe = bars + 1 + kDkStages, *b_sf = bars + 1 + 2 * kDkStages;
-    uint64_t *b_pd = b_sf + 2, *b_acc = b_pd + 2, *b_fin = b_acc + 1;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(b_fin + 1);
+    uint64_t *b_pd = b_sf + 2, *b_acc = b_pd + 2, *b_fin = b_acc + 1;  // b_fin: one per MMA warp
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(b_fin + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -232,14 +233,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(b_kv, 1);
         for (int s = 0; s < kDkStages; ++s) {
             mbar_init(b_qf + s, 1);
-            mbar_init(b_qe + s, 1);
+            mbar_init(b_qe + s, 2);  // both MMA warps
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(b_sf + x, 1);
+            mbar_init(b_sf + x, 2);  // both MMA warps
             mbar_init(b_pd + x, 256);
+            mbar_init(b_fin + x, 1);
         }
-        mbar_init(b_acc, 1);
-        mbar_init(b_fin, 1);
+        mbar_init(b_acc, 2);
         *s_abort = 0;
         // count the work items (a chunk with no valid key does no work)
         int n = 0;
@@ -295,37 +296,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issued[st]++;
             more = work_advance(p, a, b, h_end, j, w);
         }
-    } else if (warp == kMmaWarp && M > 0) {
-        // ------------------------------------- MMA issuer (whole warp, one lane issues)
+    } else if ((warp == kMmaWarp || warp == kDkMma2Warp) && M > 0) {
+        // -------------------------------- MMA issuers (two whole warps, one lane each)
+        // Warp 0 of the pair: S^T = K Q^T and dV += P^T dO; warp 1: dP^T =
+        // V dO^T and dK += dS^T Q. Each warp's accumulation reads only the
+        // columns its own score MMA wrote, and S/dP(m+2) overwrites what
+        // dV/dK(m) of the same warp reads, issued just before; so the two
+        // warps share no TMEM hazard and their waits overlap each other's MMAs.
+        const int mw = warp == kMmaWarp ? 0 : 1;
         const uint32_t idS = idesc_f16(bf16, 128, 64, false, false);
         const uint32_t idA = idesc_f16(bf16, 128, 128, false, true);
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aO = smem_addr(sO);
-        const uint32_t tdV = tbase + 256, tdK = tbase + 384;
+        const uint32_t aX = mw ? aV : aK;     // scores: A operand
+        const uint32_t aS = mw ? aO : aQ;     // scores: B operand (per stage)
+        const uint32_t aG = mw ? aQ : aO;     // accumulation: B operand (per stage)
+        const uint32_t tAcc = tbase + 256 + mw * 128, off = mw * 64;
         bool ok = mbar_wait_warp(b_kv, 0, s_abort, a.err, kSiteDkMma);
-        // S^T / dP^T of items 0 and 1
+        // scores of items 0 and 1
         for (int m = 0; ok && m < 2 && m < M; ++m) {
             if (!(ok = mbar_wait_warp(b_qf + m, 0, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
-            issue_ss_n64(tbase + m * 128, aK, aQ + m * kDkQTile, idS);       // S^T = K Q^T
-            issue_ss_n64(tbase + m * 128 + 64, aV, aO + m * kDkQTile, idS);  // dP^T = V dO^T
+            issue_ss_n64(tbase + m * 128 + off, aX, aS + m * kDkQTile, idS);
             mma_commit_w(b_sf + m);
             mma_started = 1;
         }
         for (int m = 0; ok && m < M; ++m) {
             const int x = m & 1, st = m % kDkStages;
-            const uint32_t tx = tbase + x * 128;
+            const uint32_t tx = tbase + x * 128 + off;
             if (!(ok = mbar_wait_warp(b_pd + x, (m >> 1) & 1, s_abort, a.err, kSiteDkMma))) break;
             tc_fence_after();
-            issue_ts_k64(tdV, tx, aO + st * kDkQTile, idA, m > 0);       // dV += P^T dO
-            issue_ts_k64(tdK, tx + 64, aQ + st * kDkQTile, idA, m > 0);  // dK += dS^T Q
+            issue_ts_k64(tAcc, tx, aG + st * kDkQTile, idA, m > 0);  // dV += P^T dO | dK += dS^T Q
             mma_commit_w(b_qe + st);
             const int n = m + 2;
             if (n < M) {
                 const int sn = n % kDkStages;
                 if (!(ok = mbar_wait_warp(b_qf + sn, (n / kDkStages) & 1, s_abort, a.err, kSiteDkMma))) break;
                 tc_fence_after();
-                issue_ss_n64(tx, aK, aQ + sn * kDkQTile, idS);
-                issue_ss_n64(tx + 64, aV, aO + sn * kDkQTile, idS);
+                issue_ss_n64(tx, aX, aS + sn * kDkQTile, idS);
                 mma_commit_w(b_sf + x);
             }
         }
@@ -431,11 +438,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (issued[s]) mbar_wait(b_qf + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
     }
-    if (warp == kMmaWarp && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+    if ((warp == kMmaWarp || warp == kDkMma2Warp) && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
         // the MMAs this warp issued finish before TMEM is released
         int never = 0;
-        mma_commit_w(b_fin);
-        __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
+        const int mw = warp == kMmaWarp ? 0 : 1;
+        mma_commit_w(b_fin + mw);
+        __all_sync(0xffffffffu, mbar_wait(b_fin + mw, 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
     __syncthreads();
@@ -942,9 +950,9 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     }
     prof_begin("bwd_dkdv", s);
     if (p.dtype == T_BF16)
-        k_dkdv<__nv_bfloat16><<<grid, kBwdThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__nv_bfloat16><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
     else
-        k_dkdv<__half><<<grid, kBwdThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__half><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
     prof_end(s);
     return cudaGetLastError();
 }
