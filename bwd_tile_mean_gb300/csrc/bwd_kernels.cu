@@ -30,7 +30,7 @@ enum : unsigned { kSiteDkProd = 0x201, kSiteDkMma = 0x202, kSiteDkSoft = 0x203,
 // Warp roles of the backward kernels: warps 0-3 and 4-7 are two softmax
 // groups (warp w owns TMEM lanes 32*(w%4)..+31); warp 8 issues TMA copies;
 // warp 9 owns TMEM and issues the MMAs.
-constexpr int kDqThreads = 352, kDqMmaWarp = 10;  // dQ: a second MMA-issuing warp
+constexpr int kDqThreads = 384, kDqMmaWarp = 10, kDqPMmaWarp = 11;  // dQ: three MMA-issuing warps
 constexpr int kDkThreads = 352, kDkMma2Warp = 10;  // dK/dV: a second MMA-issuing warp
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 
@@ -461,9 +461,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // The eight softmax warps (lane quarter x key-column half) read S and dP
 // into registers and release them at once, so S/dP of the next chunk run
 // on the tensor core while this chunk's dS is computed; dQ += dS K reads
-// dS from TMEM. Two warps issue MMAs: one S/dP(c) for every chunk, the
-// other dQ(c) once dS(c) is written, so the synchronisation of one warp
-// overlaps the other's MMAs. K chunks stay until dQ += dS K has read them,
+// dS from TMEM. Three warps issue MMAs: S(c), dP(c) and dQ(c) (once dS(c)
+// is written) each from their own, so the synchronisation of one warp
+// overlaps the others' MMAs. K chunks stay until dQ += dS K has read them,
 // one chunk after S, so K has three stages; V, free right after dP, has
 // two. The chunk sequence (selected tiles in ascending order, each cut into
 // 128-key chunks with valid keys) is walked from a per-warp window of the
@@ -546,8 +546,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 9;
     // b_sf / b_sfree: [0] for S, [1] for dP (each computed, then read, on its own)
-    uint64_t *b_sf = bars + 11, *b_sfree = bars + 13, *b_dsf = bars + 15, *b_dq = bars + 17, *b_fin = bars + 19;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 21);
+    uint64_t *b_sf = bars + 11, *b_sfree = bars + 13, *b_dsf = bars + 15, *b_dq = bars + 17;
+    uint64_t *b_fin = bars + 19;  // one per MMA warp
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 22);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
 
@@ -583,7 +584,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             mbar_init(b_sfree + s, 256);
         }
         for (int s = 0; s < 2; ++s) mbar_init(b_dsf + s, 256);
-        for (int s = 0; s < 2; ++s) mbar_init(b_fin + s, 1);
+        for (int s = 0; s < 3; ++s) mbar_init(b_fin + s, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -646,28 +647,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             issued_k[sk]++;
         }
-    } else if (warp == kMmaWarp && N > 0) {
-        // ------------------------------------------- S / dP issuer (whole warp)
+    } else if ((warp == kMmaWarp || warp == kDqPMmaWarp) && N > 0) {
+        // ------------------------- S issuer (warp 9) and dP issuer (warp 11)
+        // S(c) needs only S(c-1) read out, dP(c) only dP(c-1); with a warp
+        // each, the read of one overlaps the other's MMAs.
+        const bool isP = warp == kDqPMmaWarp;
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
-        const uint32_t aQ = smem_addr(sQ), aO = smem_addr(sO), aK = smem_addr(sK), aV = smem_addr(sV);
-        const uint32_t tS = tbase, tP = tbase + 128;
+        const uint32_t aA = smem_addr(isP ? sO : sQ), aB = smem_addr(isP ? sV : sK);
+        const uint32_t tD = tbase + (isP ? 128 : 0);
+        const int nst = isP ? kDqVStages : kDqKStages;
+        uint64_t *b_full = isP ? b_vf : b_kf;
         bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteDqMma);
         for (int c = 0; ok && c < N; ++c) {
-            // S(c) needs only S(c-1) read out, dP(c) only dP(c-1): the read of
-            // one overlaps the other's MMAs
-            const int sk = c % kDqKStages;
-            if (!(ok = mbar_wait_warp(b_kf + sk, (c / kDqKStages) & 1, s_abort, a.err, kSiteDqMma))) break;
-            if (c > 0 && !(ok = mbar_wait_warp(b_sfree, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
+            const int sx = c % nst;
+            if (!(ok = mbar_wait_warp(b_full + sx, (c / nst) & 1, s_abort, a.err, kSiteDqMma))) break;
+            if (c > 0 && !(ok = mbar_wait_warp(b_sfree + isP, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tS, aQ, aK + sk * kTile, idS);  // S = Q K^T
-            mma_commit_w(b_sf);
-            const int sv = c % kDqVStages;
-            if (!(ok = mbar_wait_warp(b_vf + sv, (c / kDqVStages) & 1, s_abort, a.err, kSiteDqMma))) break;
-            if (c > 0 && !(ok = mbar_wait_warp(b_sfree + 1, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
-            tc_fence_after();
-            issue_ss(tP, aO, aV + sv * kTile, idS);  // dP = dO V^T
-            mma_commit_w(b_sf + 1);
-            mma_commit_w(b_ve + sv);
+            issue_ss(tD, aA, aB + sx * kTile, idS);  // S = Q K^T | dP = dO V^T
+            mma_commit_w(b_sf + isP);
+            if (isP) mma_commit_w(b_ve + sx);
             mma_started = 1;
         }
     } else if (warp == kDqMmaWarp && N > 0) {
@@ -797,7 +795,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 if (issued_v[s]) mbar_wait(b_vf + s, (issued_v[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
         }
     }
-    if ((warp == kMmaWarp || warp == kDqMmaWarp) && mma_started && __any_sync(0xffffffffu, *s_abort != 0)) {
+    if ((warp == kMmaWarp || warp == kDqMmaWarp || warp == kDqPMmaWarp) && mma_started &&
+        __any_sync(0xffffffffu, *s_abort != 0)) {
         // the MMAs this warp issued finish before TMEM is released
         int never = 0;
         mma_commit_w(b_fin + (warp - kMmaWarp));
