@@ -28,6 +28,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fwd+bwd effective TFLOP/s (selected blocks) on 1 GB300; % of bf16 TC peak"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# attention kernel, from one `ncu --set full` capture of the current kernels
+# on this workload cut to 4 heads; every head is an independent problem, so
+# the traffic of a launch scales with the heads. Set an entry to None when its
+# kernel changes after the capture.
+DRAM_BYTES_PER_4_HEADS = {
+    "bwd_dkdv": 397.747456e6 + 142.336512e6,
+    "bwd_dq": 410.607616e6 + 73.073920e6,
+    "fwd_attn": 305.426176e6 + 66.525696e6,
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -283,8 +294,11 @@ def ours(args):
         if unit_flops is not None:
             launch_flops = 2.0 * p.D * p.tile_q * float(valid_keys.item()) * unit_flops / 2.0
             achieved = launch_flops / (info["avg_ms"] * 1e-3) / 1e12
+            dram = DRAM_BYTES_PER_4_HEADS.get(name)
+            traffic = dram * p.Hq / 4.0 if dram is not None else None
             roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
-                    "unit": "TFLOP/s", "frac": achieved / tensor_peak, "traffic": None,
+                    "unit": "TFLOP/s", "frac": achieved / tensor_peak, "traffic": traffic,
+                    "traffic_unit": "bytes per launch (ncu, 4-head capture scaled to the heads)",
                     "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
                     "flops_per_launch": launch_flops}
     cpu = None
