@@ -184,14 +184,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < N; ++c) {
             const int s = c & 1;
             // K(c-2) is free once the last group's S(c-2) is done, V(c-2) once
-            // its O += P V(c-2) is (each group's MMAs complete in issue order)
+            // that group's S(c-1) is: the MMAs complete in issue order and
+            // both groups' O += P V(c-2) were issued before it
             if (c >= 2 && !mbar_wait(b_sf + glast, c & 1, s_abort, a.err, kSiteProd)) break;
             const int kr = kvb + s_crow[c];
             mbar_expect_tx(b_kf + s, kTile);
             tma_load_4d(sK + s * kTile, &tk, b_kf + s, 0, kr, hk, bc);
             tma_load_4d(sK + s * kTile + kBox, &tk, b_kf + s, 64, kr, hk, bc);
             issued_k[s]++;
-            if (c >= 2 && !mbar_wait(b_od + glast, c & 1, s_abort, a.err, kSiteProd)) break;
+            if (c >= 2 && !mbar_wait(b_sf + glast, (c - 1) & 1, s_abort, a.err, kSiteProd)) break;
             mbar_expect_tx(b_vf + s, kTile);
             tma_load_4d(sV + s * kTile, &tv, b_vf + s, 0, kr, hk, bc);
             tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
@@ -216,7 +217,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (!(ok = mbar_wait_warp(b_pf + 1, (c - 1) & 1, s_abort, a.err, kSiteMma))) break;
                     tc_fence_after();
                     issue_pv(tO[1], tS[1], aV + sp * kTile, idO, c - 1 > 0);  // O_B += P_B(c-1) V_(c-1)
-                    mma_commit_w(b_od + 1);
                 }
                 issue_qk(tS[1], aQ + kTile, aK + s * kTile, idS);  // S_B(c)
                 mma_commit_w(b_sf + 1);
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!(ok = mbar_wait_warp(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
             tc_fence_after();
             issue_pv(tO[0], tS[0], aV + s * kTile, idO, c > 0);  // O_A += P_A(c) V_c
-            mma_commit_w(b_od + 0);
+            if (c == N - 1) mma_commit_w(b_od + 0);  // O_A final (S_A(c+1) would signal it otherwise)
         }
         if (ok && has_b) {
             const int sp = (N - 1) & 1;
@@ -307,11 +307,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float ls = (s0.x + s0.y) + (s1.x + s1.y);
             const bool resc = alpha != 1.f;
             l = l * alpha + ls;
-            if (c > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (c - 1) & 1, s_abort, a.err, kSiteSoft));
-                if (!ok) break;
-                tc_fence_after();
-            }
+            // O_g += P_g(c-1) V_(c-1) was issued before S_g(c), which is done
             if (c > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -328,7 +324,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_arrive(b_pf + g);
         }
         if (ok && N > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, (N - 1) & 1, s_abort, a.err, kSiteEpi));
+            ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, 0, s_abort, a.err, kSiteEpi));  // committed once
             if (ok) tc_fence_after();
         }
         const bool have = ok && N > 0;
