@@ -279,11 +279,35 @@ def ours(args):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
 
+    # the layout step on either side of the attention: 3D tiling of the
+    # latent [1, 20, 48, 80, heads, 128] into the attention's token order and
+    # back (HBM-bound copies; reported beside the step, not inside it)
+    latent = q.view(1, 20, 48, 80, p.Hq, p.D)
+    tiled_buf, back_buf = torch.empty_like(q), torch.empty_like(latent)
+    var_buf = torch.empty(300, dtype=torch.int32, device=dev)
+    layout = {}
+    for name, fn in (("tile_3d", lambda: vsa.tile_3d(latent, out=tiled_buf, tile_var=var_buf, stream=stream)),
+                     ("untile_3d", lambda: vsa.untile_3d(tiled_buf, (20, 48, 80), out=back_buf, stream=stream))):
+        for _ in range(3):
+            fn()
+        reps = 10
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_ms = e0.elapsed_time(e1) / reps
+        moved = 2 * q.numel() * q.element_size()  # every token row read once and written once
+        layout[name] = {"ms": t_ms, "GB_per_s": moved / (t_ms * 1e-3) / 1e9, "bytes": moved}
+    del tiled_buf, back_buf
+
     if rank != 0:
         if ws > 1:
             torch.distributed.destroy_process_group()
         return
     pk, pk_kind = peaks()
+    for v_ in layout.values():
+        v_["frac_of_hbm"] = v_["GB_per_s"] / pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tensor_peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     value = step_flops * ws / (ms * 1e-3) / 1e12
     dominant = max(kern.items(), key=lambda kv_: kv_[1]["total_ms_per_step"]) if kern else None
@@ -322,6 +346,7 @@ def ours(args):
         "e2e": {"value": step_flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches, "clocks": clocks,
+        "layout_step": {"bound": "hbm", "peak_GB_per_s": pk.get("hbm_gbs"), **layout},
         "kernels": {n: {"avg_ms": round(x["avg_ms"], 4), "launches_per_step": x["launches"] // args.steps,
                         "ms_per_step": round(x["total_ms_per_step"], 4)} for n, x in kern.items()},
     }

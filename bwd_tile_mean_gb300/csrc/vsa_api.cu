@@ -203,6 +203,9 @@ vsa_status cuda_status(cudaError_t e) {
 #define VSA_CUDA(expr) VSA_TRY(cuda_status(expr))
 
 }  // namespace
+
+vsa_status status_from_cuda(cudaError_t e) { return cuda_status(e); }
+
 }  // namespace vsa
 
 using namespace vsa;

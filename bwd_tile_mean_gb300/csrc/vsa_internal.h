@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "vsa.h"
 #include "vsa_common.cuh"
 
 namespace vsa {
@@ -13,6 +14,9 @@ namespace vsa {
 // Instrumentation: every launcher brackets its kernel with these.
 void prof_begin(const char *name, cudaStream_t s);
 void prof_end(cudaStream_t s);
+// VSA_OK for cudaSuccess; otherwise records the error (vsa_last_cuda_error)
+// and returns VSA_ERR_CUDA.
+vsa_status status_from_cuda(cudaError_t e);
 
 // Tile pooling (fp32 means of the first var tokens), [B, H, nT, D].
 cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s);

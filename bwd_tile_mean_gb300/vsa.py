@@ -29,7 +29,8 @@ STATUS = {0: "VSA_OK", 1: "VSA_ERR_NULL", 2: "VSA_ERR_SHAPE", 3: "VSA_ERR_DTYPE"
 EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_static", "vsa_mask_to_index",
            "vsa_fwd", "vsa_bwd",
            "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
-           "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count")
+           "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
+           "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d")
 
 
 class VsaError(RuntimeError):
@@ -91,6 +92,12 @@ def lib():
         L.vsa_profile_ms.restype = C.c_float
         L.vsa_profile_ms.argtypes = [C.c_int]
         L.vsa_launch_count.restype = C.c_longlong
+        L.vsa_tile_3d_count.restype = C.c_int
+        L.vsa_tile_3d_count.argtypes = [C.c_int] * 6
+        L.vsa_tile_3d.restype = C.c_int
+        L.vsa_tile_3d.argtypes = [C.c_int] * 8 + [P, P, P, P]
+        L.vsa_untile_3d.restype = C.c_int
+        L.vsa_untile_3d.argtypes = [C.c_int] * 8 + [P, P, P]
         _lib = L
     return _lib
 
@@ -254,3 +261,43 @@ class Plan:
 
 def default_scale(D: int) -> float:
     return 1.0 / math.sqrt(D)
+
+
+# ------------------------------------------------------------- 3D video tiling
+
+def vsa_tile_3d_count(T, H, W, tile=(4, 8, 8)):
+    return int(lib().vsa_tile_3d_count(T, H, W, *tile))
+
+
+def tile_3d(latent: torch.Tensor, tile=(4, 8, 8), out=None, tile_var=None, stream=None):
+    """latent [B, T, H, W, heads, D] (or [..., row] with any trailing shape)
+    -> (tiled [B, nTiles * prod(tile), heads, D], tile_var [nTiles] int32)."""
+    if not latent.is_contiguous():
+        raise ValueError("tile_3d: latent must be contiguous")
+    B, T, H, W = latent.shape[:4]
+    rest = tuple(latent.shape[4:])
+    n = vsa_tile_3d_count(T, H, W, tile)
+    slots = n * tile[0] * tile[1] * tile[2]
+    row_bytes = latent[0, 0, 0, 0].numel() * latent.element_size()
+    if out is None:
+        out = torch.empty((B, slots) + rest, dtype=latent.dtype, device=latent.device)
+    if tile_var is None:
+        tile_var = torch.empty(n, dtype=torch.int32, device=latent.device)
+    _check("vsa_tile_3d", lib().vsa_tile_3d(B, T, H, W, row_bytes, *tile, _p(latent), _p(out),
+                                            _p(tile_var), _stream(stream)))
+    return out, tile_var
+
+
+def untile_3d(tiled: torch.Tensor, grid, tile=(4, 8, 8), out=None, stream=None):
+    """tiled [B, nTiles * prod(tile), ...] -> latent [B, T, H, W, ...] for grid = (T, H, W)."""
+    if not tiled.is_contiguous():
+        raise ValueError("untile_3d: tiled must be contiguous")
+    T, H, W = grid
+    B = tiled.shape[0]
+    rest = tuple(tiled.shape[2:])
+    row_bytes = tiled[0, 0].numel() * tiled.element_size()
+    if out is None:
+        out = torch.empty((B, T, H, W) + rest, dtype=tiled.dtype, device=tiled.device)
+    _check("vsa_untile_3d", lib().vsa_untile_3d(B, T, H, W, row_bytes, *tile, _p(tiled), _p(out),
+                                                _stream(stream)))
+    return out

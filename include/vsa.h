@@ -197,6 +197,32 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    size_t workspace_bytes, vsa_stream_t stream);
 
 /* Human-readable name of a status. */
+/* 3D video tiling, the layout step on either side of the attention
+ * ([VSA-test]: _BLOCK_SIZE_3D = (4, 8, 8), and _zero_pad_tail, by which
+ * callers scatter a latent into a zeroed tile buffer so that the first var
+ * slots of a tile are its tokens). The pages do not fix the orders; here
+ * tiles are numbered in raster order of their (T, H, W) tile coordinates
+ * and the tokens of a tile fill its first slots in raster order of its own
+ * box, clipped at the latent's edges, so tile k holds var_k = product of
+ * its clipped extents tokens, followed by zero slots.
+ *   latent: device [B, T, H, W, row] with row = row_bytes bytes per token
+ *           (e.g. heads x head_dim 16-bit values), dense;
+ *   tiled:  device [B, nTiles * tT*tH*tW, row], i.e. BSHD with
+ *           S = nTiles * tile (nTiles = vsa_tile_3d_count(...)).
+ * Both pointers 16-byte aligned, row_bytes a multiple of 16; the two
+ * buffers must not overlap. vsa_tile_3d writes every slot of `tiled`
+ * (padding as zeros) and, if tile_var != NULL, the per-tile valid counts
+ * tile_var[nTiles] (int32, device; the kv_var / q_var of the attention
+ * calls). vsa_untile_3d writes every token of `latent` from the valid slots
+ * of `tiled` and reads no padding slot. Errors: VSA_ERR_NULL, VSA_ERR_LAYOUT
+ * (misaligned), VSA_ERR_SHAPE (non-positive size, row_bytes not a multiple
+ * of 16), VSA_ERR_UNSUPPORTED (more than 2^31 - 1 slots), VSA_ERR_CUDA. */
+int vsa_tile_3d_count(int T, int H, int W, int tT, int tH, int tW);
+vsa_status vsa_tile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH, int tW,
+                       const void *latent, void *tiled, int32_t *tile_var, vsa_stream_t stream);
+vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH, int tW,
+                         const void *tiled, void *latent, vsa_stream_t stream);
+
 const char *vsa_status_string(vsa_status status);
 
 /* Message of the last CUDA error behind a VSA_ERR_CUDA return, with the

@@ -22,7 +22,7 @@ def L():
 def declared():
     src = open(os.path.join(ROOT, "include", "vsa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(vsa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(L):

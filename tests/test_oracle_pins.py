@@ -457,3 +457,49 @@ def test_npu_page_length_lists_run_with_patterned_mask():
                                              full[:lq, :lk], p.scale)
                 np.testing.assert_allclose(out[r:r + lq], ro.numpy(), rtol=0, atol=1e-11)
                 r += lq
+
+
+# ------------------------------------------------------------ 3D video tiling
+
+def test_tile3d_divisible_grid_is_the_block_permutation():
+    """On a grid the box divides, tiling is the plain block permutation
+    (tiles in raster order, tokens in raster order inside each tile),
+    written here as one reshape/transpose, independent of the oracle's
+    per-tile loop."""
+    from oracle import tile3d
+    rng = np.random.default_rng(3)
+    B, T, H, W, R = 2, 8, 16, 24, 5
+    x = rng.standard_normal((B, T, H, W, R)).astype(np.float32)
+    tiled, var = tile3d.tile_3d(x, (4, 8, 8))
+    ref = x.reshape(B, 2, 4, 2, 8, 3, 8, R).transpose(0, 1, 3, 5, 2, 4, 6, 7).reshape(B, -1, R)
+    np.testing.assert_array_equal(tiled, ref)
+    assert (var == 256).all() and var.size == 12
+
+
+def test_tile3d_gated_ragged_grid_counts():
+    """The gated-ragged workload's KV grid 21x45x80 tiled 4x8x8 gives 360
+    tiles with valid counts 256 x 250, 160 x 50, 64 x 50 and 40 x 10, the
+    same list, in the same raster order, as the workload's kv_var."""
+    from oracle import tile3d
+    x = np.zeros((1, 21, 45, 80, 1), dtype=np.float32)
+    _, var = tile3d.tile_3d(x, (4, 8, 8))
+    vals, counts = np.unique(var, return_counts=True)
+    assert dict(zip(vals.tolist(), counts.tolist())) == {40: 10, 64: 50, 160: 50, 256: 250}
+    assert tile3d.tile_count(21, 45, 80) == 360
+    from bwd_tile_mean_gb300.inputs import config
+    assert var.tolist() == list(config(4).kv_var)
+
+
+def test_tile3d_round_trip_and_zero_padding():
+    """untile(tile(x)) == x on ragged grids; every slot past a tile's count
+    is zero; the counts sum to the number of tokens."""
+    from oracle import tile3d
+    rng = np.random.default_rng(4)
+    for grid in [(5, 9, 7), (1, 1, 1), (4, 8, 8), (6, 17, 3)]:
+        x = rng.standard_normal((2,) + grid + (3,)).astype(np.float32) + 1.0
+        tiled, var = tile3d.tile_3d(x, (4, 8, 8))
+        np.testing.assert_array_equal(tile3d.untile_3d(tiled, grid, (4, 8, 8)), x)
+        assert int(var.sum()) == grid[0] * grid[1] * grid[2]
+        slots = tiled.reshape(2, var.size, 256, 3)
+        for k, n in enumerate(var):
+            assert (slots[:, k, n:] == 0).all() and (slots[:, k, :n] != 0).all()
