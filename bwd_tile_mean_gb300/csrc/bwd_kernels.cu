@@ -917,6 +917,57 @@ __global__ void __launch_bounds__(128) k_compress_cols(Prob p, const float *__re
 
 }  // namespace
 
+namespace {
+
+// dgate of the gated compression branch: out_t = O_t + gate_t (*) c_i for
+// every slot t of query tile i, so dgate_t = dO_t (*) c_i (fp32 product,
+// rounded once). A half-warp per (b, slot, head) row, 16 bytes per thread;
+// in TND only rows inside a sequence exist.
+template <typename T>
+__global__ void __launch_bounds__(256) k_gate_grad(Prob p, const T *__restrict__ dO, const float *__restrict__ c,
+                                                   T *__restrict__ dgate) {
+    const int sub = threadIdx.x & 15;
+    const long long slots = (long long)p.nQ * p.tile_q;
+    const long long per_b = slots * p.Hq;
+    const long long units = (long long)p.B * per_b;
+    const long long step = ((long long)gridDim.x * blockDim.x) >> 4;
+    for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 4; u < units; u += step) {
+        const int b = (int)(u / per_b);
+        const long long rem = u - (long long)b * per_b;
+        const int s = (int)(rem / p.Hq), h = (int)(rem % p.Hq);
+        if (p.layout == L_TND && s >= p.cu_q[b + 1] - p.cu_q[b]) continue;
+        const long long o = tok_off(p, true, b, s, h) + sub * 8;
+        const float *cc = c + (((long long)b * p.Hq + h) * p.nQ + s / p.tile_q) * 128 + sub * 8;
+        const uint4 g = *reinterpret_cast<const uint4 *>(dO + o);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = unpack2<T>(gw[t]);
+            r[t] = pack2<T>(f.x * cc[2 * t], f.y * cc[2 * t + 1]);
+        }
+        *reinterpret_cast<uint4 *>(dgate + o) = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gate_grad(const Prob &p, const void *dO, const float *c, void *dgate, cudaStream_t s) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long units = (long long)p.B * p.nQ * p.tile_q * p.Hq;
+    const long long want = (units * 16 + 255) / 256;
+    const int grid = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
+    prof_begin("gate_grad", s);
+    if (p.dtype == T_BF16)
+        k_gate_grad<__nv_bfloat16><<<grid, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, c, (__nv_bfloat16 *)dgate);
+    else
+        k_gate_grad<__half><<<grid, 256, 0, s>>>(p, (const __half *)dO, c, (__half *)dgate);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *nlse2,
                             float *ndvec, cudaStream_t s) {
     const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;

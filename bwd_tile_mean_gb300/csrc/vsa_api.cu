@@ -298,6 +298,28 @@ vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const voi
     return VSA_OK;
 }
 
+vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                         const int32_t *q_var, const int32_t *kv_var, void *dgate, void *workspace,
+                         size_t workspace_bytes, vsa_stream_t stream) {
+    Prob p0, p;
+    VSA_TRY(to_prob(desc, &p0));
+    VSA_TRY(need_vars(p0, q_var, kv_var, &p, true));
+    if (!dO || !q || !k || !v || !dgate) return VSA_ERR_NULL;
+    if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dgate))
+        return VSA_ERR_LAYOUT;
+    VSA_TRY(check_ws(p, true, workspace, workspace_bytes));
+    const WsLayout L = ws_layout(p, true);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
+    float *c = at<float>(workspace, L.c);
+    VSA_CUDA(launch_pool(p, true, q, pq, s));
+    VSA_CUDA(launch_pool(p, false, k, pk, s));
+    VSA_CUDA(launch_pool(p, false, v, pv, s));
+    VSA_CUDA(launch_compress_fwd(p, pq, pk, pv, c, s));
+    VSA_CUDA(launch_gate_grad(p, dO, c, dgate, s));
+    return VSA_OK;
+}
+
 vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
                    const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
                    const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var, const int32_t *kv_var,

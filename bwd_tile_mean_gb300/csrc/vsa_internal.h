@@ -49,6 +49,8 @@ struct FwdArgs {
 cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s);
 
 // Compression branch, forward: c_i = sum_j softmax_j(scale pq.pk_j) pv_j.
+// Gated compression, gradient of the gate: dgate_t = dO_t (*) c_(tile of t).
+cudaError_t launch_gate_grad(const Prob &p, const void *dO, const float *c, void *dgate, cudaStream_t s);
 cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk, const float *pv,
                                 float *c, cudaStream_t s);
 

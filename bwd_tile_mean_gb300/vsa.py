@@ -30,7 +30,7 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_fwd", "vsa_bwd",
            "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
-           "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d")
+           "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad")
 
 
 class VsaError(RuntimeError):
@@ -92,6 +92,8 @@ def lib():
         L.vsa_profile_ms.restype = C.c_float
         L.vsa_profile_ms.argtypes = [C.c_int]
         L.vsa_launch_count.restype = C.c_longlong
+        L.vsa_gate_grad.restype = C.c_int
+        L.vsa_gate_grad.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.vsa_tile_3d_count.restype = C.c_int
         L.vsa_tile_3d_count.argtypes = [C.c_int] * 6
         L.vsa_tile_3d.restype = C.c_int
@@ -160,6 +162,12 @@ def vsa_bwd(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, idx_cap, kv_ptr, kv_
     _check("vsa_bwd", lib().vsa_bwd(
         C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(o_sparse), _p(lse), _p(q_idx), _p(q_cnt), int(idx_cap),
         _p(kv_ptr), _p(kv_qidx), _p(q_var), _p(kv_var), _p(gate), _p(dq), _p(dk), _p(dv), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def vsa_gate_grad(desc, dO, q, k, v, q_var, kv_var, dgate, workspace, stream=None):
+    _check("vsa_gate_grad", lib().vsa_gate_grad(
+        C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(q_var), _p(kv_var), _p(dgate), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -254,6 +262,12 @@ class Plan:
         vsa_bwd(self.desc, dO, q, k, v, o_sparse, lse, self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr,
                 self.kv_qidx, self.q_var, self.kv_var, gate, dq, dk, dv, self.workspace, stream)
         return dq, dk, dv
+
+    def gate_grad(self, dO, q, k, v, dgate=None, stream=None):
+        """dgate = dO (*) c (the plan must have been made with gate=True)."""
+        dgate = torch.empty_like(dO) if dgate is None else dgate
+        vsa_gate_grad(self.desc, dO, q, k, v, self.q_var, self.kv_var, dgate, self.workspace, stream)
+        return dgate
 
     def device_status(self, stream=None) -> int:
         return vsa_device_status(self.workspace, stream)

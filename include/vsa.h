@@ -197,6 +197,17 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    size_t workspace_bytes, vsa_stream_t stream);
 
 /* Human-readable name of a status. */
+/* Gradient of the compression gate (the pages' gate carries no gradient:
+ * [VSA-test] builds it without requires_grad). With out = O + gate (*) c
+ * (vsa_fwd, gated), dgate_t = dO_t (*) c_i for every slot t of query tile
+ * i (TND: every row inside a sequence); c is recomputed from q, k, v.
+ * dO and dgate are q-shaped in `layout` (dgate: same dtype), 16-byte
+ * aligned; workspace sized by vsa_workspace_size(desc, 1). Errors as for
+ * vsa_fwd. */
+vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                         const int32_t *q_var, const int32_t *kv_var, void *dgate, void *workspace,
+                         size_t workspace_bytes, vsa_stream_t stream);
+
 /* 3D video tiling, the layout step on either side of the attention
  * ([VSA-test]: _BLOCK_SIZE_3D = (4, 8, 8), and _zero_pad_tail, by which
  * callers scatter a latent into a zeroed tile buffer so that the first var

@@ -180,6 +180,25 @@ def forward_rows(p, q, k, v, q_idx, q_cnt, cap, gate=None, rows=None):
     return out
 
 
+def gate_grad(p, dO, q, k, v) -> np.ndarray:
+    """Gradient of the compression gate, float64 in dO's shape: out = O +
+    gate (*) c_i over every slot of query tile i, hence dgate = dO (*) c_i
+    (padded layouts: every slot; TND: rows inside a sequence, zero
+    elsewhere)."""
+    c = compress_c(p, q, k, v)
+    dO = _f64(dO)
+    dg = np.zeros_like(dO)
+    for b, h, s in p.rows():
+        i = s // p.tile_q
+        if p.layout == "bhsd":
+            dg[b, h, s] = dO[b, h, s] * c[b, h, i]
+        elif p.layout == "bshd":
+            dg[b, s, h] = dO[b, s, h] * c[b, h, i]
+        else:
+            dg[p.cu_q[b] + s, h] = dO[p.cu_q[b] + s, h] * c[b, h, i]
+    return dg
+
+
 def compress_grads(p, dO, gate, q, k, v):
     bd = _Bound(p)
     dpq = np.zeros((p.B, p.Hq, p.nQ, p.D))

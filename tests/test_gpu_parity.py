@@ -196,3 +196,21 @@ def test_backward_bitwise_deterministic():
     torch.cuda.synchronize()
     for a, b in zip(r1, r2):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("p", gated_cases(), ids=lambda p: p.name)
+def test_gate_grad_parity(p):
+    """dgate = dO (*) c from vsa_gate_grad against the oracle (fp64), with
+    the gradient tolerance; rows outside TND sequences stay untouched."""
+    t = make_tensors(p)
+    g = to_device(t)
+    plan = plan_for(p)
+    dgate = torch.full_like(g["dO"], 7.0)
+    plan.gate_grad(g["dO"], g["q"], g["k"], g["v"], dgate=dgate)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    ref = orc.gate_grad(p, t["dO"], t["q"], t["k"], t["v"])
+    got = dgate.double().cpu().numpy()
+    if p.layout == "tnd":
+        assert got.shape[0] == p.cu_q[-1]
+    check_tol(f"{p.name} dgate", ref, got, GRAD_TOL)

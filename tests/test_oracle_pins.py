@@ -503,3 +503,31 @@ def test_tile3d_round_trip_and_zero_padding():
         slots = tiled.reshape(2, var.size, 256, 3)
         for k, n in enumerate(var):
             assert (slots[:, k, n:] == 0).all() and (slots[:, k, :n] != 0).all()
+
+
+# ----------------------------------------------- compression gate gradient
+
+def test_gate_grad_matches_finite_differences_of_the_forward():
+    """dgate from the oracle's closed form equals the central difference of
+    the oracle's gated forward output (out = O + gate (*) c is linear in the
+    gate, so the difference is exact up to rounding), at positions in full,
+    partial and padding slots of several tiles and heads."""
+    p = Problem("gate-fd", "bshd", 1, 2, 2, 128, 256, 256, 3, 4, q_var=[256, 100, 7],
+                kv_var=[256, 40, 0, 199], topk=2, gate="randn01", seed=41)
+    t = make_tensors(p)
+    q, k, v, dO, gate = (_np(t[n]).astype(np.float64) for n in ("q", "k", "v", "dO", "gate"))
+    dg = orc.gate_grad(p, dO, q, k, v)
+    _, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    eps = 0.5
+    for (s, h, d) in [(0, 0, 0), (300, 1, 17), (511, 0, 127), (600, 1, 64), (767, 0, 5)]:
+        rows = np.asarray([[0, h, s]], dtype=np.int32)
+        gp, gm = gate.copy(), gate.copy()
+        gp[0, s, h, d] += eps
+        gm[0, s, h, d] -= eps
+        op = orc.forward_rows(p, q, k, v, qi, qc, p.cap, gate=gp, rows=rows)[0]
+        om = orc.forward_rows(p, q, k, v, qi, qc, p.cap, gate=gm, rows=rows)[0]
+        fd = (op[0, d] - om[0, d]) / (2 * eps) * dO[0, s, h, d]
+        assert abs(fd - dg[0, s, h, d]) <= 1e-12 * max(1.0, abs(fd)), (s, h, d, fd, dg[0, s, h, d])
+        # nothing else in the row moves with this gate element
+        others = np.delete(np.arange(128), d)
+        assert np.allclose(op[0, others], om[0, others], rtol=0, atol=1e-12)
