@@ -168,6 +168,36 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ layout step
+
+def layout_step(q, p, dev, stream, e0, e1):
+    """Times the 3D tiling of the latent [1, 20, 48, 80, heads, 128] into the
+    attention's token order (tile_3d) and back (untile_3d): HBM-bound copies
+    that move every token row once each way."""
+    import torch
+
+    from bwd_tile_mean_gb300 import vsa
+
+    latent = q.view(1, 20, 48, 80, p.Hq, p.D)
+    tiled_buf, back_buf = torch.empty_like(q), torch.empty_like(latent)
+    var_buf = torch.empty(300, dtype=torch.int32, device=dev)
+    res = {}
+    for name, fn in (("tile_3d", lambda: vsa.tile_3d(latent, out=tiled_buf, tile_var=var_buf, stream=stream)),
+                     ("untile_3d", lambda: vsa.untile_3d(tiled_buf, (20, 48, 80), out=back_buf, stream=stream))):
+        for _ in range(3):
+            fn()
+        reps = 10
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_ms = e0.elapsed_time(e1) / reps
+        moved = 2 * q.numel() * q.element_size()  # every token row read once and written once
+        res[name] = {"ms": t_ms, "GB_per_s": moved / (t_ms * 1e-3) / 1e9, "bytes": moved}
+    return res
+
+
 # ------------------------------------------------------------------ ours
 
 def ours(args):
@@ -181,26 +211,31 @@ def ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    p = inputs.config(3)
-    if args.heads != p.Hq:  # smaller replica of the same workload (profiling captures)
+    p = inputs.config(args.config)
+    if args.config == 3 and args.heads != p.Hq:  # smaller replica of the same workload (profiling captures)
         p = inputs.Problem(p.name, p.layout, p.B, args.heads, args.heads, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV,
                            q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, seed=p.seed)
+    gated = p.gate is not None
+    train = p.backward
     T = inputs.DTYPES[p.dtype]
     t = inputs.make_tensors(p, device=dev)
     q, k, v, dO = t["q"], t["k"], t["v"], t["dO"]
     i32 = dict(dtype=torch.int32, device=dev)
     plan = vsa.Plan(p.layout, T, p.B, p.Hq, p.Hkv, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV, p.Sq, p.Skv, p.cap,
-                    q_var=torch.as_tensor(p.q_var, **i32), kv_var=torch.as_tensor(p.kv_var, **i32),
+                    gate=gated, q_var=torch.as_tensor(p.q_var, **i32), kv_var=torch.as_tensor(p.kv_var, **i32),
                     scale=p.scale, device=dev)
+    gate = t.get("gate")
     out = torch.empty_like(q)
+    osp = torch.empty_like(q) if gated else None
     lse = torch.empty(plan.lse_shape(), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
 
     def step(qq, kk, vv, dd):
-        plan.build_block_map(qq, kk, p.topk, need_bwd_index=True)
-        plan.forward(qq, kk, vv, out=out, lse=lse)
-        plan.backward(dd, qq, kk, vv, out, lse, dq=dq, dk=dk, dv=dv)
+        plan.build_block_map(qq, kk, p.topk, need_bwd_index=train)
+        plan.forward(qq, kk, vv, gate=gate, out=out, lse=lse, o_sparse=osp)
+        if train:
+            plan.backward(dd, qq, kk, vv, osp if gated else out, lse, gate=gate, dq=dq, dk=dk, dv=dv)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -222,7 +257,7 @@ def ours(args):
     pairs = int(qc.sum().item())
     flop_unit = 2.0 * p.D * p.tile_q  # x N x 7 per pair
     fwd_flops = flop_unit * float(valid_keys.item()) * 2
-    step_flops = flop_unit * float(valid_keys.item()) * 7
+    step_flops = flop_unit * float(valid_keys.item()) * (7 if train else 2)
 
     bus = None
     try:
@@ -282,24 +317,9 @@ def ours(args):
     # the layout step on either side of the attention: 3D tiling of the
     # latent [1, 20, 48, 80, heads, 128] into the attention's token order and
     # back (HBM-bound copies; reported beside the step, not inside it)
-    latent = q.view(1, 20, 48, 80, p.Hq, p.D)
-    tiled_buf, back_buf = torch.empty_like(q), torch.empty_like(latent)
-    var_buf = torch.empty(300, dtype=torch.int32, device=dev)
     layout = {}
-    for name, fn in (("tile_3d", lambda: vsa.tile_3d(latent, out=tiled_buf, tile_var=var_buf, stream=stream)),
-                     ("untile_3d", lambda: vsa.untile_3d(tiled_buf, (20, 48, 80), out=back_buf, stream=stream))):
-        for _ in range(3):
-            fn()
-        reps = 10
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        t_ms = e0.elapsed_time(e1) / reps
-        moved = 2 * q.numel() * q.element_size()  # every token row read once and written once
-        layout[name] = {"ms": t_ms, "GB_per_s": moved / (t_ms * 1e-3) / 1e9, "bytes": moved}
-    del tiled_buf, back_buf
+    if args.config == 3:
+        layout = layout_step(q, p, dev, stream, e0, e1)
 
     if rank != 0:
         if ws > 1:
@@ -326,7 +346,7 @@ def ours(args):
                     "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
                     "flops_per_launch": launch_flops}
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.config == 3:
         v_cpu, dt, desc, threads = oracle_sample(n_tiles=2)
         cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
                "seconds": dt}
@@ -334,8 +354,11 @@ def ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "video-dit-76800: latent 20x48x80 tiled 4x8x8 -> 300 tiles, 76,800 tokens; "
-                               f"B=1, H={p.Hq}, D=128, bf16, BSHD; topk 30 (10% density)",
+        "config": {"workload": ("video-dit-76800: latent 20x48x80 tiled 4x8x8 -> 300 tiles, 76,800 tokens; "
+                                f"B=1, H={p.Hq}, D=128, bf16, BSHD; topk 30 (10% density)") if args.config == 3 else
+                               (f"{p.name}: B={p.B}, H={p.Hq}/{p.Hkv}, D=128, {p.dtype}, {p.layout}, "
+                                f"{p.nQ} Q x {p.nKV} KV tiles of {p.tile_q}/{p.tile_kv}, topk {p.topk}"
+                                + (", gated" if gated else "") + ("" if train else ", forward only")),
                    "selected_pairs": pairs, "tflop_per_step": step_flops / 1e12,
                    "fwd_tflop_per_step": fwd_flops / 1e12,
                    "l2": "inputs larger than L2 (each of q, k, v, dO is 786 MB vs 126 MB L2); no flush",
@@ -363,6 +386,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=40, help="heads of the workload (40; fewer only for profiling)")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 3, 4, 5],
+                    help="workload: 3 = video DiT 76,800 tokens (the headline); 1 tiny, 4 gated ragged, "
+                         "5 long-video forward only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -831,7 +831,9 @@ __global__ void __launch_bounds__(128) k_compress_rows(Prob p, const float *__re
                                                        float *__restrict__ ds, float *__restrict__ dpq) {
     extern __shared__ float sh[];  // sA[nKV], sD[nKV]
     float *sA = sh, *sD = sh + p.nKV;
-    __shared__ float spq[128], sdc[128], red[4];
+    __shared__ __align__(16) float spq[128];
+    __shared__ __align__(16) float sdc[128];
+    __shared__ float red[4];
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
@@ -840,20 +842,30 @@ __global__ void __launch_bounds__(128) k_compress_rows(Prob p, const float *__re
     __syncthreads();
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
     const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    // scores and dA: warp w takes tiles j = w, w+4, ...; its lanes split the
+    // 128 dims (one float4 each, coalesced) and reduce across the warp
     float mx = -INFINITY;
-    for (int j = t; j < p.nKV; j += 128) {
+    const float4 q4 = reinterpret_cast<const float4 *>(spq)[lane];
+    const float4 c4 = reinterpret_cast<const float4 *>(sdc)[lane];
+    for (int j = w; j < p.nKV; j += 4) {
         float x = -INFINITY, da = 0.f;
         if (kv_valid(p, b, j) > 0) {
-            float acc = 0.f, acc2 = 0.f;
-            for (int e = 0; e < 128; ++e) {
-                acc = fmaf(spq[e], pkh[(long long)j * 128 + e], acc);
-                acc2 = fmaf(sdc[e], pvh[(long long)j * 128 + e], acc2);
+            const float4 k4 = reinterpret_cast<const float4 *>(pkh + (long long)j * 128)[lane];
+            const float4 v4 = reinterpret_cast<const float4 *>(pvh + (long long)j * 128)[lane];
+            float acc = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+            float acc2 = c4.x * v4.x + c4.y * v4.y + c4.z * v4.z + c4.w * v4.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                acc2 += __shfl_xor_sync(0xffffffffu, acc2, off);
             }
             x = acc * p.scale;
             da = acc2;
         }
-        sA[j] = x;
-        sD[j] = da;
+        if (lane == 0) {
+            sA[j] = x;
+            sD[j] = da;
+        }
         mx = fmaxf(mx, x);
     }
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));

@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(128) k_compress_fwd(Prob p, const float *__res
                                                       const float *__restrict__ pk,
                                                       const float *__restrict__ pv, float *__restrict__ c) {
     extern __shared__ float sA[];  // [nKV]
-    __shared__ float spq[128];
+    __shared__ __align__(16) float spq[128];
     __shared__ float red[4];
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -426,23 +426,20 @@ __global__ void __launch_bounds__(128) k_compress_fwd(Prob p, const float *__res
     __syncthreads();
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
     const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    // scores: warp w takes tiles j = w, w+4, ...; its lanes split the 128
+    // dims (one float4 each, coalesced) and reduce across the warp
     float mx = -INFINITY;
-    for (int j = t; j < p.nKV; j += 128) {
+    const float4 q4 = reinterpret_cast<const float4 *>(spq)[lane];
+    for (int j = w; j < p.nKV; j += 4) {
         float x = -INFINITY;
         if (kv_valid(p, b, j) > 0) {
-            const float4 *kr = reinterpret_cast<const float4 *>(pkh + (long long)j * 128);
-            float acc = 0.f;
-#pragma unroll 8
-            for (int e = 0; e < 32; ++e) {
-                const float4 kv4 = kr[e];
-                acc = fmaf(spq[4 * e], kv4.x, acc);
-                acc = fmaf(spq[4 * e + 1], kv4.y, acc);
-                acc = fmaf(spq[4 * e + 2], kv4.z, acc);
-                acc = fmaf(spq[4 * e + 3], kv4.w, acc);
-            }
+            const float4 k4 = reinterpret_cast<const float4 *>(pkh + (long long)j * 128)[lane];
+            float acc = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             x = acc * p.scale;
         }
-        sA[j] = x;
+        if (lane == 0) sA[j] = x;
         mx = fmaxf(mx, x);
     }
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
