@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ 
         const long long w = wbase + it * 2 + half;
         if (hl == 0 && w < slots) {
             ndvec[w] = ex[it] ? -acc : 0.f;
-            nlse2[w] = ex[it] ? -lse[lo[it]] * kLog2e : -INFINITY;
+            const float lv = ex[it] ? lse[lo[it]] : -INFINITY;
+            nlse2[w] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
         }
     }
 }
@@ -215,6 +216,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(b_fin + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nwork = reinterpret_cast<int *>(s_tmem + 2);
+    // per stage: the item's query-block bits and its 64-row piece index
+    int *s_item = reinterpret_cast<int *>(sm + kDkOffCtl + 160);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int subs_kv = p.tile_kv >> 7;
@@ -286,6 +289,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             const int row = qb + w.i * p.tile_q + w.sub * kDkItem;
             const long long slot =
                 ((long long)b * p.Hq + w.h) * p.nQ * p.tile_q + w.i * p.tile_q + w.sub * kDkItem;
+            if (a.kv_qsub) {  // read by the softmax after this stage's barrier completes
+                s_item[2 * st] = a.kv_qsub[((long long)b * p.Hq + w.h) * p.nQ * a.cap + w.pos];
+                s_item[2 * st + 1] = w.sub;
+            }
             mbar_expect_tx(b_qf + st, 2 * kDkQTile + 512);
             tma_load_4d(sQ + st * kDkQTile, &tq, b_qf + st, 0, row, w.h, bc);
             tma_load_4d(sQ + st * kDkQTile + kDkQBox, &tq, b_qf + st, 64, row, w.h, bc);
@@ -359,6 +366,13 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tmem_ld32(tl + cs + 64, dr);
             tmem_wait_ld();
             if (!key_ok) {  // keys past the chunk's valid count: P^T = 0
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(-INFINITY);
+            }
+            // query blocks that did not select this tile: P^T = 0 in their
+            // columns (block_q is a multiple of 32, so this warp's 32 columns
+            // lie in one block)
+            if (a.kv_qsub && !((s_item[2 * st] >> ((s_item[2 * st + 1] * kDkItem + ch * 32) / a.block_q)) & 1)) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(-INFINITY);
             }
@@ -481,15 +495,16 @@ constexpr size_t kDqSmem = kDqOffCtl + 256;
 // the index is read once per 32 tiles rather than once per chunk, and a
 // chunk's tile is found with a ballot. All lanes call with the same c.
 struct ChunkWin {
-    const int *idx;
+    const int *idx, *sub;  // sub: query-block bit masks of the entries (NULL: whole tiles)
     int cnt, per;
     int n0, c0, chunks;  // first tile and first chunk of the window; chunks in it
-    int j, kvv, nch, first;  // this lane's tile
+    int j, kvv, nch, first, bits;  // this lane's tile
 };
 __device__ __forceinline__ void win_load(const Prob &p, int b, ChunkWin &w, int lane) {
     const int n = w.n0 + lane;
     w.j = n < w.cnt ? w.idx[n] : 0;
     w.kvv = n < w.cnt ? kv_valid(p, b, w.j) : 0;
+    w.bits = (n < w.cnt && w.sub) ? w.sub[n] : -1;
     w.nch = min(w.per, (w.kvv + 127) >> 7);
     int inc = w.nch;
 #pragma unroll
@@ -500,9 +515,11 @@ __device__ __forceinline__ void win_load(const Prob &p, int b, ChunkWin &w, int 
     w.first = inc - w.nch;
     w.chunks = __shfl_sync(0xffffffffu, inc, 31);
 }
-__device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *idx, int cnt, int lane) {
+__device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *idx, const int *sub, int cnt,
+                                               int lane) {
     ChunkWin w;
     w.idx = idx;
+    w.sub = sub;
     w.cnt = cnt;
     w.per = p.tile_kv >> 7;
     w.n0 = 0;
@@ -512,7 +529,8 @@ __device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *i
 }
 // Row (of the KV tile's first key, within the batch entry) and valid key
 // count of chunk c; chunks are visited in increasing order.
-__device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int c, int lane, int &row, int &valid) {
+__device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int c, int lane, int &row, int &valid,
+                                          int &bits) {
     while (c >= w.c0 + w.chunks) {
         if (w.n0 + 32 >= w.cnt) return false;
         w.c0 += w.chunks;
@@ -525,6 +543,7 @@ __device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int
     const int first = __shfl_sync(0xffffffffu, w.first, L);
     const int kvv = __shfl_sync(0xffffffffu, w.kvv, L);
     const int j = __shfl_sync(0xffffffffu, w.j, L);
+    bits = __shfl_sync(0xffffffffu, w.bits, L);
     const int sub = cw - first;
     row = j * p.tile_kv + sub * 128;
     valid = min(128, kvv - sub * 128);
@@ -611,7 +630,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (warp == kProdWarp && N > 0) {
         // ------------------------------------ TMA producer (whole warp, lane 0 issues)
-        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_cnt[qrow], lane);
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, a.q_cnt[qrow], lane);
         if (lane == 0) {
             mbar_expect_tx(b_q, 2 * kTile);
             tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
@@ -621,8 +640,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
-            int crow = 0, cval = 0;
-            if (!win_chunk(p, b, cw, c, lane, crow, cval)) break;
+            int crow = 0, cval = 0, cbits = -1;
+            if (!win_chunk(p, b, cw, c, lane, crow, cval, cbits)) break;
             const int sk = c % kDqKStages, sv = c % kDqVStages;
             const int kr = kvb + crow;
             // V first: its stage frees when dP(c-2) completes, which precedes
@@ -693,11 +712,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const float nl2 = N > 0 ? a.nlse2[slot] : -INFINITY;
         const float ndv = N > 0 ? a.ndvec[slot] : 0.f;
         bool ok = true;
-        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_cnt[qrow], lane);
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_sub ? a.q_sub + qrow * a.cap : nullptr,
+                                a.q_cnt[qrow], lane);
         for (int c = 0; c < N; ++c) {
-            int crow = 0, cval = 0;
-            win_chunk(p, b, cw, c, lane, crow, cval);
-            const int valid = cval - ch * 64;
+            int crow = 0, cval = 0, cbits = -1;
+            win_chunk(p, b, cw, c, lane, crow, cval, cbits);
+            int valid = cval - ch * 64;
+            // query blocks: a row whose block did not select this tile sees no key of it
+            if (a.q_sub && !((cbits >> ((half * 128 + r) / a.block_q)) & 1)) valid = 0;
             uint32_t sr[64], dr[64];
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
             if (!ok) break;

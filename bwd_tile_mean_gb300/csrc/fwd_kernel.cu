@@ -43,7 +43,7 @@ namespace {
 constexpr int kTile = 32 * 1024;  // one [128 x 128] 16-bit tile = two 64-column TMA boxes
 constexpr int kBox = 16 * 1024;
 constexpr int kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile, kOffCtl = 6 * kTile;
-constexpr int kCtlBytes = 256 + kMaxChunks * 4 + kMaxChunks * 2;
+constexpr int kCtlBytes = 256 + kMaxChunks * 4 + kMaxChunks * 2 + kMaxChunks * 4;
 constexpr size_t kFwdSmem = kOffCtl + kCtlBytes;
 constexpr int kFwdThreads = 320;
 constexpr int kFwdProdWarp = 8, kFwdMmaWarp = 9;
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     int *s_crow = reinterpret_cast<int *>(sm + kOffCtl + 256);
     short *s_cval = reinterpret_cast<short *>(s_crow + kMaxChunks);
+    int *s_csub = reinterpret_cast<int *>(s_cval + kMaxChunks);  // query-block bits of each chunk's tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
@@ -134,11 +135,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int total = 0;
         for (int n0 = 0; n0 < cnt; n0 += 32) {
             const int n = n0 + lane;
-            int j = 0, kvv = 0, nc = 0;
+            int j = 0, kvv = 0, nc = 0, bits = -1;
             if (n < cnt) {
                 j = idx[n];
                 kvv = kv_valid(p, b, j);
                 nc = min(per, (kvv + 127) >> 7);
+                if (a.q_sub) bits = a.q_sub[qrow * a.cap + n];
             }
             int inc = nc;
 #pragma unroll
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (pos < kMaxChunks) {
                     s_crow[pos] = j * p.tile_kv + c * 128;
                     s_cval[pos] = (short)min(128, kvv - c * 128);
+                    s_csub[pos] = bits;
                 }
             }
             total += __shfl_sync(0xffffffffu, inc, 31);
@@ -248,7 +251,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(b_sf + g, c & 1, s_abort, a.err, kSiteSoft));
             if (!ok) break;
             tc_fence_after();
-            const int valid = s_cval[c];
+            int valid = s_cval[c];
+            // query blocks: a row whose block did not select this tile sees no key of it
+            if (a.q_sub && !((s_csub[c] >> ((g * 128 + r) / a.block_q)) & 1)) valid = 0;
             // The whole row of S (128 scores) comes into registers with one
             // wait; its max is taken first (the scale is positive, so on raw
             // scores). A row whose max exceeds the running max by more than
@@ -284,7 +289,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 alpha = ex2(m_ref - mx);  // 0 on the first chunk
                 m_ref = mx;
             }
-            const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_ref, -m_ref);
+            // (a row that has seen no key yet keeps m_ref = -inf; its scores
+            // are all -inf and must give P = 0, not inf - inf)
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_use, -m_use);
             uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -327,9 +335,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(b_od + g, 0, s_abort, a.err, kSiteEpi));  // committed once
             if (ok) tc_fence_after();
         }
-        const bool have = ok && N > 0;
-        const float inv_l = have ? 1.f / l : 0.f;
-        const float lse_v = have ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        const bool have = ok && N > 0;                 // warp-uniform: TMEM holds O
+        const bool row_has = have && l > 0.f;           // l = 0: the row saw no key (O = 0, LSE = -inf)
+        const float inv_l = row_has ? 1.f / l : 0.f;
+        const float lse_v = row_has ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
         const bool row_ok = r < nrows[g];
         const int row = i * p.tile_q + g * 128 + r;  // within the batch entry
         const long long ro = tok_off(p, true, b, row, h);

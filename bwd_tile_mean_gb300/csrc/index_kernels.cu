@@ -294,4 +294,98 @@ cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ query blocks
+// A caller's mask at query-block granularity: block_q rows (dividing
+// tile_q) x one KV tile, [B, Hq, nQb, nKV] ([NPU-test]: block_shape
+// [32, 128] and [64, 128]). The attention kernels keep tiles of tile_q
+// rows: a tile attends to the union of its blocks' selections, and a bit
+// mask per (tile, selected KV tile) -- bit s set iff block s of the tile
+// selected it -- masks the keys row by row.
+namespace {
+
+__device__ __forceinline__ bool block_exists(const Prob &p, int b, int i, int s, int bq, int nQb) {
+    const int blk = i * (p.tile_q / bq) + s;
+    if (blk >= nQb) return false;
+    if (p.layout == L_TND) return i * p.tile_q + s * bq < p.cu_q[b + 1] - p.cu_q[b];
+    return true;
+}
+__device__ __forceinline__ int tile_bits(const Prob &p, const uint8_t *__restrict__ bm, int nQb, int bq, int b,
+                                         int h, int i, int j) {
+    const int ns = p.tile_q / bq;
+    const uint8_t *m = bm + ((long long)b * p.Hq + h) * nQb * p.nKV;
+    int bits = 0;
+    for (int sb = 0; sb < ns; ++sb)
+        if (block_exists(p, b, i, sb, bq, nQb) && m[(long long)(i * ns + sb) * p.nKV + j] != 0) bits |= 1 << sb;
+    return bits;
+}
+
+// tile map = union over each tile's blocks
+__global__ void __launch_bounds__(256) k_block_union(Prob p, int bq, int nQb, const uint8_t *__restrict__ bm,
+                                                     uint8_t *__restrict__ tmap) {
+    const long long n = (long long)p.B * p.Hq * p.nQ * p.nKV;
+    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n;
+         x += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(x % p.nKV);
+        const long long r = x / p.nKV;
+        const int i = (int)(r % p.nQ), h = (int)((r / p.nQ) % p.Hq), b = (int)(r / ((long long)p.nQ * p.Hq));
+        tmap[x] = tile_bits(p, bm, nQb, bq, b, h, i, j) != 0;
+    }
+}
+
+// bit masks of the Q-owned index entries and, when kv_ptr is given, of the
+// KV-owned ones (entry pos of KV tile j: kv_ptr[j] <= pos < kv_ptr[j+1])
+__global__ void __launch_bounds__(256) k_block_bits(Prob p, int bq, int nQb, const uint8_t *__restrict__ bm,
+                                                    const int *__restrict__ q_idx, const int *__restrict__ q_cnt,
+                                                    int cap, int *__restrict__ q_sub, const int *__restrict__ kv_ptr,
+                                                    const int *__restrict__ kv_qidx, int *__restrict__ kv_qsub) {
+    const long long n = (long long)p.B * p.Hq * p.nQ * cap;
+    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n;
+         x += (long long)gridDim.x * blockDim.x) {
+        const long long r = x / cap;  // (b, h, i) row of the Q-owned index; also the KV-owned list's entry
+        const int slot = (int)(x % cap);
+        const int i = (int)(r % p.nQ), h = (int)((r / p.nQ) % p.Hq), b = (int)(r / ((long long)p.nQ * p.Hq));
+        q_sub[x] = slot < q_cnt[r] ? tile_bits(p, bm, nQb, bq, b, h, i, q_idx[x]) : 0;
+        if (kv_ptr) {
+            // entry pos of head (b, h)'s KV-owned list
+            const long long bh = (long long)b * p.Hq + h;
+            const long long pos = x - bh * p.nQ * cap;
+            const int *ptr = kv_ptr + bh * (p.nKV + 1);
+            int bits = 0;
+            if (pos < ptr[p.nKV]) {
+                int lo = 0, hi = p.nKV;  // largest j with ptr[j] <= pos
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (ptr[mid] <= pos) lo = mid; else hi = mid;
+                }
+                bits = tile_bits(p, bm, nQb, bq, b, h, kv_qidx[bh * p.nQ * cap + pos], lo);
+            }
+            kv_qsub[x] = bits;
+        }
+    }
+}
+
+int grid_for(long long n) {
+    const long long g = (n + 255) / 256;
+    return (int)(g < 1 ? 1 : (g > 65535 ? 65535 : g));
+}
+
+}  // namespace
+
+cudaError_t launch_block_index(const Prob &p, int bq, int nQb, const uint8_t *bm, uint8_t *tmap, int *q_idx,
+                               int *q_cnt, int *q_sub, int cap, int *kv_ptr, int *kv_qidx, int *kv_qsub,
+                               cudaStream_t s) {
+    prof_begin("block_union", s);
+    k_block_union<<<grid_for((long long)p.B * p.Hq * p.nQ * p.nKV), 256, 0, s>>>(p, bq, nQb, bm, tmap);
+    prof_end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if ((e = launch_mask_index(p, tmap, q_idx, q_cnt, cap, s)) != cudaSuccess) return e;
+    if (kv_ptr && (e = launch_transpose(p, tmap, kv_ptr, kv_qidx, cap, s)) != cudaSuccess) return e;
+    prof_begin("block_bits", s);
+    k_block_bits<<<grid_for((long long)p.B * p.Hq * p.nQ * cap), 256, 0, s>>>(p, bq, nQb, bm, q_idx, q_cnt, cap, q_sub,
+                                                                            kv_ptr, kv_qidx, kv_qsub);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
 }  // namespace vsa

@@ -257,10 +257,11 @@ vsa_status vsa_mask_to_index(const vsa_desc *desc, const uint8_t *block_map, con
     return VSA_OK;
 }
 
-vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const void *v, const int32_t *q_idx,
-                   const int32_t *q_cnt, int idx_cap, const int32_t *q_var, const int32_t *kv_var,
-                   const void *gate, void *out, float *lse, void *o_sparse, void *workspace,
-                   size_t workspace_bytes, vsa_stream_t stream) {
+namespace {
+vsa_status fwd_impl(const vsa_desc *desc, const void *q, const void *k, const void *v, const int32_t *q_idx,
+                    const int32_t *q_cnt, const int32_t *q_sub, int block_q, int idx_cap, const int32_t *q_var,
+                    const int32_t *kv_var, const void *gate, void *out, float *lse, void *o_sparse,
+                    void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
     VSA_TRY(need_vars(p0, q_var, kv_var, &p, gate != nullptr));
@@ -285,6 +286,8 @@ vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const voi
     a.o_sparse = o_sparse ? o_sparse : out;
     a.lse = lse;
     a.gate = gate;
+    a.q_sub = q_sub;
+    a.block_q = block_q;
     a.err = at<unsigned>(workspace, 0);
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
@@ -296,6 +299,26 @@ vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const voi
     }
     VSA_CUDA(launch_fwd(p, a, s));
     return VSA_OK;
+}
+}  // namespace
+
+vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const void *v, const int32_t *q_idx,
+                   const int32_t *q_cnt, int idx_cap, const int32_t *q_var, const int32_t *kv_var,
+                   const void *gate, void *out, float *lse, void *o_sparse, void *workspace,
+                   size_t workspace_bytes, vsa_stream_t stream) {
+    return fwd_impl(desc, q, k, v, q_idx, q_cnt, nullptr, 0, idx_cap, q_var, kv_var, gate, out, lse, o_sparse,
+                    workspace, workspace_bytes, stream);
+}
+
+vsa_status vsa_fwd_blocks(const vsa_desc *desc, int block_q, const void *q, const void *k, const void *v,
+                          const int32_t *q_idx, const int32_t *q_cnt, const int32_t *q_sub, int idx_cap,
+                          const int32_t *q_var, const int32_t *kv_var, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vsa_stream_t stream) {
+    if (!desc || !q_sub) return VSA_ERR_NULL;
+    if (block_q < 32 || block_q > desc->tile_q || desc->tile_q % block_q != 0 || block_q % 32 != 0)
+        return VSA_ERR_SHAPE;
+    return fwd_impl(desc, q, k, v, q_idx, q_cnt, q_sub, block_q, idx_cap, q_var, kv_var, nullptr, out, lse,
+                    nullptr, workspace, workspace_bytes, stream);
 }
 
 vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
@@ -320,11 +343,12 @@ vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, co
     return VSA_OK;
 }
 
-vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
-                   const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
-                   const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var, const int32_t *kv_var,
-                   const void *gate, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
-                   vsa_stream_t stream) {
+namespace {
+vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                    const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt,
+                    const int32_t *q_sub, int block_q, int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx,
+                    const int32_t *kv_qsub, const int32_t *q_var, const int32_t *kv_var, const void *gate,
+                    void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
     VSA_TRY(need_vars(p0, q_var, kv_var, &p));
@@ -352,6 +376,9 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
+    a.q_sub = q_sub;
+    a.kv_qsub = kv_qsub;
+    a.block_q = block_q;
     a.err = at<unsigned>(workspace, 0);
     float *ndvec = at<float>(workspace, L.ndvec), *nlse2 = at<float>(workspace, L.nlse2);
     a.ndvec = ndvec;
@@ -372,6 +399,48 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
     }
     VSA_CUDA(launch_bwd_dkdv(p, a, s));
     VSA_CUDA(launch_bwd_dq(p, a, s));
+    return VSA_OK;
+}
+}  // namespace
+
+vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                   const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
+                   const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var, const int32_t *kv_var,
+                   const void *gate, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                   vsa_stream_t stream) {
+    return bwd_impl(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, nullptr, 0, idx_cap, kv_ptr, kv_qidx, nullptr,
+                    q_var, kv_var, gate, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+vsa_status vsa_bwd_blocks(const vsa_desc *desc, int block_q, const void *dO, const void *q, const void *k,
+                          const void *v, const void *out, const float *lse, const int32_t *q_idx,
+                          const int32_t *q_cnt, const int32_t *q_sub, int idx_cap, const int32_t *kv_ptr,
+                          const int32_t *kv_qidx, const int32_t *kv_qsub, const int32_t *q_var,
+                          const int32_t *kv_var, void *dq, void *dk, void *dv, void *workspace,
+                          size_t workspace_bytes, vsa_stream_t stream) {
+    if (!desc || !q_sub || !kv_qsub) return VSA_ERR_NULL;
+    if (block_q < 32 || block_q > desc->tile_q || desc->tile_q % block_q != 0 || block_q % 32 != 0)
+        return VSA_ERR_SHAPE;
+    return bwd_impl(desc, dO, q, k, v, out, lse, q_idx, q_cnt, q_sub, block_q, idx_cap, kv_ptr, kv_qidx, kv_qsub,
+                    q_var, kv_var, nullptr, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+vsa_status vsa_mask_to_index_blocks(const vsa_desc *desc, int block_q, int nQb, const uint8_t *block_mask,
+                                    const int32_t *q_var, const int32_t *kv_var, int need_bwd_index,
+                                    uint8_t *tile_map, int32_t *q_idx, int32_t *q_cnt, int32_t *q_sub, int idx_cap,
+                                    int32_t *kv_ptr, int32_t *kv_qidx, int32_t *kv_qsub, vsa_stream_t stream) {
+    Prob p0, p;
+    VSA_TRY(to_prob(desc, &p0));
+    VSA_TRY(need_vars(p0, q_var, kv_var, &p, false));
+    if (!block_mask || !tile_map || !q_idx || !q_cnt || !q_sub) return VSA_ERR_NULL;
+    if (need_bwd_index && (!kv_ptr || !kv_qidx || !kv_qsub)) return VSA_ERR_NULL;
+    if (block_q < 32 || block_q > p.tile_q || p.tile_q % block_q != 0 || block_q % 32 != 0) return VSA_ERR_SHAPE;
+    if (nQb < 1 || nQb > p.nQ * (p.tile_q / block_q)) return VSA_ERR_SHAPE;
+    if (idx_cap < p.nKV) return VSA_ERR_SHAPE;
+    if (p.nKV > 16000) return VSA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    VSA_CUDA(launch_block_index(p, block_q, nQb, block_mask, tile_map, q_idx, q_cnt, q_sub, idx_cap,
+                                need_bwd_index ? kv_ptr : nullptr, kv_qidx, kv_qsub, s));
     return VSA_OK;
 }
 

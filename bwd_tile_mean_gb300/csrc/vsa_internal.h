@@ -26,6 +26,12 @@ cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int t
 // Caller-given block map -> Q-owned index.
 cudaError_t launch_mask_index(const Prob &p, const uint8_t *map, int *q_idx, int *q_cnt, int cap,
                               cudaStream_t s);
+// Query-block mask [B, Hq, nQb, nKV] (block_q rows per block) -> tile map
+// (union over each tile's blocks), Q-owned index with per-entry block bit
+// masks, and (kv_ptr != NULL) the KV-owned index with its bit masks.
+cudaError_t launch_block_index(const Prob &p, int bq, int nQb, const uint8_t *bm, uint8_t *tmap, int *q_idx,
+                               int *q_cnt, int *q_sub, int cap, int *kv_ptr, int *kv_qidx, int *kv_qsub,
+                               cudaStream_t s);
 // Block map -> KV-owned index.
 cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int *kv_qidx, int cap,
                              cudaStream_t s);
@@ -44,6 +50,8 @@ struct FwdArgs {
     float *lse;
     const void *gate;   // NULL: no compression
     const float *c;     // [B, Hq, nQ, D] compression output (gate != NULL)
+    const int *q_sub;   // per-entry query-block bit masks (NULL: whole tiles)
+    int block_q;        // rows per query block when q_sub != NULL
     unsigned *err;
 };
 cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s);
@@ -70,6 +78,8 @@ struct BwdArgs {
     const int *kv_ptr, *kv_qidx;
     void *dq, *dk, *dv;
     const float *dpq, *dpk, *dpv;   // compression gradients (NULL without a gate)
+    const int *q_sub, *kv_qsub;     // query-block bit masks of both indices (NULL: whole tiles)
+    int block_q;
     unsigned *err;
 };
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s);

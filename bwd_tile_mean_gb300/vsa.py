@@ -30,7 +30,8 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_fwd", "vsa_bwd",
            "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
-           "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad")
+           "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
+           "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks")
 
 
 class VsaError(RuntimeError):
@@ -92,6 +93,15 @@ def lib():
         L.vsa_profile_ms.restype = C.c_float
         L.vsa_profile_ms.argtypes = [C.c_int]
         L.vsa_launch_count.restype = C.c_longlong
+        L.vsa_mask_to_index_blocks.restype = C.c_int
+        L.vsa_mask_to_index_blocks.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, P, P, P, C.c_int, P, P, P, P,
+                                               C.c_int, P, P, P, P]
+        L.vsa_fwd_blocks.restype = C.c_int
+        L.vsa_fwd_blocks.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, P, P,
+                                     C.c_size_t, P]
+        L.vsa_bwd_blocks.restype = C.c_int
+        L.vsa_bwd_blocks.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, P, P, P, C.c_int, P, P, P, P,
+                                     P, P, P, P, P, C.c_size_t, P]
         L.vsa_gate_grad.restype = C.c_int
         L.vsa_gate_grad.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.vsa_tile_3d_count.restype = C.c_int
@@ -261,6 +271,41 @@ class Plan:
         dv = torch.empty_like(v) if dv is None else dv
         vsa_bwd(self.desc, dO, q, k, v, o_sparse, lse, self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr,
                 self.kv_qidx, self.q_var, self.kv_var, gate, dq, dk, dv, self.workspace, stream)
+        return dq, dk, dv
+
+    def mask_to_index_blocks(self, block_q, block_mask, need_bwd_index=True, stream=None):
+        """Index from a query-block mask [B, Hq, nQb, nKV] (block_q rows per
+        block); keeps the per-entry block bits for forward_blocks /
+        backward_blocks."""
+        self.block_q = block_q
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.q_sub = torch.empty_like(self.q_idx)
+        self.kv_qsub = torch.empty_like(self.kv_qidx)
+        _check("vsa_mask_to_index_blocks", lib().vsa_mask_to_index_blocks(
+            C.byref(self.desc), int(block_q), int(block_mask.shape[2]), _p(block_mask), _p(self.q_var),
+            _p(self.kv_var), int(bool(need_bwd_index)), _p(self.block_map), _p(self.q_idx), _p(self.q_cnt),
+            _p(self.q_sub), int(self.idx_cap), _p(self.kv_ptr if need_bwd_index else None),
+            _p(self.kv_qidx if need_bwd_index else None), _p(self.kv_qsub if need_bwd_index else None),
+            _stream(stream)))
+
+    def forward_blocks(self, q, k, v, out=None, lse=None, stream=None):
+        out = torch.empty_like(q) if out is None else out
+        lse = torch.empty(self.lse_shape(), dtype=torch.float32, device=q.device) if lse is None else lse
+        _check("vsa_fwd_blocks", lib().vsa_fwd_blocks(
+            C.byref(self.desc), int(self.block_q), _p(q), _p(k), _p(v), _p(self.q_idx), _p(self.q_cnt),
+            _p(self.q_sub), int(self.idx_cap), _p(self.q_var), _p(self.kv_var), _p(out), _p(lse),
+            _p(self.workspace), self.workspace.numel() * self.workspace.element_size(), _stream(stream)))
+        return out, lse
+
+    def backward_blocks(self, dO, q, k, v, out, lse, dq=None, dk=None, dv=None, stream=None):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        _check("vsa_bwd_blocks", lib().vsa_bwd_blocks(
+            C.byref(self.desc), int(self.block_q), _p(dO), _p(q), _p(k), _p(v), _p(out), _p(lse), _p(self.q_idx),
+            _p(self.q_cnt), _p(self.q_sub), int(self.idx_cap), _p(self.kv_ptr), _p(self.kv_qidx), _p(self.kv_qsub),
+            _p(self.q_var), _p(self.kv_var), _p(dq), _p(dk), _p(dv), _p(self.workspace),
+            self.workspace.numel() * self.workspace.element_size(), _stream(stream)))
         return dq, dk, dv
 
     def gate_grad(self, dO, q, k, v, dgate=None, stream=None):

@@ -197,6 +197,38 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    size_t workspace_bytes, vsa_stream_t stream);
 
 /* Human-readable name of a status. */
+/* Query blocks smaller than a tile ([NPU-test]: block_shape [32, 128] and
+ * [64, 128] with an explicit block_sparse_mask): a caller's mask
+ * block_mask [B, Hq, nQb, nKV] uint8 (nonzero = attend) whose rows are
+ * query blocks of block_q rows (block_q a multiple of 32 dividing tile_q;
+ * nQb <= nQ * tile_q / block_q; TND: per sequence, ceil(max_len /
+ * block_q) blocks, blocks past a sequence's end ignored) and whose columns
+ * are the KV tiles. The kernels keep tiles of tile_q query rows: a tile's
+ * index lists the union of its blocks' selections, and q_sub [B, Hq, nQ,
+ * idx_cap] int32 (bit s set iff block s of the tile selected the entry's
+ * KV tile) and kv_qsub [B, Hq, nQ*idx_cap] (the same bits for the KV-owned
+ * entries) mask the keys of the other blocks' rows. Outputs as for
+ * vsa_mask_to_index plus tile_map [B, Hq, nQ, nKV] uint8 (the union map).
+ * A row whose block selects nothing gets O = 0, LSE = -inf and no
+ * gradient. vsa_fwd_blocks / vsa_bwd_blocks are vsa_fwd / vsa_bwd (no
+ * compression branch) with these masks; block_q must equal the one the
+ * index was built with. */
+vsa_status vsa_mask_to_index_blocks(const vsa_desc *desc, int block_q, int nQb, const uint8_t *block_mask,
+                                    const int32_t *q_var, const int32_t *kv_var, int need_bwd_index,
+                                    uint8_t *tile_map, int32_t *q_idx, int32_t *q_cnt, int32_t *q_sub,
+                                    int idx_cap, int32_t *kv_ptr, int32_t *kv_qidx, int32_t *kv_qsub,
+                                    vsa_stream_t stream);
+vsa_status vsa_fwd_blocks(const vsa_desc *desc, int block_q, const void *q, const void *k, const void *v,
+                          const int32_t *q_idx, const int32_t *q_cnt, const int32_t *q_sub, int idx_cap,
+                          const int32_t *q_var, const int32_t *kv_var, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vsa_stream_t stream);
+vsa_status vsa_bwd_blocks(const vsa_desc *desc, int block_q, const void *dO, const void *q, const void *k,
+                          const void *v, const void *out, const float *lse, const int32_t *q_idx,
+                          const int32_t *q_cnt, const int32_t *q_sub, int idx_cap, const int32_t *kv_ptr,
+                          const int32_t *kv_qidx, const int32_t *kv_qsub, const int32_t *q_var,
+                          const int32_t *kv_var, void *dq, void *dk, void *dv, void *workspace,
+                          size_t workspace_bytes, vsa_stream_t stream);
+
 /* Gradient of the compression gate (the pages' gate carries no gradient:
  * [VSA-test] builds it without requires_grad). With out = O + gate (*) c
  * (vsa_fwd, gated), dgate_t = dO_t (*) c_i for every slot t of query tile
