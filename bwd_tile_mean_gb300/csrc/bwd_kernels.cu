@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     uint8_t *sQ = sm + kDqOffQ, *sO = sm + kDqOffO, *sK = sm + kDqOffK, *sV = sm + kDqOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kDqOffCtl);
-    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7;
+    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_ke = bars + 4, *b_vf = bars + 7, *b_ve = bars + 9;
     // b_sf / b_sfree: [0] for S, [1] for dP (each computed, then read, on its own)
     uint64_t *b_sf = bars + 11, *b_sfree = bars + 13, *b_dsf = bars + 15, *b_dq = bars + 17;
     uint64_t *b_fin = bars + 19;  // one per MMA warp
@@ -595,6 +595,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         for (int s = 0; s < kDqVStages; ++s) {
             mbar_init(b_vf + s, 1);
+            mbar_init(b_ve + s, 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(b_dq + s, 1);
         for (int s = 0; s < 2; ++s) {
@@ -646,7 +647,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const int kr = kvb + crow;
             // V first: its stage frees when dP(c-2) completes, which precedes
             // dQ(c-3), the MMA that frees K's stage
-            if (c >= kDqVStages && !mbar_wait_warp(b_sf + 1, c & 1, s_abort, a.err, kSiteDqProd))  // dP(c-2) done
+            if (c >= kDqVStages &&
+                !mbar_wait_warp(b_ve + sv, ((c / kDqVStages) - 1) & 1, s_abort, a.err, kSiteDqProd))
                 break;
             if (lane == 0) {
                 mbar_expect_tx(b_vf + sv, kTile);
@@ -682,6 +684,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             issue_ss(tD, aA, aB + sx * kTile, idS);  // S = Q K^T | dP = dO V^T
             mma_commit_w(b_sf + isP);
+            if (isP) mma_commit_w(b_ve + sx);  // V_c free once dP(c) is done
             mma_started = 1;
         }
     } else if (warp == kDqMmaWarp && N > 0) {

@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     uint8_t *sQ = sm + kOffQ, *sK = sm + kOffK, *sV = sm + kOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffCtl);
-    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_vf = bars + 3, *b_sf = bars + 7;
-    uint64_t *b_pf = bars + 9, *b_od = bars + 11, *b_fin = bars + 13;
+    uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_vf = bars + 3, *b_ke = bars + 5, *b_sf = bars + 7;
+    uint64_t *b_pf = bars + 9, *b_od = bars + 11, *b_fin = bars + 13, *b_ve = bars + 14;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 16);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(b_sf + s, 1);
             mbar_init(b_pf + s, 128);
             mbar_init(b_od + s, 1);
+            mbar_init(b_ke + s, 1);
+            mbar_init(b_ve + s, 1);
         }
         mbar_init(b_fin, 1);
         *s_abort = 0;
@@ -173,7 +175,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int issued_q = 0, issued_k[2] = {0, 0}, issued_v[2] = {0, 0}, mma_started = 0;
 
     if (warp == kFwdProdWarp && lane == 0 && N > 0) {
-        const int glast = has_b ? 1 : 0;
         // ---------------------------------------------------- TMA producer
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
@@ -186,16 +187,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         issued_q = 1;
         for (int c = 0; c < N; ++c) {
             const int s = c & 1;
-            // K(c-2) is free once the last group's S(c-2) is done, V(c-2) once
-            // that group's S(c-1) is: the MMAs complete in issue order and
-            // both groups' O += P V(c-2) were issued before it
-            if (c >= 2 && !mbar_wait(b_sf + glast, c & 1, s_abort, a.err, kSiteProd)) break;
+            // stage s is free once the MMAs reading K(c-2) / V(c-2) are done;
+            // each release barrier completes once per use of its stage, so
+            // the producer can never be two phases behind it
+            if (c >= 2 && !mbar_wait(b_ke + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteProd)) break;
             const int kr = kvb + s_crow[c];
             mbar_expect_tx(b_kf + s, kTile);
             tma_load_4d(sK + s * kTile, &tk, b_kf + s, 0, kr, hk, bc);
             tma_load_4d(sK + s * kTile + kBox, &tk, b_kf + s, 64, kr, hk, bc);
             issued_k[s]++;
-            if (c >= 2 && !mbar_wait(b_sf + glast, (c - 1) & 1, s_abort, a.err, kSiteProd)) break;
+            if (c >= 2 && !mbar_wait(b_ve + s, ((c >> 1) - 1) & 1, s_abort, a.err, kSiteProd)) break;
             mbar_expect_tx(b_vf + s, kTile);
             tma_load_4d(sV + s * kTile, &tv, b_vf + s, 0, kr, hk, bc);
             tma_load_4d(sV + s * kTile + kBox, &tv, b_vf + s, 64, kr, hk, bc);
@@ -220,15 +221,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (!(ok = mbar_wait_warp(b_pf + 1, (c - 1) & 1, s_abort, a.err, kSiteMma))) break;
                     tc_fence_after();
                     issue_pv(tO[1], tS[1], aV + sp * kTile, idO, c - 1 > 0);  // O_B += P_B(c-1) V_(c-1)
+                    mma_commit_w(b_ve + sp);  // V_(c-1) read by both groups
                 }
                 issue_qk(tS[1], aQ + kTile, aK + s * kTile, idS);  // S_B(c)
                 mma_commit_w(b_sf + 1);
             }
+            mma_commit_w(b_ke + s);  // K_c is read by the S MMAs only
             if (!(ok = mbar_wait_warp(b_pf + 0, c & 1, s_abort, a.err, kSiteMma))) break;
             if (!(ok = mbar_wait_warp(b_vf + s, (c >> 1) & 1, s_abort, a.err, kSiteMma))) break;
             tc_fence_after();
             issue_pv(tO[0], tS[0], aV + s * kTile, idO, c > 0);  // O_A += P_A(c) V_c
             if (c == N - 1) mma_commit_w(b_od + 0);  // O_A final (S_A(c+1) would signal it otherwise)
+            if (!has_b) mma_commit_w(b_ve + s);
         }
         if (ok && has_b) {
             const int sp = (N - 1) & 1;
@@ -236,6 +240,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_after();
                 issue_pv(tO[1], tS[1], aV + sp * kTile, idO, N - 1 > 0);
                 mma_commit_w(b_od + 1);
+                mma_commit_w(b_ve + sp);
             }
         }
     } else if (warp < 8 && (warp < 4 || has_b)) {
