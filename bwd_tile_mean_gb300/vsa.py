@@ -31,7 +31,7 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
-           "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks")
+           "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout")
 
 
 class VsaError(RuntimeError):
@@ -93,6 +93,8 @@ def lib():
         L.vsa_profile_ms.restype = C.c_float
         L.vsa_profile_ms.argtypes = [C.c_int]
         L.vsa_launch_count.restype = C.c_longlong
+        L.vsa_check_wait_timeout.restype = C.c_int
+        L.vsa_check_wait_timeout.argtypes = [P, C.c_ulonglong, P, P]
         L.vsa_mask_to_index_blocks.restype = C.c_int
         L.vsa_mask_to_index_blocks.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, P, P, P, C.c_int, P, P, P, P,
                                                C.c_int, P, P, P, P]
@@ -360,3 +362,12 @@ def untile_3d(tiled: torch.Tensor, grid, tile=(4, 8, 8), out=None, stream=None):
     _check("vsa_untile_3d", lib().vsa_untile_3d(B, T, H, W, row_bytes, *tile, _p(tiled), _p(out),
                                                 _stream(stream)))
     return out
+
+
+def check_wait_timeout(workspace: torch.Tensor, limit_ns: int = 50_000_000, stream=None) -> int:
+    """Run the bounded-wait failure check; returns the device's completed flag
+    (0: the wait timed out as it should)."""
+    done = torch.full((1,), -1, dtype=torch.int32, device=workspace.device)
+    _check("vsa_check_wait_timeout", lib().vsa_check_wait_timeout(_p(workspace), int(limit_ns), _p(done),
+                                                                    _stream(stream)))
+    return int(done.item())

@@ -197,6 +197,18 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    size_t workspace_bytes, vsa_stream_t stream);
 
 /* Human-readable name of a status. */
+/* Failure-path check: launches one warp that waits, with the library's
+ * bounded mbarrier wait, on a barrier that nothing ever arrives on. After
+ * limit_ns of wall time (0 < limit_ns <= 10 s) the wait gives up, records
+ * its site code (0x7E57) in workspace's status word -- read and cleared by
+ * vsa_device_status, exactly as a timed-out wait inside an attention
+ * kernel -- and the kernel returns; the context stays usable. *completed
+ * (device int32) receives 0 (timed out) or 1 (the wait returned as if the
+ * phase had completed, a library defect). workspace: 256-byte aligned, at
+ * least 256 bytes. */
+vsa_status vsa_check_wait_timeout(void *workspace, unsigned long long limit_ns, int32_t *completed,
+                                  vsa_stream_t stream);
+
 /* Query blocks smaller than a tile ([NPU-test]: block_shape [32, 128] and
  * [64, 128] with an explicit block_sparse_mask): a caller's mask
  * block_mask [B, Hq, nQb, nKV] uint8 (nonzero = attend) whose rows are
