@@ -35,9 +35,9 @@ METRIC = "fwd+bwd effective TFLOP/s (selected blocks) on 1 GB300; % of bf16 TC p
 # the traffic of a launch scales with the heads. Set an entry to None when its
 # kernel changes after the capture.
 DRAM_BYTES_PER_4_HEADS = {
-    "bwd_dkdv": None,  # changed after the capture
-    "bwd_dq": None,  # changed after the capture
-    "fwd_attn": None,  # changed after the capture
+    "bwd_dkdv": 397.200128e6 + 141.905152e6,
+    "bwd_dq": 406.098432e6 + 73.191424e6,
+    "fwd_attn": 306.897408e6 + 67.292672e6,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
