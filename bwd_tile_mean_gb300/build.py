@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libvsa.so")
-SOURCES = ["vsa_api.cu", "index_kernels.cu", "fwd_kernel.cu", "bwd_kernels.cu", "noalloc.cu", "tile3d.cu", "waitcheck.cu"]
+SOURCES = ["vsa_api.cu", "index_kernels.cu", "fwd_kernel.cu", "bwd_kernels.cu", "noalloc.cu", "tile3d.cu", "waitcheck.cu",
+           "host_step.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]

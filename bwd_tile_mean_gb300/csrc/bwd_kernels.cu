@@ -9,9 +9,11 @@
 // saved LSE with softmax_scale = D^-0.5).
 //
 // rowsum(P dP) equals Dvec = rowsum(dO * O), computed once per query row
-// by k_dvec. The KV-owned pass k_dkdv and the Q-owned pass k_dq each
+// by k_bwd_prep. The KV-owned pass k_dkdv and the Q-owned pass k_dq each
 // recompute S and dP on the tensor core, so neither needs atomics and every
 // output element is written by exactly one CTA.
+#include <climits>
+
 #include "sm103_ptx.cuh"
 #include "vsa_internal.h"
 
@@ -40,39 +42,53 @@ constexpr int kProdWarp = 8, kMmaWarp = 9;
 // rowsum(P dP) of the softmax backward); both are stored negated so the
 // consumers add them. Slots that are not query rows (past a varlen
 // sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there. A half-warp
-// reads one 256-byte row (16 bytes per lane); each warp keeps four row
-// pairs in flight.
+// reads one 256-byte row (16 bytes per lane); a warp takes 8 rows, all
+// loads issued before the first use. Rows are visited in memory order of dO
+// and O (the heads of a token are adjacent in BSHD and TND, the tokens of a
+// head in BHSD), so consecutive warps stream contiguous memory. Row indices
+// fit in 32 bits (the host checks), which keeps the index arithmetic short.
+constexpr int kPrepIt = 4;  // row pairs per warp
+
+// Batch entry, token and head of the prep row with memory-order index w.
+__device__ __forceinline__ void prep_row(const Prob &p, int per, int w, int &b, int &s, int &h) {
+    const int bs = per * p.Hq;
+    b = w / bs;
+    const int rem = w - b * bs;
+    if (p.layout == L_BHSD) {
+        h = rem / per;
+        s = rem - h * per;
+    } else {
+        s = rem / p.Hq;
+        h = rem - s * p.Hq;
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
                                                   const float *__restrict__ lse, float *__restrict__ nlse2,
                                                   float *__restrict__ ndvec) {
     const int per = p.nQ * p.tile_q;
-    const long long slots = (long long)p.B * p.Hq * per;
+    const int slots = p.B * p.Hq * per;
     const int half = (threadIdx.x >> 4) & 1, hl = threadIdx.x & 15;
-    const long long wbase = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * 8;
-    uint4 av[4], cv[4];
-    bool ex[4];
-    long long lo[4];
+    const int wbase = (blockIdx.x * 8 + (threadIdx.x >> 5)) * (2 * kPrepIt);
+    uint4 av[kPrepIt], cv[kPrepIt];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const long long w = wbase + it * 2 + half;
-        ex[it] = false;
-        lo[it] = -1;
+    for (int it = 0; it < kPrepIt; ++it) {
+        const int w = wbase + it * 2 + half;
         av[it] = make_uint4(0, 0, 0, 0);
         cv[it] = make_uint4(0, 0, 0, 0);
         if (w < slots) {
-            const int s = (int)(w % per), h = (int)((w / per) % p.Hq), b = (int)(w / ((long long)per * p.Hq));
-            ex[it] = p.layout == L_TND ? (s < p.cu_q[b + 1] - p.cu_q[b]) : true;
-            if (ex[it]) {
+            int b, s, h;
+            prep_row(p, per, w, b, s, h);
+            if (p.layout != L_TND || s < p.cu_q[b + 1] - p.cu_q[b]) {
                 const long long o = tok_off(p, true, b, s, h) + hl * 8;
                 av[it] = __ldg(reinterpret_cast<const uint4 *>(dO + o));
                 cv[it] = __ldg(reinterpret_cast<const uint4 *>(O + o));
-                lo[it] = lse_off(p, b, h, s);
             }
         }
     }
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    for (int it = 0; it < kPrepIt; ++it) {
         const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
         const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
         float acc = 0.f;
@@ -84,11 +100,15 @@ __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ 
         }
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        const long long w = wbase + it * 2 + half;
+        const int w = wbase + it * 2 + half;
         if (hl == 0 && w < slots) {
-            ndvec[w] = ex[it] ? -acc : 0.f;
-            const float lv = ex[it] ? lse[lo[it]] : -INFINITY;
-            nlse2[w] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
+            int b, s, h;
+            prep_row(p, per, w, b, s, h);
+            const bool ex = p.layout != L_TND || s < p.cu_q[b + 1] - p.cu_q[b];
+            const long long slot = ((long long)b * p.Hq + h) * per + s;
+            ndvec[slot] = ex ? -acc : 0.f;
+            const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
+            nlse2[slot] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
         }
     }
 }
@@ -1009,7 +1029,8 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
                             float *ndvec, cudaStream_t s) {
     const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;
     if (slots == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((slots + 63) / 64);
+    if (slots > (long long)INT_MAX - 2 * 8 * 2 * kPrepIt) return cudaErrorInvalidValue;
+    const unsigned blocks = (unsigned)((slots + 8 * 2 * kPrepIt - 1) / (8 * 2 * kPrepIt));
     prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
         k_bwd_prep<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)o,

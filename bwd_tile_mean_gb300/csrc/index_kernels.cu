@@ -78,106 +78,166 @@ cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, c
 }
 
 // ---------------------------------------------------------------- select
-// Block = 8 warps = 8 query tiles of one (b, h). Key-tile means are staged
-// through shared memory in chunks of 128 tiles (rows padded to 129 floats so
-// lanes reading different tiles at the same d hit different banks). Lane l
-// of warp w computes the scores of tiles l, l+32, ... of query tile
-// i0 + w; the warp then takes the top-k by repeated warp-wide argmax under
-// (score desc, index asc).
-constexpr int kSelRows = 8;
+// Block = 8 warps = 8 * RPW query tiles of one (b, h); warp w owns query
+// tiles i0 + w * RPW .. + RPW - 1. Key-tile means are staged through shared
+// memory in chunks of 128 tiles with 16-byte copies (rows padded to 132
+// floats, so the 16-byte reads of eight lanes at a time hit distinct bank
+// groups). Lane l computes the scores of tiles l, l+32, l+64, l+96 of a
+// chunk for the warp's RPW query tiles; every score is one __fmaf_rn chain
+// over ascending d, as in the fixed-order definition.
+//
+// Top-k: scores map to order-preserving 32-bit keys (-0 folded into +0, so
+// equal scores give equal keys); a 32-step bitwise search finds the k-th
+// largest key T (the largest T with at least k keys >= T). The selection is
+// every key > T plus the lowest-indexed keys == T up to k, which is the
+// repeated-argmax rule with ties to the lower tile index.
 constexpr int kSelChunk = 128;
+constexpr int kSelPitch = 132;
 
-__device__ __forceinline__ bool sel_better(float v, int j, float bv, int bj) {
-    return j != INT_MAX && (bj == INT_MAX || v > bv || (v == bv && j < bj));
+__device__ __forceinline__ uint32_t score_key(float x) {
+    if (x == 0.f) x = 0.f;
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+template <int RPW>
 __global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict__ pq,
                                                 const float *__restrict__ pk, int topk, uint8_t *map,
                                                 int *q_idx, int *q_cnt, int cap) {
-    extern __shared__ float sm[];
-    float *spk = sm;                                  // [kSelChunk][129]
-    float *spq = spk + kSelChunk * 129;               // [kSelRows][128]
-    float *ssc = spq + kSelRows * 128;                // [kSelRows][nKV]
-    uint8_t *ssel = reinterpret_cast<uint8_t *>(ssc + kSelRows * p.nKV);  // [kSelRows][nKV]
+    constexpr int R = 8 * RPW;
+    extern __shared__ __align__(16) float sm[];
+    float *spk = sm;                                  // [kSelChunk][kSelPitch]
+    float *spq = spk + kSelChunk * kSelPitch;         // [R][128]
+    float *ssc = spq + R * 128;                       // [R][nKV]
     const int b = blockIdx.z, h = blockIdx.y, hk = h / (p.Hq / p.Hkv);
-    const int i0 = blockIdx.x * kSelRows, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = i0 + w;
-    const int D = p.D;  // 128
-    for (int e = threadIdx.x; e < kSelRows * D; e += blockDim.x) {
-        int r = e / D, ii = i0 + r;
-        spq[e] = ii < p.nQ ? pq[(((long long)b * p.Hq + h) * p.nQ + ii) * D + (e % D)] : 0.f;
+    const int i0 = blockIdx.x * R, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = 128;
+    for (int e = threadIdx.x; e < R * D / 4; e += blockDim.x) {
+        const int r = e / (D / 4), ii = i0 + r;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ii < p.nQ) v = __ldg(reinterpret_cast<const float4 *>(pq + (((long long)b * p.Hq + h) * p.nQ + ii) * D) + (e % (D / 4)));
+        reinterpret_cast<float4 *>(spq)[e] = v;
     }
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * D;
     for (int j0 = 0; j0 < p.nKV; j0 += kSelChunk) {
         const int nj = min(kSelChunk, p.nKV - j0);
         __syncthreads();
-        for (int e = threadIdx.x; e < nj * D; e += blockDim.x)
-            spk[(e / D) * 129 + (e % D)] = pkh[(long long)j0 * D + e];
-        __syncthreads();
-        if (i < p.nQ) {
-            for (int jj = lane; jj < nj; jj += 32) {
-                float acc = 0.f;
-                const float *a = spq + w * D, *c = spk + jj * 129;
-#pragma unroll 16
-                for (int e = 0; e < D; ++e) acc = __fmaf_rn(a[e], c[e], acc);
-                ssc[w * p.nKV + j0 + jj] = kv_valid(p, b, j0 + jj) > 0 ? acc : -INFINITY;
-            }
-        }
-    }
-    __syncthreads();
-    if (i >= p.nQ) return;
-    const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
-    float *sc = ssc + w * p.nKV;
-    uint8_t *sel = ssel + w * p.nKV;
-    for (int j = lane; j < p.nKV; j += 32) sel[j] = 0;
-    __syncwarp();
-    const int k = q_rows(p, b, i) > 0 ? min(topk, p.nKV) : 0;
-    for (int n = 0; n < k; ++n) {
-        float bv = -INFINITY;
-        int bj = INT_MAX;
-        for (int j = lane; j < p.nKV; j += 32)
-            if (!sel[j] && sel_better(sc[j], j, bv, bj)) {
-                bv = sc[j];
-                bj = j;
+        {
+            float4 buf[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int e = threadIdx.x + u * 256;  // 4096 16-byte words per full chunk
+                buf[u] = e < nj * (D / 4) ? __ldg(reinterpret_cast<const float4 *>(pkh + (long long)j0 * D) + e)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oj = __shfl_xor_sync(0xffffffffu, bj, off);
-            if (sel_better(ov, oj, bv, bj)) {
-                bv = ov;
-                bj = oj;
+            for (int u = 0; u < 16; ++u) {
+                const int e = threadIdx.x + u * 256;
+                if (e < nj * (D / 4))
+                    *reinterpret_cast<float4 *>(spk + (e / (D / 4)) * kSelPitch + (e % (D / 4)) * 4) = buf[u];
             }
         }
-        if (lane == 0) sel[bj] = 1;
-        __syncwarp();
+        __syncthreads();
+        float acc[RPW][4];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[r][u] = 0.f;
+        const float *aq = spq + (w * RPW) * D;
+#pragma unroll 2
+        for (int e = 0; e < D; e += 4) {
+            float4 c4[4], a4[RPW];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                c4[u] = *reinterpret_cast<const float4 *>(spk + (lane + 32 * u) * kSelPitch + e);
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) a4[r] = *reinterpret_cast<const float4 *>(aq + r * D + e);
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc[r][u] = __fmaf_rn(a4[r].x, c4[u].x, acc[r][u]);
+                    acc[r][u] = __fmaf_rn(a4[r].y, c4[u].y, acc[r][u]);
+                    acc[r][u] = __fmaf_rn(a4[r].z, c4[u].z, acc[r][u]);
+                    acc[r][u] = __fmaf_rn(a4[r].w, c4[u].w, acc[r][u]);
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int jj = lane + 32 * u;
+            if (jj < nj) {
+                const bool valid = kv_valid(p, b, j0 + jj) > 0;
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) ssc[(w * RPW + r) * p.nKV + j0 + jj] = valid ? acc[r][u] : -INFINITY;
+            }
+        }
     }
-    int cnt = 0;
-    for (int j0 = 0; j0 < p.nKV; j0 += 32) {
-        const int j = j0 + lane;
-        const bool on = j < p.nKV && sel[j];
-        if (j < p.nKV) map[row * p.nKV + j] = on ? 1 : 0;
-        const bool f = on && kv_valid(p, b, j) > 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) q_idx[row * cap + cnt + __popc(bal & ((1u << lane) - 1u))] = j;
-        cnt += __popc(bal);
+    __syncwarp();
+    for (int r = 0; r < RPW; ++r) {
+        const int i = i0 + w * RPW + r;
+        if (i >= p.nQ) break;
+        const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
+        const float *sc = ssc + (w * RPW + r) * p.nKV;
+        const int k = q_rows(p, b, i) > 0 ? min(topk, p.nKV) : 0;
+        uint32_t T = 0xFFFFFFFFu;  // no key reaches it: nothing selected when k = 0
+        int need = 0;             // keys == T to take, lowest index first
+        if (k > 0) {
+            uint32_t pre = 0u;
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t cand = pre | (1u << bit);
+                int c = 0;
+                for (int j = lane; j < p.nKV; j += 32) c += score_key(sc[j]) >= cand;
+                if ((int)__reduce_add_sync(0xffffffffu, (unsigned)c) >= k) pre = cand;
+            }
+            T = pre;
+            int gt = 0;
+            for (int j = lane; j < p.nKV; j += 32) gt += score_key(sc[j]) > T;
+            need = k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+        }
+        int cnt = 0, taken = 0;
+        for (int j0 = 0; j0 < p.nKV; j0 += 32) {
+            const int j = j0 + lane;
+            const bool inb = k > 0 && j < p.nKV;
+            const uint32_t key = inb ? score_key(sc[j]) : 0u;
+            const bool tie = inb && key == T;
+            const unsigned eq = __ballot_sync(0xffffffffu, tie);
+            const bool on = inb && (key > T || (tie && taken + __popc(eq & ((1u << lane) - 1u)) < need));
+            taken += __popc(eq);
+            if (j < p.nKV) map[row * p.nKV + j] = on ? 1 : 0;
+            const bool f = on && kv_valid(p, b, j) > 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            if (f) q_idx[row * cap + cnt + __popc(bal & ((1u << lane) - 1u))] = j;
+            cnt += __popc(bal);
+        }
+        for (int n = cnt + lane; n < cap; n += 32) q_idx[row * cap + n] = -1;
+        if (lane == 0) q_cnt[row] = cnt;
     }
-    for (int n = cnt + lane; n < cap; n += 32) q_idx[row * cap + n] = -1;
-    if (lane == 0) q_cnt[row] = cnt;
+}
+
+size_t select_smem(int rpw, int nKV) {
+    return sizeof(float) * ((size_t)kSelChunk * kSelPitch + (size_t)8 * rpw * 128 + (size_t)8 * rpw * nKV);
 }
 
 cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map, int *q_idx,
                           int *q_cnt, int cap, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (kSelChunk * 129 + kSelRows * 128 + (size_t)kSelRows * p.nKV) +
-                        (size_t)kSelRows * p.nKV;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_select<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_select<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_select<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attr = true;
     }
-    dim3 grid((p.nQ + kSelRows - 1) / kSelRows, p.Hq, p.B);
+    const size_t cap_smem = 227 * 1024;
+    const int rpw = select_smem(4, p.nKV) <= cap_smem ? 4 : (select_smem(2, p.nKV) <= cap_smem ? 2 : 1);
+    const int R = 8 * rpw;
+    dim3 grid((p.nQ + R - 1) / R, p.Hq, p.B);
     prof_begin("select_topk", s);
-    k_select<<<grid, 256, smem, s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
+    if (rpw == 4)
+        k_select<4><<<grid, 256, select_smem(4, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
+    else if (rpw == 2)
+        k_select<2><<<grid, 256, select_smem(2, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
+    else
+        k_select<1><<<grid, 256, select_smem(1, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
     prof_end(s);
     return cudaGetLastError();
 }

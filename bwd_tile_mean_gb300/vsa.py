@@ -31,7 +31,8 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_status_string", "vsa_last_cuda_error", "vsa_device_status", "vsa_profile_enable", "vsa_profile_count",
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
-           "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout")
+           "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
+           "vsa_train_step_host_size", "vsa_train_step_host")
 
 
 class VsaError(RuntimeError):
@@ -112,6 +113,11 @@ def lib():
         L.vsa_tile_3d.argtypes = [C.c_int] * 8 + [P, P, P, P]
         L.vsa_untile_3d.restype = C.c_int
         L.vsa_untile_3d.argtypes = [C.c_int] * 8 + [P, P, P]
+        L.vsa_train_step_host_size.restype = C.c_size_t
+        L.vsa_train_step_host_size.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int]
+        L.vsa_train_step_host.restype = C.c_int
+        L.vsa_train_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, P, P, P,
+                                          C.c_size_t, P]
         _lib = L
     return _lib
 
@@ -318,6 +324,31 @@ class Plan:
 
     def device_status(self, stream=None) -> int:
         return vsa_device_status(self.workspace, stream)
+
+    def train_step_host(self, q, k, v, dO, topk, groups, out=None, lse=None, dq=None, dk=None, dv=None,
+                        stream=None):
+        """vsa_train_step_host: one step (block map, forward, backward) from
+        host tensors (pin them for overlap), heads in `groups` slices whose
+        copies overlap the kernels. Outputs are host tensors (allocated
+        pinned when not given); `stream` is left ordered after the last
+        copy back, so synchronise it before reading them. Returns (out, lse,
+        dq, dk, dv); out / lse only if passed in."""
+        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk)))
+        if need == 0:
+            raise ValueError("invalid descriptor, groups or topk for vsa_train_step_host")
+        buf = getattr(self, "_host_step_buf", None)
+        if buf is None or buf.numel() < need:
+            buf = self._host_step_buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+        dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if dq is None else dq
+        dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True) if dk is None else dk
+        dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True) if dv is None else dv
+        for t in (q, k, v, dO, out, lse, dq, dk, dv):
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("vsa_train_step_host takes contiguous host tensors")
+        _check("vsa_train_step_host", lib().vsa_train_step_host(
+            C.byref(self.desc), int(groups), _p(q), _p(k), _p(v), _p(dO), _p(self.q_var), _p(self.kv_var),
+            int(topk), _p(out), _p(lse), _p(dq), _p(dk), _p(dv), _p(buf), need, _stream(stream)))
+        return out, lse, dq, dk, dv
 
 
 def default_scale(D: int) -> float:

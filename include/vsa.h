@@ -278,6 +278,44 @@ vsa_status vsa_tile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH
 vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH, int tW,
                          const void *tiled, void *latent, vsa_stream_t stream);
 
+/* One training step (block map, forward, backward; no compression branch)
+ * from HOST buffers, with the copies overlapped with the kernels. Every
+ * head is an independent problem (the per-(batch, head) loops of
+ * [NPU-test]'s TND/GQA golden), so the heads are cut into `groups` slices
+ * of Hq/groups query and Hkv/groups key/value heads (Hkv % groups == 0;
+ * GQA groups stay whole). Slice g's q, k, v, dO are copied host -> device
+ * (strided 2D copies into a compact staging slot) on an internal stream
+ * while slice g-1 computes on `stream` and slice g-2's results are copied
+ * device -> host on a second internal stream; two staging slots alternate.
+ * Each slice runs vsa_build_block_map (topk, with the KV-owned index),
+ * vsa_fwd and vsa_bwd on its own descriptor, so every output is
+ * bit-identical to those calls on the whole problem.
+ *   q, k, v, dO:   host, in desc's layout and dtype (page-locked memory
+ *                  lets the copies run asynchronously and overlap);
+ *   out, lse:      host outputs O and LSE (lse: fp32 [B, Hq, Sq], TND
+ *                  [Hq, T_q]); either may be NULL (then not copied back);
+ *   dq, dk, dv:    host gradients, shaped like q, k, v;
+ *   q_var, kv_var, desc->cu_seqlens_*: device, as for the other calls;
+ *   device_buf:    device staging memory, 256-byte aligned, at least
+ *                  vsa_train_step_host_size(desc, groups, topk) bytes
+ *                  (two slots of one slice's tensors, indices, LSE and
+ *                  workspace), owned by the caller.
+ * The call only enqueues work: everything it does is ordered after the
+ * work already queued on `stream`, and `stream` reaches the end of the call
+ * only after the last copy back has finished (synchronise `stream` before
+ * reading the host outputs; keep the host buffers alive until then).
+ * Errors: those of the three calls; VSA_ERR_SHAPE for groups < 1 or not
+ * dividing Hkv, topk < 1; VSA_ERR_NULL for a missing required host
+ * pointer; VSA_ERR_WORKSPACE for a NULL, misaligned or small device_buf;
+ * VSA_ERR_CUDA when a copy, stream or event call fails.
+ * vsa_train_step_host_size returns 0 for an invalid descriptor, groups or
+ * topk. */
+size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk);
+vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, const void *k, const void *v,
+                               const void *dO, const int32_t *q_var, const int32_t *kv_var, int topk,
+                               void *out, float *lse, void *dq, void *dk, void *dv, void *device_buf,
+                               size_t device_bytes, vsa_stream_t stream);
+
 const char *vsa_status_string(vsa_status status);
 
 /* Message of the last CUDA error behind a VSA_ERR_CUDA return, with the

@@ -82,3 +82,25 @@ def test_host_validation_errors(L):
     big = desc(nKV=4000, Skv=4000 * 256)
     assert L.vsa_build_block_map(C.byref(big), FAKE, FAKE, FAKE, FAKE, 2, 0, FAKE, FAKE, FAKE, 2, None, None,
                                  FAKE, 1 << 40, None) == 5   # nKV past the selection kernel limit
+
+
+def test_train_step_host_validation(L):
+    d = desc(Hq=4, Hkv=2)
+    one, two = L.vsa_train_step_host_size(C.byref(d), 1, 2), L.vsa_train_step_host_size(C.byref(d), 2, 2)
+    assert one > two > 0                               # two slots of a half-size slice
+    assert L.vsa_train_step_host_size(C.byref(d), 3, 2) == 0   # groups must divide Hkv
+    assert L.vsa_train_step_host_size(C.byref(d), 0, 2) == 0
+    assert L.vsa_train_step_host_size(C.byref(d), 2, 0) == 0   # topk < 1
+    assert L.vsa_train_step_host_size(C.byref(desc(D=64)), 1, 2) == 0
+
+    def call(groups=2, topk=2, q=FAKE, dq=FAKE, buf=C.c_void_p(1 << 20), nbytes=two, dd=d):
+        return L.vsa_train_step_host(C.byref(dd), groups, q, FAKE, FAKE, FAKE, FAKE, FAKE, topk, None, None, dq,
+                                     FAKE, FAKE, buf, nbytes, None)
+    assert call(groups=3) == 2                         # VSA_ERR_SHAPE
+    assert call(topk=0) == 2
+    assert call(q=None) == 1                           # VSA_ERR_NULL
+    assert call(dq=None) == 1
+    assert call(buf=None) == 7                         # VSA_ERR_WORKSPACE
+    assert call(buf=C.c_void_p((1 << 20) + 16)) == 7   # staging not 256-byte aligned
+    assert call(nbytes=two - 1) == 7
+    assert call(dd=desc(Hq=4, Hkv=2, dtype=5)) == 2    # the slice descriptor is checked too
