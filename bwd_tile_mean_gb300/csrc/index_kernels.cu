@@ -17,15 +17,25 @@
 namespace vsa {
 
 // ------------------------------------------------------------------ pool
-// One warp per (b, h, tile); lane l owns dims 4l..4l+3 and reads 8 bytes
-// of each token row, so a warp reads whole 256-byte rows (coalesced).
+// One warp per (tensor, b, h, tile); lane l owns dims 4l..4l+3 and reads 8
+// bytes of each token row, so a warp reads whole 256-byte rows (coalesced),
+// 16 rows in flight, and adds them in ascending token order. The tensors of
+// one call (q and k, or q, k and v) share one launch, so small problems
+// still fill the GPU.
 template <typename T>
-__global__ void __launch_bounds__(256) k_pool(Prob p, int q_side, const T *__restrict__ x,
-                                              float *__restrict__ out) {
+__global__ void __launch_bounds__(256) k_pool(Prob p, PoolSegs segs) {
+    long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    int si = 0;
+    while (si < segs.n && w >= segs.s[si].warps) {
+        w -= segs.s[si].warps;
+        ++si;
+    }
+    if (si >= segs.n) return;
+    const bool q_side = segs.s[si].q_side != 0;
+    const T *x = static_cast<const T *>(segs.s[si].x);
+    float *out = segs.s[si].out;
     const int H = q_side ? p.Hq : p.Hkv, nT = q_side ? p.nQ : p.nKV;
     const int Tt = q_side ? p.tile_q : p.tile_kv;
-    const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (w >= (long long)p.B * H * nT) return;
     const int t = (int)(w % nT), h = (int)((w / nT) % H), b = (int)(w / ((long long)nT * H));
     const int lane = threadIdx.x & 31;
     const int var = q_side ? q_valid(p, b, t) : kv_valid(p, b, t);
@@ -33,12 +43,12 @@ __global__ void __launch_bounds__(256) k_pool(Prob p, int q_side, const T *__res
     const T *base = x + tok_off(p, q_side, b, t * Tt, h) + lane * 4;
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     int r = 0;
-    for (; r + 8 <= var; r += 8) {
-        uint2 buf[8];
+    for (; r + 16 <= var; r += 16) {
+        uint2 buf[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) buf[u] = __ldg(reinterpret_cast<const uint2 *>(base + (long long)(r + u) * rs));
+        for (int u = 0; u < 16; ++u) buf[u] = __ldg(reinterpret_cast<const uint2 *>(base + (long long)(r + u) * rs));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
             float2 a = unpack2<T>(buf[u].x), c = unpack2<T>(buf[u].y);
             s[0] = __fadd_rn(s[0], a.x);
             s[1] = __fadd_rn(s[1], a.y);
@@ -63,18 +73,40 @@ __global__ void __launch_bounds__(256) k_pool(Prob p, int q_side, const T *__res
     *reinterpret_cast<float4 *>(out + w * p.D + lane * 4) = o;
 }
 
-cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s) {
-    const int H = q_side ? p.Hq : p.Hkv, nT = q_side ? p.nQ : p.nKV;
-    const long long warps = (long long)p.B * H * nT;
-    const int blocks = (int)((warps + 7) / 8);
+cudaError_t launch_pools(const Prob &p, const PoolSegs &segs_in, cudaStream_t s) {
+    PoolSegs segs = segs_in;
+    long long warps = 0;
+    for (int i = 0; i < segs.n; ++i) {
+        const bool q = segs.s[i].q_side != 0;
+        segs.s[i].warps = (long long)p.B * (q ? p.Hq : p.Hkv) * (q ? p.nQ : p.nKV);
+        warps += segs.s[i].warps;
+    }
+    const long long blocks = (warps + 7) / 8;
     if (blocks == 0) return cudaSuccess;
     prof_begin("pool", s);
     if (p.dtype == T_BF16)
-        k_pool<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, q_side, (const __nv_bfloat16 *)x, out);
+        k_pool<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, segs);
     else
-        k_pool<__half><<<blocks, 256, 0, s>>>(p, q_side, (const __half *)x, out);
+        k_pool<__half><<<(unsigned)blocks, 256, 0, s>>>(p, segs);
     prof_end(s);
     return cudaGetLastError();
+}
+
+cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s) {
+    PoolSegs segs{};
+    segs.n = 1;
+    segs.s[0] = PoolSeg{x, out, q_side ? 1 : 0, 0};
+    return launch_pools(p, segs, s);
+}
+
+cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
+                            float *pv, cudaStream_t s) {
+    PoolSegs segs{};
+    segs.s[0] = PoolSeg{q, pq, 1, 0};
+    segs.s[1] = PoolSeg{k, pk, 0, 0};
+    segs.s[2] = PoolSeg{v, pv, 0, 0};
+    segs.n = v ? 3 : 2;
+    return launch_pools(p, segs, s);
 }
 
 // ---------------------------------------------------------------- select

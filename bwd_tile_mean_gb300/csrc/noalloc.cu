@@ -101,8 +101,7 @@ extern "C" vsa_status vsa_build_block_map_static(const vsa_desc *desc, const voi
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Every element of pq and pk is written by the pooling kernels before
     // it is read, so the array needs no clearing between calls.
-    if (launch_pool(p, true, q, pq, s) != cudaSuccess) return VSA_ERR_CUDA;
-    if (launch_pool(p, false, k, pk, s) != cudaSuccess) return VSA_ERR_CUDA;
+    if (launch_pool_qkv(p, q, pq, k, pk, nullptr, nullptr, s) != cudaSuccess) return VSA_ERR_CUDA;
     if (launch_select(p, pq, pk, topk, block_map, q_idx, q_cnt, idx_cap, s) != cudaSuccess) return VSA_ERR_CUDA;
     if (need_bwd_index && launch_transpose(p, block_map, kv_ptr, kv_qidx, idx_cap, s) != cudaSuccess)
         return VSA_ERR_CUDA;

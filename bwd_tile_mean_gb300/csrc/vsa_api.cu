@@ -234,8 +234,7 @@ vsa_status vsa_build_block_map(const vsa_desc *desc, const void *q, const void *
     const WsLayout L = ws_layout(p, false);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk);
-    VSA_CUDA(launch_pool(p, true, q, pq, s));
-    VSA_CUDA(launch_pool(p, false, k, pk, s));
+    VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, nullptr, nullptr, s));
     VSA_CUDA(launch_select(p, pq, pk, topk, block_map, q_idx, q_cnt, idx_cap, s));
     if (need_bwd_index) VSA_CUDA(launch_transpose(p, block_map, kv_ptr, kv_qidx, idx_cap, s));
     return VSA_OK;
@@ -291,9 +290,7 @@ vsa_status fwd_impl(const vsa_desc *desc, const void *q, const void *k, const vo
     a.err = at<unsigned>(workspace, 0);
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
-        VSA_CUDA(launch_pool(p, true, q, pq, s));
-        VSA_CUDA(launch_pool(p, false, k, pk, s));
-        VSA_CUDA(launch_pool(p, false, v, pv, s));
+        VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));
         a.c = at<float>(workspace, L.c);
         VSA_CUDA(launch_compress_fwd(p, pq, pk, pv, const_cast<float *>(a.c), s));
     }
@@ -335,9 +332,7 @@ vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
     float *c = at<float>(workspace, L.c);
-    VSA_CUDA(launch_pool(p, true, q, pq, s));
-    VSA_CUDA(launch_pool(p, false, k, pk, s));
-    VSA_CUDA(launch_pool(p, false, v, pv, s));
+    VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));
     VSA_CUDA(launch_compress_fwd(p, pq, pk, pv, c, s));
     VSA_CUDA(launch_gate_grad(p, dO, c, dgate, s));
     return VSA_OK;
@@ -386,9 +381,7 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
     VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, nlse2, ndvec, s));
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
-        VSA_CUDA(launch_pool(p, true, q, pq, s));
-        VSA_CUDA(launch_pool(p, false, k, pk, s));
-        VSA_CUDA(launch_pool(p, false, v, pv, s));
+        VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));
         float *dpq = at<float>(workspace, L.dpq), *dpk = at<float>(workspace, L.dpk),
               *dpv = at<float>(workspace, L.dpv);
         VSA_CUDA(launch_compress_bwd(p, dO, gate, pq, pk, pv, at<float>(workspace, L.dc), at<float>(workspace, L.A),

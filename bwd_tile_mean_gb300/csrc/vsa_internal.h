@@ -19,7 +19,21 @@ void prof_end(cudaStream_t s);
 vsa_status status_from_cuda(cudaError_t e);
 
 // Tile pooling (fp32 means of the first var tokens), [B, H, nT, D].
+struct PoolSeg {
+    const void *x;     // q, k or v in the problem's layout
+    float *out;        // tile means [B, H, nT, D]
+    int q_side;        // 1: query tiles (q_var), 0: key/value tiles (kv_var)
+    long long warps;   // filled by launch_pools
+};
+struct PoolSegs {
+    PoolSeg s[3];
+    int n;
+};
+cudaError_t launch_pools(const Prob &p, const PoolSegs &segs, cudaStream_t s);
 cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s);
+// q and k (v == NULL) or q, k and v in one launch.
+cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
+                            float *pv, cudaStream_t s);
 // Coarse scores + per-row top-k -> block map and Q-owned index.
 cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map,
                           int *q_idx, int *q_cnt, int cap, cudaStream_t s);
