@@ -17,7 +17,8 @@
 //
 // Two staging slots alternate; a slot's inputs are refilled once the step
 // that read them is done, and its outputs are rewritten once their copy
-// back is done (events). A head slice is a strided 2D region of every
+// back is done (events). Within a slice the forward starts once q, k, v
+// have landed (dO follows during it), and O goes back during the backward. A head slice is a strided 2D region of every
 // layout (BSHD/TND: a run of Hs*D elements per token; BHSD: a run of
 // Hs*S*D per batch entry), copied with cudaMemcpy2DAsync. The step per
 // slice calls the same entry points as a device caller (vsa_build_block_map,
@@ -141,7 +142,9 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
 
     cudaStream_t sc = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+    // per slot: q/k/v landed, dO landed, forward done, step done, copies back done
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[2] = {}, ev_do[2] = {}, ev_fwd[2] = {}, ev_comp[2] = {},
+                ev_out[2] = {};
     vsa_status rc = VSA_OK;
     auto cu = [&](cudaError_t e) {
         if (e != cudaSuccess && rc == VSA_OK) rc = status_from_cuda(e);
@@ -156,7 +159,8 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
               cu(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking)) &&
               cu(cudaEventCreateWithFlags(&ev_start, evf)) && cu(cudaEventCreateWithFlags(&ev_end, evf));
     for (int i = 0; ok && i < 2; ++i)
-        ok = cu(cudaEventCreateWithFlags(&ev_in[i], evf)) && cu(cudaEventCreateWithFlags(&ev_comp[i], evf)) &&
+        ok = cu(cudaEventCreateWithFlags(&ev_in[i], evf)) && cu(cudaEventCreateWithFlags(&ev_do[i], evf)) &&
+             cu(cudaEventCreateWithFlags(&ev_fwd[i], evf)) && cu(cudaEventCreateWithFlags(&ev_comp[i], evf)) &&
              cu(cudaEventCreateWithFlags(&ev_out[i], evf));
     // both side streams start after what the caller queued before this call
     ok = ok && cu(cudaEventRecord(ev_start, sc)) && cu(cudaStreamWaitEvent(s_in, ev_start, 0)) &&
@@ -170,9 +174,10 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
         const Strided rq = head_slice(*desc, true, g * hq, hq, row), rk = head_slice(*desc, false, g * hk, hk, row);
         // inputs of slice g; the slot's previous inputs were read by step g-2
         if (g >= 2) ok = cu(cudaStreamWaitEvent(s_in, ev_comp[slot], 0));
+        // (q, k, v first: the block map and the forward start before dO lands)
         ok = ok && cu(copy_in(base + L.q, q, rq, s_in)) && cu(copy_in(base + L.k, k, rk, s_in)) &&
-             cu(copy_in(base + L.v, v, rk, s_in)) && cu(copy_in(base + L.dO, dO, rq, s_in)) &&
-             cu(cudaEventRecord(ev_in[slot], s_in));
+             cu(copy_in(base + L.v, v, rk, s_in)) && cu(cudaEventRecord(ev_in[slot], s_in)) &&
+             cu(copy_in(base + L.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
         // step g on the caller's stream; the slot's previous outputs were copied back
         ok = ok && cu(cudaStreamWaitEvent(sc, ev_in[slot], 0));
         if (ok && g >= 2) ok = cu(cudaStreamWaitEvent(sc, ev_out[slot], 0));
@@ -186,16 +191,19 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
                                     kvptr, kvqidx, ws, L.ws_bytes, stream)) &&
              vs(vsa_fwd(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, nullptr,
                         base + L.out, lse_d, nullptr, ws, L.ws_bytes, stream)) &&
+             cu(cudaEventRecord(ev_fwd[slot], sc)) && cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
              vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, base + L.out, lse_d, qidx, qcnt, cap,
                         kvptr, kvqidx, q_var, kv_var, nullptr, base + L.dq, base + L.dk, base + L.dv, ws, L.ws_bytes,
                         stream)) &&
              cu(cudaEventRecord(ev_comp[slot], sc));
-        // outputs of slice g
-        ok = ok && cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0));
+        // outputs of slice g: O and LSE are final after the forward, the
+        // gradients after the backward
+        ok = ok && cu(cudaStreamWaitEvent(s_out, ev_fwd[slot], 0));
         if (ok && out) ok = cu(copy_out(out, base + L.out, rq, s_out));
         if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, g * hq, hq), s_out));
-        ok = ok && cu(copy_out(dq, base + L.dq, rq, s_out)) && cu(copy_out(dk, base + L.dk, rk, s_out)) &&
-             cu(copy_out(dv, base + L.dv, rk, s_out)) && cu(cudaEventRecord(ev_out[slot], s_out));
+        ok = ok && cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + L.dq, rq, s_out)) &&
+             cu(copy_out(dk, base + L.dk, rk, s_out)) && cu(copy_out(dv, base + L.dv, rk, s_out)) &&
+             cu(cudaEventRecord(ev_out[slot], s_out));
     }
     // the caller's stream completes after the last copy back (and after the
     // input stream, so no copy outlives the call's work on its stream)
@@ -206,6 +214,8 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
     // destruction is deferred by the runtime until the queued work is done
     for (int i = 0; i < 2; ++i) {
         if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+        if (ev_do[i]) cudaEventDestroy(ev_do[i]);
+        if (ev_fwd[i]) cudaEventDestroy(ev_fwd[i]);
         if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
         if (ev_out[i]) cudaEventDestroy(ev_out[i]);
     }
