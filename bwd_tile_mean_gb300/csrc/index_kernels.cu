@@ -254,19 +254,17 @@ cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int t
                           int *q_cnt, int cap, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_select<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_select<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_select<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attr = true;
     }
     const size_t cap_smem = 227 * 1024;
-    const int rpw = select_smem(4, p.nKV) <= cap_smem ? 4 : (select_smem(2, p.nKV) <= cap_smem ? 2 : 1);
+    // two query tiles per warp: two blocks fit on an SM for the usual tile counts
+    const int rpw = select_smem(2, p.nKV) <= cap_smem ? 2 : 1;
     const int R = 8 * rpw;
     dim3 grid((p.nQ + R - 1) / R, p.Hq, p.B);
     prof_begin("select_topk", s);
-    if (rpw == 4)
-        k_select<4><<<grid, 256, select_smem(4, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
-    else if (rpw == 2)
+    if (rpw == 2)
         k_select<2><<<grid, 256, select_smem(2, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
     else
         k_select<1><<<grid, 256, select_smem(1, p.nKV), s>>>(p, pq, pk, topk, map, q_idx, q_cnt, cap);
