@@ -290,12 +290,13 @@ def ours(args):
             for n, x in per.items()}
 
     # end to end through the public API with host buffers (pinned), copies timed
-    host_in = {n: x.to("cpu").pin_memory() for n, x in (("q", q), ("k", k), ("v", v), ("dO", dO))}
+    ins = (("q", q), ("k", k), ("v", v), ("dO", dO)) + ((("gate", gate),) if gated else ())
+    host_in = {n: x.to("cpu").pin_memory() for n, x in ins}
     host_out = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for n, x in
                 (("out", out), ("dq", dq), ("dk", dk), ("dv", dv))}
     groups = max(g for g in range(1, 9) if p.Hkv % g == 0)
-    pipelined = train and not gated
-    dbuf = {} if pipelined else {n: torch.empty_like(x) for n, x in (("q", q), ("k", k), ("v", v), ("dO", dO))}
+    pipelined = train
+    dbuf = {} if pipelined else {n: torch.empty_like(x) for n, x in ins}
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
     e_steps = max(2, min(args.steps, 10))
@@ -304,12 +305,12 @@ def ours(args):
         if pipelined:
             # the library's host-buffer step: head slices, copies overlapped with the kernels
             plan.train_step_host(host_in["q"], host_in["k"], host_in["v"], host_in["dO"], p.topk, groups,
-                                 out=host_out["out"], dq=host_out["dq"], dk=host_out["dk"], dv=host_out["dv"],
-                                 stream=stream)
+                                 gate=host_in.get("gate"), out=host_out["out"], dq=host_out["dq"],
+                                 dk=host_out["dk"], dv=host_out["dv"], stream=stream)
             return
         for n in dbuf:
             dbuf[n].copy_(host_in[n], non_blocking=True)
-        step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["dO"])
+        step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["dO"])  # (forward only: no gate in these configurations)
         for n, x in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
             host_out[n].copy_(x, non_blocking=True)
 

@@ -23,8 +23,9 @@
 // Hs*S*D per batch entry), copied with cudaMemcpy2DAsync. The step per
 // slice calls the same entry points as a device caller (vsa_build_block_map,
 // vsa_fwd, vsa_bwd on the slice's descriptor), so results are bit-identical
-// to running the whole problem on the device. No device memory is
-// allocated here: the caller provides the staging buffer.
+// to running the whole problem on the device; with a gate, the gated
+// compression branch runs too (its tile means are per head as well). No
+// device memory is allocated here: the caller provides the staging buffer.
 #include <cstdint>
 
 #include "vsa.h"
@@ -35,12 +36,13 @@ namespace {
 
 struct SlotLayout {
     size_t q, k, v, dO, out, dq, dk, dv, lse, map, qidx, qcnt, kvptr, kvqidx, ws, ws_bytes, bytes;
+    size_t gate, osp;  // gated compression branch only
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Sizes of one head slice (descriptor `s`: Hq and Hkv already divided).
-SlotLayout slot_layout(const vsa_desc &s, int cap) {
+SlotLayout slot_layout(const vsa_desc &s, int cap, bool gated) {
     SlotLayout L{};
     const size_t es = 2;
     const bool tnd = s.layout == VSA_LAYOUT_TND;
@@ -67,7 +69,11 @@ SlotLayout slot_layout(const vsa_desc &s, int cap) {
     L.qcnt = take(rows * 4);
     L.kvptr = take((size_t)s.B * s.Hq * (s.nKV + 1) * 4);
     L.kvqidx = take(rows * cap * 4);
-    L.ws_bytes = vsa_workspace_size(&s, 0);
+    if (gated) {
+        L.gate = take(qb);
+        L.osp = take(qb);
+    }
+    L.ws_bytes = vsa_workspace_size(&s, gated ? 1 : 0);
     L.ws = take(L.ws_bytes);
     L.bytes = off;
     return L;
@@ -119,15 +125,15 @@ vsa_status check_groups(const vsa_desc *d, int groups, int topk, vsa_desc *slice
 
 using namespace vsa;
 
-extern "C" size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk) {
+extern "C" size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk, int with_gate) {
     vsa_desc s;
     int cap = 0;
     if (check_groups(desc, groups, topk, &s, &cap) != VSA_OK) return 0;
-    return 2 * slot_layout(s, cap).bytes;
+    return 2 * slot_layout(s, cap, with_gate != 0).bytes;
 }
 
 extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, const void *k,
-                                          const void *v, const void *dO, const int32_t *q_var,
+                                          const void *v, const void *dO, const void *gate, const int32_t *q_var,
                                           const int32_t *kv_var, int topk, void *out, float *lse, void *dq,
                                           void *dk, void *dv, void *device_buf, size_t device_bytes,
                                           vsa_stream_t stream) {
@@ -136,7 +142,8 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
     const vsa_status st = check_groups(desc, groups, topk, &sd, &cap);
     if (st != VSA_OK) return st;
     if (!q || !k || !v || !dO || !dq || !dk || !dv) return VSA_ERR_NULL;
-    const SlotLayout L = slot_layout(sd, cap);
+    const bool gated = gate != nullptr;
+    const SlotLayout L = slot_layout(sd, cap, gated);
     if (!device_buf || (reinterpret_cast<uintptr_t>(device_buf) & 255u) != 0 || device_bytes < 2 * L.bytes)
         return VSA_ERR_WORKSPACE;
 
@@ -176,7 +183,9 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
         if (g >= 2) ok = cu(cudaStreamWaitEvent(s_in, ev_comp[slot], 0));
         // (q, k, v first: the block map and the forward start before dO lands)
         ok = ok && cu(copy_in(base + L.q, q, rq, s_in)) && cu(copy_in(base + L.k, k, rk, s_in)) &&
-             cu(copy_in(base + L.v, v, rk, s_in)) && cu(cudaEventRecord(ev_in[slot], s_in)) &&
+             cu(copy_in(base + L.v, v, rk, s_in));
+        if (ok && gated) ok = cu(copy_in(base + L.gate, gate, rq, s_in));
+        ok = ok && cu(cudaEventRecord(ev_in[slot], s_in)) &&
              cu(copy_in(base + L.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
         // step g on the caller's stream; the slot's previous outputs were copied back
         ok = ok && cu(cudaStreamWaitEvent(sc, ev_in[slot], 0));
@@ -187,14 +196,17 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
         int32_t *kvptr = reinterpret_cast<int32_t *>(base + L.kvptr);
         int32_t *kvqidx = reinterpret_cast<int32_t *>(base + L.kvqidx);
         float *lse_d = reinterpret_cast<float *>(base + L.lse);
+        // gated: O (the sparse attention output) stays in its own buffer, out = O + gate (*) c
+        const void *g_d = gated ? base + L.gate : nullptr;
+        void *osp_d = gated ? base + L.osp : nullptr;
         ok = vs(vsa_build_block_map(&sd, base + L.q, base + L.k, q_var, kv_var, topk, 1, base + L.map, qidx, qcnt, cap,
                                     kvptr, kvqidx, ws, L.ws_bytes, stream)) &&
-             vs(vsa_fwd(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, nullptr,
-                        base + L.out, lse_d, nullptr, ws, L.ws_bytes, stream)) &&
+             vs(vsa_fwd(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, g_d, base + L.out,
+                        lse_d, osp_d, ws, L.ws_bytes, stream)) &&
              cu(cudaEventRecord(ev_fwd[slot], sc)) && cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
-             vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, base + L.out, lse_d, qidx, qcnt, cap,
-                        kvptr, kvqidx, q_var, kv_var, nullptr, base + L.dq, base + L.dk, base + L.dv, ws, L.ws_bytes,
-                        stream)) &&
+             vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out, lse_d,
+                        qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk, base + L.dv,
+                        ws, L.ws_bytes, stream)) &&
              cu(cudaEventRecord(ev_comp[slot], sc));
         // outputs of slice g: O and LSE are final after the forward, the
         // gradients after the backward

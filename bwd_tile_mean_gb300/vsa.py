@@ -114,10 +114,10 @@ def lib():
         L.vsa_untile_3d.restype = C.c_int
         L.vsa_untile_3d.argtypes = [C.c_int] * 8 + [P, P, P]
         L.vsa_train_step_host_size.restype = C.c_size_t
-        L.vsa_train_step_host_size.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int]
+        L.vsa_train_step_host_size.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, C.c_int]
         L.vsa_train_step_host.restype = C.c_int
-        L.vsa_train_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, P, P, P,
-                                          C.c_size_t, P]
+        L.vsa_train_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P,
+                                          P, C.c_size_t, P]
         _lib = L
     return _lib
 
@@ -325,15 +325,17 @@ class Plan:
     def device_status(self, stream=None) -> int:
         return vsa_device_status(self.workspace, stream)
 
-    def train_step_host(self, q, k, v, dO, topk, groups, out=None, lse=None, dq=None, dk=None, dv=None,
-                        stream=None):
-        """vsa_train_step_host: one step (block map, forward, backward) from
-        host tensors (pin them for overlap), heads in `groups` slices whose
-        copies overlap the kernels. Outputs are host tensors (allocated
-        pinned when not given); `stream` is left ordered after the last
-        copy back, so synchronise it before reading them. Returns (out, lse,
-        dq, dk, dv); out / lse only if passed in."""
-        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk)))
+    def train_step_host(self, q, k, v, dO, topk, groups, gate=None, out=None, lse=None, dq=None, dk=None,
+                        dv=None, stream=None):
+        """vsa_train_step_host: one step (block map, forward, backward; with
+        a gate also the gated compression branch) from host tensors (pin
+        them for overlap), heads in `groups` slices whose copies overlap the
+        kernels. Outputs are host tensors (allocated pinned when not given);
+        `stream` is left ordered after the last copy back, so synchronise it
+        before reading them. Returns (out, lse, dq, dk, dv); out / lse only
+        if passed in."""
+        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk),
+                                                  int(gate is not None)))
         if need == 0:
             raise ValueError("invalid descriptor, groups or topk for vsa_train_step_host")
         buf = getattr(self, "_host_step_buf", None)
@@ -342,11 +344,11 @@ class Plan:
         dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if dq is None else dq
         dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True) if dk is None else dk
         dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True) if dv is None else dv
-        for t in (q, k, v, dO, out, lse, dq, dk, dv):
+        for t in (q, k, v, dO, gate, out, lse, dq, dk, dv):
             if t is not None and (t.is_cuda or not t.is_contiguous()):
                 raise ValueError("vsa_train_step_host takes contiguous host tensors")
         _check("vsa_train_step_host", lib().vsa_train_step_host(
-            C.byref(self.desc), int(groups), _p(q), _p(k), _p(v), _p(dO), _p(self.q_var), _p(self.kv_var),
+            C.byref(self.desc), int(groups), _p(q), _p(k), _p(v), _p(dO), _p(gate), _p(self.q_var), _p(self.kv_var),
             int(topk), _p(out), _p(lse), _p(dq), _p(dk), _p(dv), _p(buf), need, _stream(stream)))
         return out, lse, dq, dk, dv
 

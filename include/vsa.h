@@ -278,8 +278,9 @@ vsa_status vsa_tile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH
 vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH, int tW,
                          const void *tiled, void *latent, vsa_stream_t stream);
 
-/* One training step (block map, forward, backward; no compression branch)
- * from HOST buffers, with the copies overlapped with the kernels. Every
+/* One training step (block map, forward, backward; with gate != NULL also
+ * the gated compression branch) from HOST buffers, with the copies
+ * overlapped with the kernels. Every
  * head is an independent problem (the per-(batch, head) loops of
  * [NPU-test]'s TND/GQA golden), so the heads are cut into `groups` slices
  * of Hq/groups query and Hkv/groups key/value heads (Hkv % groups == 0;
@@ -292,14 +293,17 @@ vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int 
  * bit-identical to those calls on the whole problem.
  *   q, k, v, dO:   host, in desc's layout and dtype (page-locked memory
  *                  lets the copies run asynchronously and overlap);
+ *   gate:          host, q-shaped, or NULL (no compression branch); with a
+ *                  gate, out = O + gate (*) c as in vsa_fwd, and the
+ *                  backward's compression gradients are included;
  *   out, lse:      host outputs O and LSE (lse: fp32 [B, Hq, Sq], TND
  *                  [Hq, T_q]); either may be NULL (then not copied back);
  *   dq, dk, dv:    host gradients, shaped like q, k, v;
  *   q_var, kv_var, desc->cu_seqlens_*: device, as for the other calls;
  *   device_buf:    device staging memory, 256-byte aligned, at least
- *                  vsa_train_step_host_size(desc, groups, topk) bytes
- *                  (two slots of one slice's tensors, indices, LSE and
- *                  workspace), owned by the caller.
+ *                  vsa_train_step_host_size(desc, groups, topk,
+ *                  gate != NULL) bytes (two slots of one slice's tensors,
+ *                  indices, LSE and workspace), owned by the caller.
  * The call only enqueues work: everything it does is ordered after the
  * work already queued on `stream`, and `stream` reaches the end of the call
  * only after the last copy back has finished (synchronise `stream` before
@@ -310,10 +314,10 @@ vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int 
  * VSA_ERR_CUDA when a copy, stream or event call fails.
  * vsa_train_step_host_size returns 0 for an invalid descriptor, groups or
  * topk. */
-size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk);
+size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk, int with_gate);
 vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, const void *k, const void *v,
-                               const void *dO, const int32_t *q_var, const int32_t *kv_var, int topk,
-                               void *out, float *lse, void *dq, void *dk, void *dv, void *device_buf,
+                               const void *dO, const void *gate, const int32_t *q_var, const int32_t *kv_var,
+                               int topk, void *out, float *lse, void *dq, void *dk, void *dv, void *device_buf,
                                size_t device_bytes, vsa_stream_t stream);
 
 const char *vsa_status_string(vsa_status status);

@@ -86,16 +86,18 @@ def test_host_validation_errors(L):
 
 def test_train_step_host_validation(L):
     d = desc(Hq=4, Hkv=2)
-    one, two = L.vsa_train_step_host_size(C.byref(d), 1, 2), L.vsa_train_step_host_size(C.byref(d), 2, 2)
+    size = lambda dd, g, k, gate=0: L.vsa_train_step_host_size(C.byref(dd), g, k, gate)
+    one, two = size(d, 1, 2), size(d, 2, 2)
     assert one > two > 0                               # two slots of a half-size slice
-    assert L.vsa_train_step_host_size(C.byref(d), 3, 2) == 0   # groups must divide Hkv
-    assert L.vsa_train_step_host_size(C.byref(d), 0, 2) == 0
-    assert L.vsa_train_step_host_size(C.byref(d), 2, 0) == 0   # topk < 1
-    assert L.vsa_train_step_host_size(C.byref(desc(D=64)), 1, 2) == 0
+    assert size(d, 2, 2, 1) > two                      # the gate, o_sparse and gated workspace
+    assert size(d, 3, 2) == 0                          # groups must divide Hkv
+    assert size(d, 0, 2) == 0
+    assert size(d, 2, 0) == 0                          # topk < 1
+    assert size(desc(D=64), 1, 2) == 0
 
-    def call(groups=2, topk=2, q=FAKE, dq=FAKE, buf=C.c_void_p(1 << 20), nbytes=two, dd=d):
-        return L.vsa_train_step_host(C.byref(dd), groups, q, FAKE, FAKE, FAKE, FAKE, FAKE, topk, None, None, dq,
-                                     FAKE, FAKE, buf, nbytes, None)
+    def call(groups=2, topk=2, q=FAKE, dq=FAKE, buf=C.c_void_p(1 << 20), nbytes=two, dd=d, gate=None):
+        return L.vsa_train_step_host(C.byref(dd), groups, q, FAKE, FAKE, FAKE, gate, FAKE, FAKE, topk, None, None,
+                                     dq, FAKE, FAKE, buf, nbytes, None)
     assert call(groups=3) == 2                         # VSA_ERR_SHAPE
     assert call(topk=0) == 2
     assert call(q=None) == 1                           # VSA_ERR_NULL
@@ -103,4 +105,5 @@ def test_train_step_host_validation(L):
     assert call(buf=None) == 7                         # VSA_ERR_WORKSPACE
     assert call(buf=C.c_void_p((1 << 20) + 16)) == 7   # staging not 256-byte aligned
     assert call(nbytes=two - 1) == 7
+    assert call(gate=FAKE) == 7                        # a gate needs the larger staging buffer
     assert call(dd=desc(Hq=4, Hkv=2, dtype=5)) == 2    # the slice descriptor is checked too

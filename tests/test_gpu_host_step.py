@@ -24,6 +24,8 @@ def cases():
                  kv_lens=[540, 23, 200], topk=3, seed=73), 2),
         (Problem("host-one-group", "bshd", 1, 2, 1, 128, 256, 256, 2, 3, q_var=[256, 256], kv_var=[256] * 3,
                  topk=2, seed=74), 1),
+        (Problem("host-gated-ragged", "bshd", 1, 4, 4, 128, 256, 256, 3, 5, q_var=[256, 160, 256],
+                 kv_var=[256, 160, 64, 40, 256], topk=3, gate="uniform_token_head", seed=75), 2),
     ]
 
 
@@ -38,8 +40,9 @@ def test_host_step_equals_device_path(case):
     g = to_device(t)
     plan = plan_for(p)
     plan.build_block_map(g["q"], g["k"], p.topk)
-    out, lse, osp = plan.forward(g["q"], g["k"], g["v"])
-    dq, dk, dv = plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse)
+    gate = g.get("gate")
+    out, lse, osp = plan.forward(g["q"], g["k"], g["v"], gate=gate)
+    dq, dk, dv = plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse, gate=gate)
     torch.cuda.synchronize()
 
     hp = plan_for(p)
@@ -47,14 +50,15 @@ def test_host_step_equals_device_path(case):
     h_lse = torch.empty(tuple(lse.shape), dtype=torch.float32, pin_memory=True)
     stream = torch.cuda.Stream()
     o2, l2, dq2, dk2, dv2 = hp.train_step_host(host(g["q"]), host(g["k"]), host(g["v"]), host(g["dO"]), p.topk,
-                                               groups, out=h_out, lse=h_lse, stream=stream)
+                                               groups, gate=None if gate is None else host(gate), out=h_out,
+                                               lse=h_lse, stream=stream)
     stream.synchronize()
     assert hp.device_status() == 0
     for name, a, b in (("out", out, o2), ("dq", dq, dq2), ("dk", dk, dk2), ("dv", dv, dv2)):
         assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16)), name
     assert torch.equal(lse.cpu(), l2)
 
-    if p.name == "host-one-group":  # and directly against the oracle
+    if p.name in ("host-one-group", "host-gated-ragged"):  # and directly against the oracle
         ref = orc.run_full(p, t)
         check_tol("host out", ref["out"], o2.double().numpy(), OUT_TOL)
         for n, x in (("dq", dq2), ("dk", dk2), ("dv", dv2)):

@@ -63,6 +63,57 @@ def test_block_map_bit_exact(p):
     assert np.array_equal(plan.kv_qidx.cpu().numpy(), kq)
 
 
+def tie_cases():
+    """Selections decided by ties: duplicated K tiles (equal scores for every
+    query), an all-zero K tile (score exactly 0), an all-zero Q tile (every
+    score 0), empty KV tiles (-inf), more KV tiles than a warp's lanes, and
+    topk above the number of valid tiles."""
+    a = Problem("ties-40kv", "bshd", 1, 4, 2, 128, 256, 256, 3, 40, q_var=[256, 256, 256],
+                kv_var=[256] * 3 + [0] + [256] * 26 + [0] + [256] * 9, topk=10, seed=31)
+    b = Problem("ties-topk-gt-valid", "bhsd", 1, 2, 2, 128, 256, 256, 2, 6, q_var=[256, 256],
+                kv_var=[256, 0, 120, 0, 256, 0], topk=5, seed=32)
+    return [a, b]
+
+
+def make_ties(p, t):
+    k, q = t["k"].clone(), t["q"].clone()
+    T = p.tile_kv
+
+    def tile(x, j):  # token range of tile j in the layout
+        return (slice(None), slice(None), slice(j * T, (j + 1) * T)) if p.layout == "bhsd" else \
+            (slice(None), slice(j * T, (j + 1) * T))
+    for j in (7, 13, 21, 33):
+        if j < p.nKV:
+            k[tile(k, j)] = k[tile(k, 0)]
+    k[tile(k, 2)] = 0
+    if p.nKV > 5:
+        k[tile(k, 5)] = k[tile(k, 4)]
+    q[tile(q, 1)] = 0
+    t = dict(t)
+    t["k"], t["q"] = k, q
+    return t
+
+
+@pytest.mark.parametrize("p", tie_cases(), ids=lambda p: p.name)
+def test_block_map_ties_bit_exact(p):
+    t = make_ties(p, make_tensors(p))
+    plan, _ = run_map(p, t)
+    m, qi, qc, sc = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    kp, kq = orc.transpose(p, qi, qc, p.cap)
+    torch.cuda.synchronize()
+    # the constructed ties are really there: equal scores across duplicated
+    # tiles, or (topk above the valid tiles) the lowest empty tiles chosen
+    if p.nKV > 7:
+        assert np.any(sc[..., 0] == sc[..., 7])
+    else:
+        assert np.all(m[..., 1] == 1) and np.all(m[..., 3] == 1) and not np.any(m[..., 5])
+    assert np.array_equal(plan.block_map.cpu().numpy(), m)
+    assert np.array_equal(plan.q_cnt.cpu().numpy(), qc)
+    assert np.array_equal(plan.q_idx.cpu().numpy(), qi)
+    assert np.array_equal(plan.kv_ptr.cpu().numpy(), kp)
+    assert np.array_equal(plan.kv_qidx.cpu().numpy(), kq)
+
+
 def test_mask_index_bit_exact_varlen():
     p = config(2)
     t = make_tensors(p)
