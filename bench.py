@@ -290,29 +290,25 @@ def ours(args):
             for n, x in per.items()}
 
     # end to end through the public API with host buffers (pinned), copies timed
-    ins = (("q", q), ("k", k), ("v", v), ("dO", dO)) + ((("gate", gate),) if gated else ())
+    # (training: q, k, v, dO [, gate] in, O, dq, dk, dv out; inference: q, k, v [, gate] in, O out)
+    ins = (("q", q), ("k", k), ("v", v)) + ((("dO", dO),) if train else ()) + ((("gate", gate),) if gated else ())
+    outs = (("out", out),) + ((("dq", dq), ("dk", dk), ("dv", dv)) if train else ())
     host_in = {n: x.to("cpu").pin_memory() for n, x in ins}
-    host_out = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for n, x in
-                (("out", out), ("dq", dq), ("dk", dk), ("dv", dv))}
+    host_out = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for n, x in outs}
     groups = max(g for g in range(1, 9) if p.Hkv % g == 0)
-    pipelined = train
-    dbuf = {} if pipelined else {n: torch.empty_like(x) for n, x in ins}
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
     e_steps = max(2, min(args.steps, 10))
 
     def e2e_step():
-        if pipelined:
-            # the library's host-buffer step: head slices, copies overlapped with the kernels
+        # the library's host-buffer step: head slices, copies overlapped with the kernels
+        if train:
             plan.train_step_host(host_in["q"], host_in["k"], host_in["v"], host_in["dO"], p.topk, groups,
                                  gate=host_in.get("gate"), out=host_out["out"], dq=host_out["dq"],
                                  dk=host_out["dk"], dv=host_out["dv"], stream=stream)
-            return
-        for n in dbuf:
-            dbuf[n].copy_(host_in[n], non_blocking=True)
-        step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["dO"])  # (forward only: no gate in these configurations)
-        for n, x in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
-            host_out[n].copy_(x, non_blocking=True)
+        else:
+            plan.fwd_step_host(host_in["q"], host_in["k"], host_in["v"], p.topk, groups, gate=host_in.get("gate"),
+                               out=host_out["out"], stream=stream)
 
     e2e_step()
     barrier()
@@ -377,8 +373,8 @@ def ours(args):
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": step_flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": (f"vsa_train_step_host: {groups} head slices, copies overlapped with the kernels"
-                         if pipelined else "copies, then the step, then copies back, on one stream")},
+                "path": f"{'vsa_train_step_host' if train else 'vsa_fwd_step_host'}: {groups} head slices, "
+                        "copies overlapped with the kernels"},
         "gpu_launches": launches, "clocks": clocks,
         "layout_step": {"bound": "hbm", "peak_GB_per_s": pk.get("hbm_gbs"), **layout},
         "kernels": {n: {"avg_ms": round(x["avg_ms"], 4), "launches_per_step": x["launches"] // args.steps,

@@ -15,6 +15,8 @@
 //   caller stream:          step(0) step(1) step(2) ...
 //   out-stream:                     D2H(0)  D2H(1) ...
 //
+// vsa_fwd_step_host is the same pipeline for inference (block map without
+// the KV-owned index, forward; O and LSE come back).
 // Two staging slots alternate; a slot's inputs are refilled once the step
 // that read them is done, and its outputs are rewritten once their copy
 // back is done (events). Within a slice the forward starts once q, k, v
@@ -132,16 +134,21 @@ extern "C" size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int
     return 2 * slot_layout(s, cap, with_gate != 0).bytes;
 }
 
-extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, const void *k,
-                                          const void *v, const void *dO, const void *gate, const int32_t *q_var,
-                                          const int32_t *kv_var, int topk, void *out, float *lse, void *dq,
-                                          void *dk, void *dv, void *device_buf, size_t device_bytes,
-                                          vsa_stream_t stream) {
+namespace vsa {
+namespace {
+
+// The pipelined step; train == false runs the block map and the forward
+// only (no dO in, no gradients out, no KV-owned index).
+vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q, const void *k, const void *v,
+                     const void *dO, const void *gate, const int32_t *q_var, const int32_t *kv_var, int topk,
+                     void *out, float *lse, void *dq, void *dk, void *dv, void *device_buf, size_t device_bytes,
+                     vsa_stream_t stream) {
     vsa_desc sd;
     int cap = 0;
     const vsa_status st = check_groups(desc, groups, topk, &sd, &cap);
     if (st != VSA_OK) return st;
-    if (!q || !k || !v || !dO || !dq || !dk || !dv) return VSA_ERR_NULL;
+    if (!q || !k || !v) return VSA_ERR_NULL;
+    if (train ? (!dO || !dq || !dk || !dv) : !out) return VSA_ERR_NULL;
     const bool gated = gate != nullptr;
     const SlotLayout L = slot_layout(sd, cap, gated);
     if (!device_buf || (reinterpret_cast<uintptr_t>(device_buf) & 255u) != 0 || device_bytes < 2 * L.bytes)
@@ -185,8 +192,8 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
         ok = ok && cu(copy_in(base + L.q, q, rq, s_in)) && cu(copy_in(base + L.k, k, rk, s_in)) &&
              cu(copy_in(base + L.v, v, rk, s_in));
         if (ok && gated) ok = cu(copy_in(base + L.gate, gate, rq, s_in));
-        ok = ok && cu(cudaEventRecord(ev_in[slot], s_in)) &&
-             cu(copy_in(base + L.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
+        ok = ok && cu(cudaEventRecord(ev_in[slot], s_in));
+        if (ok && train) ok = cu(copy_in(base + L.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
         // step g on the caller's stream; the slot's previous outputs were copied back
         ok = ok && cu(cudaStreamWaitEvent(sc, ev_in[slot], 0));
         if (ok && g >= 2) ok = cu(cudaStreamWaitEvent(sc, ev_out[slot], 0));
@@ -199,23 +206,27 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
         // gated: O (the sparse attention output) stays in its own buffer, out = O + gate (*) c
         const void *g_d = gated ? base + L.gate : nullptr;
         void *osp_d = gated ? base + L.osp : nullptr;
-        ok = vs(vsa_build_block_map(&sd, base + L.q, base + L.k, q_var, kv_var, topk, 1, base + L.map, qidx, qcnt, cap,
-                                    kvptr, kvqidx, ws, L.ws_bytes, stream)) &&
+        ok = vs(vsa_build_block_map(&sd, base + L.q, base + L.k, q_var, kv_var, topk, train ? 1 : 0, base + L.map,
+                                    qidx, qcnt, cap, train ? kvptr : nullptr, train ? kvqidx : nullptr, ws,
+                                    L.ws_bytes, stream)) &&
              vs(vsa_fwd(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, g_d, base + L.out,
                         lse_d, osp_d, ws, L.ws_bytes, stream)) &&
-             cu(cudaEventRecord(ev_fwd[slot], sc)) && cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
-             vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out, lse_d,
-                        qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk, base + L.dv,
-                        ws, L.ws_bytes, stream)) &&
-             cu(cudaEventRecord(ev_comp[slot], sc));
+             cu(cudaEventRecord(ev_fwd[slot], sc));
+        if (ok && train)
+            ok = cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
+                 vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out, lse_d,
+                            qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk, base + L.dv,
+                            ws, L.ws_bytes, stream));
+        ok = ok && cu(cudaEventRecord(ev_comp[slot], sc));
         // outputs of slice g: O and LSE are final after the forward, the
         // gradients after the backward
         ok = ok && cu(cudaStreamWaitEvent(s_out, ev_fwd[slot], 0));
         if (ok && out) ok = cu(copy_out(out, base + L.out, rq, s_out));
         if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, g * hq, hq), s_out));
-        ok = ok && cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + L.dq, rq, s_out)) &&
-             cu(copy_out(dk, base + L.dk, rk, s_out)) && cu(copy_out(dv, base + L.dv, rk, s_out)) &&
-             cu(cudaEventRecord(ev_out[slot], s_out));
+        if (ok && train)
+            ok = cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + L.dq, rq, s_out)) &&
+                 cu(copy_out(dk, base + L.dk, rk, s_out)) && cu(copy_out(dv, base + L.dv, rk, s_out));
+        ok = ok && cu(cudaEventRecord(ev_out[slot], s_out));
     }
     // the caller's stream completes after the last copy back (and after the
     // input stream, so no copy outlives the call's work on its stream)
@@ -236,4 +247,24 @@ extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, cons
     if (s_in) cudaStreamDestroy(s_in);
     if (s_out) cudaStreamDestroy(s_out);
     return rc;
+}
+
+}  // namespace
+}  // namespace vsa
+
+extern "C" vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, const void *k,
+                                          const void *v, const void *dO, const void *gate, const int32_t *q_var,
+                                          const int32_t *kv_var, int topk, void *out, float *lse, void *dq,
+                                          void *dk, void *dv, void *device_buf, size_t device_bytes,
+                                          vsa_stream_t stream) {
+    return step_host(desc, groups, true, q, k, v, dO, gate, q_var, kv_var, topk, out, lse, dq, dk, dv, device_buf,
+                     device_bytes, stream);
+}
+
+extern "C" vsa_status vsa_fwd_step_host(const vsa_desc *desc, int groups, const void *q, const void *k,
+                                        const void *v, const void *gate, const int32_t *q_var, const int32_t *kv_var,
+                                        int topk, void *out, float *lse, void *device_buf, size_t device_bytes,
+                                        vsa_stream_t stream) {
+    return step_host(desc, groups, false, q, k, v, nullptr, gate, q_var, kv_var, topk, out, lse, nullptr, nullptr,
+                     nullptr, device_buf, device_bytes, stream);
 }

@@ -32,7 +32,7 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
            "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
-           "vsa_train_step_host_size", "vsa_train_step_host")
+           "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host")
 
 
 class VsaError(RuntimeError):
@@ -118,6 +118,9 @@ def lib():
         L.vsa_train_step_host.restype = C.c_int
         L.vsa_train_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P,
                                           P, C.c_size_t, P]
+        L.vsa_fwd_step_host.restype = C.c_int
+        L.vsa_fwd_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, C.c_size_t,
+                                        P]
         _lib = L
     return _lib
 
@@ -351,6 +354,26 @@ class Plan:
             C.byref(self.desc), int(groups), _p(q), _p(k), _p(v), _p(dO), _p(gate), _p(self.q_var), _p(self.kv_var),
             int(topk), _p(out), _p(lse), _p(dq), _p(dk), _p(dv), _p(buf), need, _stream(stream)))
         return out, lse, dq, dk, dv
+
+    def fwd_step_host(self, q, k, v, topk, groups, gate=None, out=None, lse=None, stream=None):
+        """vsa_fwd_step_host: block map and forward from host tensors, head
+        slices overlapped with the copies; returns host (out, lse) (out
+        allocated pinned when not given; lse only if passed in)."""
+        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk),
+                                                  int(gate is not None)))
+        if need == 0:
+            raise ValueError("invalid descriptor, groups or topk for vsa_fwd_step_host")
+        buf = getattr(self, "_host_step_buf", None)
+        if buf is None or buf.numel() < need:
+            buf = self._host_step_buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if out is None else out
+        for t in (q, k, v, gate, out, lse):
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("vsa_fwd_step_host takes contiguous host tensors")
+        _check("vsa_fwd_step_host", lib().vsa_fwd_step_host(
+            C.byref(self.desc), int(groups), _p(q), _p(k), _p(v), _p(gate), _p(self.q_var), _p(self.kv_var),
+            int(topk), _p(out), _p(lse), _p(buf), need, _stream(stream)))
+        return out, lse
 
 
 def default_scale(D: int) -> float:

@@ -320,6 +320,17 @@ vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, 
                                int topk, void *out, float *lse, void *dq, void *dk, void *dv, void *device_buf,
                                size_t device_bytes, vsa_stream_t stream);
 
+/* The same pipeline for inference: per head slice, vsa_build_block_map
+ * (need_bwd_index = 0, the inference path of [FA4-adapt]
+ * _build_sparse_tensors) and vsa_fwd (gated when gate != NULL), with q, k,
+ * v (and gate) copied in and out (required) and lse (optional) copied back.
+ * device_buf as for vsa_train_step_host (vsa_train_step_host_size covers
+ * this call too). Errors as for vsa_train_step_host; VSA_ERR_NULL also
+ * when out is NULL. */
+vsa_status vsa_fwd_step_host(const vsa_desc *desc, int groups, const void *q, const void *k, const void *v,
+                             const void *gate, const int32_t *q_var, const int32_t *kv_var, int topk, void *out,
+                             float *lse, void *device_buf, size_t device_bytes, vsa_stream_t stream);
+
 const char *vsa_status_string(vsa_status status);
 
 /* Message of the last CUDA error behind a VSA_ERR_CUDA return, with the

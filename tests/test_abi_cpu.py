@@ -107,3 +107,8 @@ def test_train_step_host_validation(L):
     assert call(nbytes=two - 1) == 7
     assert call(gate=FAKE) == 7                        # a gate needs the larger staging buffer
     assert call(dd=desc(Hq=4, Hkv=2, dtype=5)) == 2    # the slice descriptor is checked too
+    # the forward-only pipeline: out is required, the rest as above
+    fwd = lambda out=FAKE, buf=C.c_void_p(1 << 20): L.vsa_fwd_step_host(C.byref(d), 2, FAKE, FAKE, FAKE, None, FAKE,
+                                                                         FAKE, 2, out, None, buf, two, None)
+    assert fwd(out=None) == 1
+    assert fwd(buf=None) == 7

@@ -63,3 +63,28 @@ def test_host_step_equals_device_path(case):
         check_tol("host out", ref["out"], o2.double().numpy(), OUT_TOL)
         for n, x in (("dq", dq2), ("dk", dk2), ("dv", dv2)):
             check_tol(f"host {n}", ref[n], x.double().numpy(), GRAD_TOL)
+
+
+@pytest.mark.parametrize("case", [c for c in cases() if c[0].name in ("host-bshd-gqa", "host-tnd-fp16",
+                                                                      "host-gated-ragged")],
+                         ids=lambda c: c[0].name)
+def test_fwd_step_host_equals_device_forward(case):
+    """vsa_fwd_step_host (inference: block map without the KV-owned index,
+    forward) equals the device forward bit for bit."""
+    p, groups = case
+    t = make_tensors(p)
+    g = to_device(t)
+    plan = plan_for(p)
+    plan.build_block_map(g["q"], g["k"], p.topk, need_bwd_index=False)
+    gate = g.get("gate")
+    out, lse, _ = plan.forward(g["q"], g["k"], g["v"], gate=gate)
+    torch.cuda.synchronize()
+    hp = plan_for(p)
+    h_lse = torch.empty(tuple(lse.shape), dtype=torch.float32, pin_memory=True)
+    stream = torch.cuda.Stream()
+    o2, l2 = hp.fwd_step_host(host(g["q"]), host(g["k"]), host(g["v"]), p.topk, groups,
+                              gate=None if gate is None else host(gate), lse=h_lse, stream=stream)
+    stream.synchronize()
+    assert hp.device_status() == 0
+    assert torch.equal(out.cpu().view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse.cpu(), l2)
