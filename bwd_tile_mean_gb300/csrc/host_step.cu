@@ -268,3 +268,22 @@ extern "C" vsa_status vsa_fwd_step_host(const vsa_desc *desc, int groups, const 
     return step_host(desc, groups, false, q, k, v, nullptr, gate, q_var, kv_var, topk, out, lse, nullptr, nullptr,
                      nullptr, device_buf, device_bytes, stream);
 }
+
+extern "C" vsa_status vsa_step_host_status(const vsa_desc *desc, int groups, int topk, int with_gate,
+                                           void *device_buf, vsa_stream_t stream, int32_t *code) {
+    if (!device_buf || !code) return VSA_ERR_NULL;
+    vsa_desc sd;
+    int cap = 0;
+    const vsa_status st = check_groups(desc, groups, topk, &sd, &cap);
+    if (st != VSA_OK) return st;
+    const SlotLayout L = slot_layout(sd, cap, with_gate != 0);
+    *code = 0;
+    for (int slot = 0; slot < 2; ++slot) {
+        int32_t c = 0;
+        const vsa_status r =
+            vsa_device_status(static_cast<uint8_t *>(device_buf) + slot * L.bytes + L.ws, stream, &c);
+        if (r != VSA_OK && r != VSA_ERR_DEVICE) return r;
+        if (c != 0 && *code == 0) *code = c;
+    }
+    return *code ? VSA_ERR_DEVICE : VSA_OK;
+}

@@ -32,7 +32,7 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
            "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
-           "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host")
+           "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host", "vsa_step_host_status")
 
 
 class VsaError(RuntimeError):
@@ -118,6 +118,8 @@ def lib():
         L.vsa_train_step_host.restype = C.c_int
         L.vsa_train_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P,
                                           P, C.c_size_t, P]
+        L.vsa_step_host_status.restype = C.c_int
+        L.vsa_step_host_status.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, C.c_int, P, P, C.POINTER(C.c_int32)]
         L.vsa_fwd_step_host.restype = C.c_int
         L.vsa_fwd_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, C.c_size_t,
                                         P]
@@ -328,6 +330,29 @@ class Plan:
     def device_status(self, stream=None) -> int:
         return vsa_device_status(self.workspace, stream)
 
+    def _staging(self, groups, topk, gated):
+        """Zeroed device staging memory for the host-buffer steps (kept and
+        reused; its status words start at 0)."""
+        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk), int(gated)))
+        if need == 0:
+            raise ValueError("invalid descriptor, groups or topk for the host-buffer step")
+        buf = getattr(self, "_host_step_buf", None)
+        if buf is None or buf.numel() < need:
+            buf = self._host_step_buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        self._host_step_args = (int(groups), int(topk), int(gated))
+        return buf, need
+
+    def host_step_status(self, stream=None) -> int:
+        """vsa_step_host_status for the last host-buffer step: synchronises
+        and returns the first failure code of its staging slots (0 = none)."""
+        groups, topk, gated = self._host_step_args
+        code = C.c_int32(0)
+        rc = lib().vsa_step_host_status(C.byref(self.desc), groups, topk, gated, _p(self._host_step_buf),
+                                        _stream(stream), C.byref(code))
+        if rc not in (0, 9):
+            raise VsaError("vsa_step_host_status", rc)
+        return int(code.value)
+
     def train_step_host(self, q, k, v, dO, topk, groups, gate=None, out=None, lse=None, dq=None, dk=None,
                         dv=None, stream=None):
         """vsa_train_step_host: one step (block map, forward, backward; with
@@ -337,13 +362,7 @@ class Plan:
         `stream` is left ordered after the last copy back, so synchronise it
         before reading them. Returns (out, lse, dq, dk, dv); out / lse only
         if passed in."""
-        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk),
-                                                  int(gate is not None)))
-        if need == 0:
-            raise ValueError("invalid descriptor, groups or topk for vsa_train_step_host")
-        buf = getattr(self, "_host_step_buf", None)
-        if buf is None or buf.numel() < need:
-            buf = self._host_step_buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+        buf, need = self._staging(groups, topk, gate is not None)
         dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if dq is None else dq
         dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True) if dk is None else dk
         dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True) if dv is None else dv
@@ -359,13 +378,7 @@ class Plan:
         """vsa_fwd_step_host: block map and forward from host tensors, head
         slices overlapped with the copies; returns host (out, lse) (out
         allocated pinned when not given; lse only if passed in)."""
-        need = int(lib().vsa_train_step_host_size(C.byref(self.desc), int(groups), int(topk),
-                                                  int(gate is not None)))
-        if need == 0:
-            raise ValueError("invalid descriptor, groups or topk for vsa_fwd_step_host")
-        buf = getattr(self, "_host_step_buf", None)
-        if buf is None or buf.numel() < need:
-            buf = self._host_step_buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+        buf, need = self._staging(groups, topk, gate is not None)
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if out is None else out
         for t in (q, k, v, gate, out, lse):
             if t is not None and (t.is_cuda or not t.is_contiguous()):

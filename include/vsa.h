@@ -300,7 +300,8 @@ vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int 
  *                  [Hq, T_q]); either may be NULL (then not copied back);
  *   dq, dk, dv:    host gradients, shaped like q, k, v;
  *   q_var, kv_var, desc->cu_seqlens_*: device, as for the other calls;
- *   device_buf:    device staging memory, 256-byte aligned, at least
+ *   device_buf:    device staging memory (zeroed before its first use,
+ *                  see vsa_step_host_status), 256-byte aligned, at least
  *                  vsa_train_step_host_size(desc, groups, topk,
  *                  gate != NULL) bytes (two slots of one slice's tensors,
  *                  indices, LSE and workspace), owned by the caller.
@@ -330,6 +331,18 @@ vsa_status vsa_train_step_host(const vsa_desc *desc, int groups, const void *q, 
 vsa_status vsa_fwd_step_host(const vsa_desc *desc, int groups, const void *q, const void *k, const void *v,
                              const void *gate, const int32_t *q_var, const int32_t *kv_var, int topk, void *out,
                              float *lse, void *device_buf, size_t device_bytes, vsa_stream_t stream);
+
+/* Failures inside the two host-buffer steps: the kernels of each head slice
+ * record a timed-out internal wait in the status word of their staging
+ * slot's workspace (as vsa_device_status describes for a caller's
+ * workspace). This call synchronises `stream`, reads and clears both
+ * slots' words in device_buf (desc, groups, topk and with_gate as in the
+ * step's call) and sets *code to the first nonzero one (0 = no failure);
+ * it returns VSA_ERR_DEVICE when *code != 0. The words are only ever set,
+ * from 0, by a failing wait, so device_buf must be zeroed once before its
+ * first use. */
+vsa_status vsa_step_host_status(const vsa_desc *desc, int groups, int topk, int with_gate, void *device_buf,
+                                vsa_stream_t stream, int32_t *code);
 
 const char *vsa_status_string(vsa_status status);
 

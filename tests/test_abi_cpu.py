@@ -112,3 +112,7 @@ def test_train_step_host_validation(L):
                                                                          FAKE, 2, out, None, buf, two, None)
     assert fwd(out=None) == 1
     assert fwd(buf=None) == 7
+    # reading the staging slots' status words: arguments checked on the host
+    code = C.c_int32(0)
+    assert L.vsa_step_host_status(C.byref(d), 2, 2, 0, None, None, C.byref(code)) == 1
+    assert L.vsa_step_host_status(C.byref(d), 3, 2, 0, FAKE, None, C.byref(code)) == 2

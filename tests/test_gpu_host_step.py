@@ -53,7 +53,7 @@ def test_host_step_equals_device_path(case):
                                                groups, gate=None if gate is None else host(gate), out=h_out,
                                                lse=h_lse, stream=stream)
     stream.synchronize()
-    assert hp.device_status() == 0
+    assert hp.host_step_status(stream) == 0
     for name, a, b in (("out", out, o2), ("dq", dq, dq2), ("dk", dk, dk2), ("dv", dv, dv2)):
         assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16)), name
     assert torch.equal(lse.cpu(), l2)
@@ -85,6 +85,6 @@ def test_fwd_step_host_equals_device_forward(case):
     o2, l2 = hp.fwd_step_host(host(g["q"]), host(g["k"]), host(g["v"]), p.topk, groups,
                               gate=None if gate is None else host(gate), lse=h_lse, stream=stream)
     stream.synchronize()
-    assert hp.device_status() == 0
+    assert hp.host_step_status(stream) == 0
     assert torch.equal(out.cpu().view(torch.int16), o2.view(torch.int16))
     assert torch.equal(lse.cpu(), l2)
