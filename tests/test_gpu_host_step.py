@@ -18,7 +18,7 @@ def cases():
     return [
         (Problem("host-bshd-gqa", "bshd", 2, 8, 4, 128, 256, 256, 3, 5, q_var=[256, 256, 200],
                  kv_var=[256, 77, 256, 0, 256], topk=3, seed=71), 2),
-        (Problem("host-bhsd", "bhsd", 1, 6, 6, 128, 128, 256, 4, 3, q_var=[128] * 4, kv_var=[256, 130, 9],
+        (Problem("host-bhsd", "bhsd", 2, 6, 6, 128, 128, 256, 4, 3, q_var=[128] * 4, kv_var=[256, 130, 9],
                  topk=2, seed=72), 3),
         (Problem("host-tnd-fp16", "tnd", 3, 4, 2, 128, 256, 128, 3, 5, dtype="fp16", q_lens=[300, 17, 513],
                  kv_lens=[540, 23, 200], topk=3, seed=73), 2),

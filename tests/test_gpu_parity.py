@@ -94,6 +94,25 @@ def make_ties(p, t):
     return t
 
 
+def test_block_map_many_kv_tiles_bit_exact():
+    """2,600 KV tiles (past the point where the selection kernel keeps one
+    query tile per warp to fit shared memory; 21 staging chunks), topk 100."""
+    nkv = 2600
+    kv_var = [128] * nkv
+    kv_var[5], kv_var[1000], kv_var[2599] = 0, 17, 1
+    p = Problem("many-kv", "bshd", 1, 2, 1, 128, 128, 128, 4, nkv, q_var=[128] * 4, kv_var=kv_var, topk=100, seed=33)
+    t = make_tensors(p)
+    plan, _ = run_map(p, t)
+    m, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    kp, kq = orc.transpose(p, qi, qc, p.cap)
+    torch.cuda.synchronize()
+    assert np.array_equal(plan.block_map.cpu().numpy(), m)
+    assert np.array_equal(plan.q_cnt.cpu().numpy(), qc)
+    assert np.array_equal(plan.q_idx.cpu().numpy(), qi)
+    assert np.array_equal(plan.kv_ptr.cpu().numpy(), kp)
+    assert np.array_equal(plan.kv_qidx.cpu().numpy(), kq)
+
+
 @pytest.mark.parametrize("p", tie_cases(), ids=lambda p: p.name)
 def test_block_map_ties_bit_exact(p):
     t = make_ties(p, make_tensors(p))
