@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ 
 
 // ----------------------------------------------------------- MMA helpers
 // Measured on GB300 (all SMs busy, M = 128, K = 16 per instruction): an
-// MMA with N = 64 takes about as long as one with N = 128, so every MMA
-// here uses N = 128 (A and B from shared memory, or A from TMEM).
+// MMA with N = 128 takes 64 cycles with A from shared memory or from TMEM;
+// N = 64 takes 45-48, ~70% of the N = 128 rate per FLOP. The dQ pass uses
+// N = 128 throughout; the dK/dV pass's 64-row items make its S^T and dP^T
+// MMAs N = 64 (the price of two TMEM buffers for them).
 
 // D = A B^T, A and B [128 x 128] K-major 128-byte-swizzled tiles (two
 // 64-column boxes 16 KB apart); 8 MMAs of K = 16.

@@ -92,13 +92,6 @@ cudaError_t launch_pools(const Prob &p, const PoolSegs &segs_in, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s) {
-    PoolSegs segs{};
-    segs.n = 1;
-    segs.s[0] = PoolSeg{x, out, q_side ? 1 : 0, 0};
-    return launch_pools(p, segs, s);
-}
-
 cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
                             float *pv, cudaStream_t s) {
     PoolSegs segs{};

@@ -30,7 +30,6 @@ struct PoolSegs {
     int n;
 };
 cudaError_t launch_pools(const Prob &p, const PoolSegs &segs, cudaStream_t s);
-cudaError_t launch_pool(const Prob &p, bool q_side, const void *x, float *out, cudaStream_t s);
 // q and k (v == NULL) or q, k and v in one launch.
 cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
                             float *pv, cudaStream_t s);
