@@ -280,14 +280,15 @@ vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int 
 
 /* One training step (block map, forward, backward; with gate != NULL also
  * the gated compression branch) from HOST buffers, with the copies
- * overlapped with the kernels. Every
- * head is an independent problem (the per-(batch, head) loops of
- * [NPU-test]'s TND/GQA golden), so the heads are cut into `groups` slices
- * of Hq/groups query and Hkv/groups key/value heads (Hkv % groups == 0;
- * GQA groups stay whole). Slice g's q, k, v, dO are copied host -> device
- * (strided 2D copies into a compact staging slot) on an internal stream
- * while slice g-1 computes on `stream` and slice g-2's results are copied
- * device -> host on a second internal stream; two staging slots alternate.
+ * overlapped with the kernels. Every head is an independent problem (the
+ * per-(batch, head) loops of [NPU-test]'s TND/GQA golden), so the heads are
+ * cut into `groups` slices of Hq/groups query and Hkv/groups key/value
+ * heads (Hkv % groups == 0; GQA groups stay whole). Slice g's inputs are
+ * copied host -> device (strided 2D copies into a compact staging slot) on
+ * an internal stream while earlier slices compute on `stream`, and each
+ * slice's results are copied device -> host on a second internal stream as
+ * soon as they are final (O and LSE after the forward, the gradients after
+ * the backward); two staging slots alternate.
  * Each slice runs vsa_build_block_map (topk, with the KV-owned index),
  * vsa_fwd and vsa_bwd on its own descriptor, so every output is
  * bit-identical to those calls on the whole problem.
