@@ -332,6 +332,37 @@ def _bwd(p, t, qi, qc, cap, gate=None):
 
 
 @pytest.mark.parametrize("layout,Hkv", [("bhsd", 2), ("bshd", 1)])
+def test_rowsum_do_o_equals_sum_p_dp(layout, Hkv):
+    """The identity behind the backward preprocess: with O_t = sum_u P_tu v_u,
+    dO_t . O_t = sum_u P_tu (dO_t . v_u). The left side uses the oracle's O,
+    the right side its LSE through P_tu = exp(scale q_t . k_u - LSE_t) over
+    the allowed keys, computed here in fp64 -- so the oracle's two forward
+    outputs are checked against each other (an empty tile and partial tiles
+    included)."""
+    p = small(layout, kv_var=(256, 173, 0, 79, 256), q_var=(256, 61, 199), topk=3, Hkv=Hkv)
+    t = make_tensors(p)
+    qi, qc, cap, (_, osp, lse) = _fwd(p, t)
+    q, k, v, dO = (to_bhsd(p, _np(t[n]), n in ("q", "dO")).numpy() for n in ("q", "k", "v", "dO"))
+    g = p.Hq // p.Hkv
+    rows = p.rows()
+    checked = 0
+    for b in range(p.B):
+        for h in range(p.Hq):
+            sel = (rows[:, 0] == b) & (rows[:, 1] == h)
+            s_idx = rows[sel, 2]
+            m = key_mask(p, qi, qc, b, h).numpy()[s_idx]            # [rows, Skv]
+            S = p.scale * q[b, h, s_idx] @ k[b, h // g].T
+            L = lse[sel][:, None]
+            P = np.where(m, np.exp(np.where(m, S, 0.0) - np.where(np.isfinite(L), L, 0.0)), 0.0)
+            dP = dO[b, h, s_idx] @ v[b, h // g].T
+            rhs = (P * dP).sum(axis=1)
+            lhs = (dO[b, h, s_idx] * osp[sel]).sum(axis=1)
+            np.testing.assert_allclose(lhs, rhs, rtol=1e-9, atol=1e-12)
+            checked += len(s_idx)
+    assert checked == len(rows)
+
+
+@pytest.mark.parametrize("layout,Hkv", [("bhsd", 2), ("bshd", 1)])
 def test_sparse_grads_equal_torch_autograd(layout, Hkv):
     p = small(layout, kv_var=(256, 173, 79, 256), q_var=(256, 61, 199), topk=2, Hkv=Hkv)
     t = make_tensors(p)
