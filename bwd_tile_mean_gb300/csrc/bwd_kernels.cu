@@ -41,75 +41,79 @@ constexpr int kProdWarp = 8, kMmaWarp = 9;
 // nlse2[w] = -LSE * log2(e) and ndvec[w] = -sum_d dO_d O_d (minus
 // rowsum(P dP) of the softmax backward); both are stored negated so the
 // consumers add them. Slots that are not query rows (past a varlen
-// sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there. A half-warp
-// reads one 256-byte row (16 bytes per lane); a warp takes 8 rows, all
-// loads issued before the first use. Rows are visited in memory order of dO
-// and O (the heads of a token are adjacent in BSHD and TND, the tokens of a
-// head in BHSD), so consecutive warps stream contiguous memory. Row indices
-// fit in 32 bits (the host checks), which keeps the index arithmetic short.
-constexpr int kPrepIt = 4;  // row pairs per warp
-
-// Batch entry, token and head of the prep row with memory-order index w.
-__device__ __forceinline__ void prep_row(const Prob &p, int per, int w, int &b, int &s, int &h) {
-    const int bs = per * p.Hq;
-    b = w / bs;
-    const int rem = w - b * bs;
-    if (p.layout == L_BHSD) {
-        h = rem / per;
-        s = rem - h * per;
-    } else {
-        s = rem / p.Hq;
-        h = rem - s * p.Hq;
-    }
-}
+// sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there.
+// A warp takes 32 consecutive slots of one (b, h): each half-warp reads a
+// 256-byte row of dO and of O (16 bytes per lane), 16 rows in flight per
+// lane, reduces it, and the 32 row sums gather into lane r, so the LSE read
+// and both writes are one coalesced 128-byte access each. Warps visit the
+// 32-row groups in memory order of dO and O (heads of a token adjacent in
+// BSHD and TND, tokens of a head in BHSD) in a grid-stride loop sized to
+// the GPU.
+constexpr int kPrepRows = 32;  // slots per warp task
 
 template <typename T>
-__global__ void __launch_bounds__(256) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
+__global__ void __launch_bounds__(256, 2) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
                                                   const float *__restrict__ lse, float *__restrict__ nlse2,
-                                                  float *__restrict__ ndvec) {
+                                                  float *__restrict__ ndvec, int ntasks) {
     const int per = p.nQ * p.tile_q;
-    const int slots = p.B * p.Hq * per;
-    const int half = (threadIdx.x >> 4) & 1, hl = threadIdx.x & 15;
-    const int wbase = (blockIdx.x * 8 + (threadIdx.x >> 5)) * (2 * kPrepIt);
-    uint4 av[kPrepIt], cv[kPrepIt];
+    const int groups = per / kPrepRows;
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const int nwarps = gridDim.x * (blockDim.x >> 5);
+    for (int task = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks; task += nwarps) {
+        int b, h, g;
+        if (p.layout == L_BHSD) {
+            g = task % groups;
+            const int bh = task / groups;
+            h = bh % p.Hq;
+            b = bh / p.Hq;
+        } else {
+            h = task % p.Hq;
+            const int bg = task / p.Hq;
+            g = bg % groups;
+            b = bg / groups;
+        }
+        const int s0 = g * kPrepRows;
+        const int len = p.layout == L_TND ? seq_len(p, true, b) : per;
+        float mine = 0.f;  // dO . O of slot s0 + lane
 #pragma unroll
-    for (int it = 0; it < kPrepIt; ++it) {
-        const int w = wbase + it * 2 + half;
-        av[it] = make_uint4(0, 0, 0, 0);
-        cv[it] = make_uint4(0, 0, 0, 0);
-        if (w < slots) {
-            int b, s, h;
-            prep_row(p, per, w, b, s, h);
-            if (p.layout != L_TND || s < p.cu_q[b + 1] - p.cu_q[b]) {
-                const long long o = tok_off(p, true, b, s, h) + hl * 8;
-                av[it] = __ldg(reinterpret_cast<const uint4 *>(dO + o));
-                cv[it] = __ldg(reinterpret_cast<const uint4 *>(O + o));
+        for (int batch = 0; batch < 2; ++batch) {
+            uint4 av[8], cv[8];
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int s = s0 + batch * 16 + it * 2 + half;
+                av[it] = make_uint4(0, 0, 0, 0);
+                cv[it] = make_uint4(0, 0, 0, 0);
+                if (s < len) {
+                    const long long o = tok_off(p, true, b, s, h) + hl * 8;
+                    av[it] = __ldg(reinterpret_cast<const uint4 *>(dO + o));
+                    cv[it] = __ldg(reinterpret_cast<const uint4 *>(O + o));
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
+                const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
+                float acc = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 x = unpack2<T>(aw[u]), y = unpack2<T>(cw[u]);
+                    acc = fmaf(x.x, y.x, acc);
+                    acc = fmaf(x.y, y.y, acc);
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                const int r0 = batch * 16 + it * 2;  // half 0 summed row r0, half 1 row r0 + 1
+                const float v0 = __shfl_sync(0xffffffffu, acc, 0), v1 = __shfl_sync(0xffffffffu, acc, 16);
+                if (lane == r0) mine = v0;
+                if (lane == r0 + 1) mine = v1;
             }
         }
-    }
-#pragma unroll
-    for (int it = 0; it < kPrepIt; ++it) {
-        const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
-        const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 x = unpack2<T>(aw[u]), y = unpack2<T>(cw[u]);
-            acc = fmaf(x.x, y.x, acc);
-            acc = fmaf(x.y, y.y, acc);
-        }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        const int w = wbase + it * 2 + half;
-        if (hl == 0 && w < slots) {
-            int b, s, h;
-            prep_row(p, per, w, b, s, h);
-            const bool ex = p.layout != L_TND || s < p.cu_q[b + 1] - p.cu_q[b];
-            const long long slot = ((long long)b * p.Hq + h) * per + s;
-            ndvec[slot] = ex ? -acc : 0.f;
-            const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
-            nlse2[slot] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
-        }
+        const int s = s0 + lane;
+        const bool ex = s < len;
+        const long long slot = ((long long)b * p.Hq + h) * per + s;
+        ndvec[slot] = ex ? -mine : 0.f;
+        const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
+        nlse2[slot] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
     }
 }
 
@@ -192,15 +196,28 @@ struct WorkIter {
     int h, pos, end, sub, i, nsub;
 };
 
+// The KV-owned list of tile j for query head h: entries [pos, end) of
+// kv_qidx. Offsets are clamped into [0, nQ * cap] with end >= pos and
+// entries into [0, nQ), so a corrupt index (invalid input, reported by
+// vsa_check_inputs) cannot move a read or a load outside its buffer.
+__device__ __forceinline__ void kv_list(const Prob &p, const BwdArgs &a, int b, int h, int j, int &pos,
+                                        int &end) {
+    const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
+    const int cap_all = p.nQ * a.cap;
+    pos = clampi(ptr[j], 0, cap_all);
+    end = clampi(ptr[j + 1], pos, cap_all);
+}
+__device__ __forceinline__ int kv_entry(const Prob &p, const BwdArgs &a, int b, int h, int pos) {
+    return clampi(a.kv_qidx[((long long)b * p.Hq + h) * p.nQ * a.cap + pos], 0, p.nQ - 1);
+}
+
 __device__ __forceinline__ bool work_next_list(const Prob &p, const BwdArgs &a, int b, int h_end, int j,
                                                WorkIter &w) {
     while (w.pos >= w.end) {
         if (++w.h >= h_end) return false;
-        const int *ptr = a.kv_ptr + ((long long)b * p.Hq + w.h) * (p.nKV + 1);
-        w.pos = ptr[j];
-        w.end = ptr[j + 1];
+        kv_list(p, a, b, w.h, j, w.pos, w.end);
     }
-    w.i = a.kv_qidx[((long long)b * p.Hq + w.h) * p.nQ * a.cap + w.pos];
+    w.i = kv_entry(p, a, b, w.h, w.pos);
     w.nsub = (q_rows(p, b, w.i) + kDkItem - 1) / kDkItem;
     w.sub = 0;
     return true;
@@ -208,9 +225,7 @@ __device__ __forceinline__ bool work_next_list(const Prob &p, const BwdArgs &a, 
 __device__ __forceinline__ bool work_first(const Prob &p, const BwdArgs &a, int b, int h0, int h_end, int j,
                                            WorkIter &w) {
     w.h = h0;
-    const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h0) * (p.nKV + 1);
-    w.pos = ptr[j];
-    w.end = ptr[j + 1];
+    kv_list(p, a, b, h0, j, w.pos, w.end);
     return work_next_list(p, a, b, h_end, j, w);
 }
 __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, int b, int h_end, int j,
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     kvalid = kvalid < 0 ? 0 : (kvalid > 128 ? 128 : kvalid);
     const int key0 = j * p.tile_kv + ck * 128;  // within the batch entry
     if (p.layout == L_TND && kvalid == 0) return;  // keys outside the sequence do not exist
-    const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0), qb = (p.layout == L_TND ? p.cu_q[b] : 0);
+    const int kvb = (p.layout == L_TND ? seq_start(p, false, b) : 0), qb = (p.layout == L_TND ? seq_start(p, true, b) : 0);
     const int bc = (p.layout == L_TND ? 0 : b);
 
     if (threadIdx.x == 0) {
@@ -271,13 +286,13 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         int n = 0;
         if (kvalid > 0)
             for (int h = h0; h < h_end; ++h) {
-                const int *ptr = a.kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
+                int pos, end;
+                kv_list(p, a, b, h, j, pos, end);
                 if (p.layout != L_TND) {  // every query tile has tile_q rows
-                    n += (ptr[j + 1] - ptr[j]) * (p.tile_q / kDkItem);
+                    n += (end - pos) * (p.tile_q / kDkItem);
                     continue;
                 }
-                const int *lst = a.kv_qidx + ((long long)b * p.Hq + h) * p.nQ * a.cap;
-                for (int q = ptr[j]; q < ptr[j + 1]; ++q) n += (q_rows(p, b, lst[q]) + kDkItem - 1) / kDkItem;
+                for (int q = pos; q < end; ++q) n += (q_rows(p, b, kv_entry(p, a, b, h, q)) + kDkItem - 1) / kDkItem;
             }
         *s_nwork = n;
         fence_mbar_init();
@@ -525,7 +540,8 @@ struct ChunkWin {
 __device__ __forceinline__ void win_load(const Prob &p, int b, ChunkWin &w, int lane) {
     const int n = w.n0 + lane;
     w.j = n < w.cnt ? w.idx[n] : 0;
-    w.kvv = n < w.cnt ? kv_valid(p, b, w.j) : 0;
+    // tile ids outside [0, nKV) (invalid input) contribute no chunk
+    w.kvv = (n < w.cnt && w.j >= 0 && w.j < p.nKV) ? kv_valid(p, b, w.j) : 0;
     w.bits = (n < w.cnt && w.sub) ? w.sub[n] : -1;
     w.nch = min(w.per, (w.kvv + 127) >> 7);
     int inc = w.nch;
@@ -542,7 +558,7 @@ __device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *i
     ChunkWin w;
     w.idx = idx;
     w.sub = sub;
-    w.cnt = cnt;
+    w.cnt = cnt;  // already clamped into [0, idx_cap] by the caller
     w.per = p.tile_kv >> 7;
     w.n0 = 0;
     w.c0 = 0;
@@ -600,12 +616,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row0 = i * p.tile_q + half * 128;
     int nrows = 128;
     if (p.layout == L_TND) {
-        nrows = (p.cu_q[b + 1] - p.cu_q[b]) - row0;
+        nrows = seq_len(p, true, b) - row0;
         if (nrows <= 0) return;
         nrows = nrows > 128 ? 128 : nrows;
     }
-    const int qrc = (p.layout == L_TND ? p.cu_q[b] : 0) + row0;
-    const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0);
+    const int qrc = (p.layout == L_TND ? seq_start(p, true, b) : 0) + row0;
+    const int kvb = (p.layout == L_TND ? seq_start(p, false, b) : 0);
     const int bc = (p.layout == L_TND ? 0 : b);
     const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
 
@@ -630,12 +646,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         fence_mbar_init();
     }
     if (warp == kProdWarp) {
-        // number of 128-key chunks with valid keys
-        const int cnt = a.q_cnt[qrow];
+        // number of 128-key chunks with valid keys (counts clamped to
+        // idx_cap, tile ids outside [0, nKV) skipped, as in win_load)
+        const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);
         const int *idx = a.q_idx + qrow * a.cap;
         const int per = p.tile_kv >> 7;
         int total = 0;
-        for (int n = lane; n < cnt; n += 32) total += min(per, (kv_valid(p, b, idx[n]) + 127) >> 7);
+        for (int n = lane; n < cnt; n += 32) {
+            const int j = idx[n];
+            total += (j >= 0 && j < p.nKV) ? min(per, (kv_valid(p, b, j) + 127) >> 7) : 0;
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
@@ -653,7 +673,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (warp == kProdWarp && N > 0) {
         // ------------------------------------ TMA producer (whole warp, lane 0 issues)
-        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, a.q_cnt[qrow], lane);
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, clampi(a.q_cnt[qrow], 0, a.cap), lane);
         if (lane == 0) {
             mbar_expect_tx(b_q, 2 * kTile);
             tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
@@ -738,7 +758,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const float ndv = N > 0 ? a.ndvec[slot] : 0.f;
         bool ok = true;
         ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_sub ? a.q_sub + qrow * a.cap : nullptr,
-                                a.q_cnt[qrow], lane);
+                                clampi(a.q_cnt[qrow], 0, a.cap), lane);
         for (int c = 0; c < N; ++c) {
             int crow = 0, cval = 0, cbits = -1;
             win_chunk(p, b, cw, c, lane, crow, cval, cbits);
@@ -994,7 +1014,7 @@ __global__ void __launch_bounds__(256) k_gate_grad(Prob p, const T *__restrict__
         const int b = (int)(u / per_b);
         const long long rem = u - (long long)b * per_b;
         const int s = (int)(rem / p.Hq), h = (int)(rem % p.Hq);
-        if (p.layout == L_TND && s >= p.cu_q[b + 1] - p.cu_q[b]) continue;
+        if (p.layout == L_TND && s >= seq_len(p, true, b)) continue;
         const long long o = tok_off(p, true, b, s, h) + sub * 8;
         const float *cc = c + (((long long)b * p.Hq + h) * p.nQ + s / p.tile_q) * 128 + sub * 8;
         const uint4 g = *reinterpret_cast<const uint4 *>(dO + o);
@@ -1031,14 +1051,20 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
                             float *ndvec, cudaStream_t s) {
     const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;
     if (slots == 0) return cudaSuccess;
-    if (slots > (long long)INT_MAX - 2 * 8 * 2 * kPrepIt) return cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)((slots + 8 * 2 * kPrepIt - 1) / (8 * 2 * kPrepIt));
+    if (slots > (long long)INT_MAX) return cudaErrorInvalidValue;
+    const int ntasks = (int)(slots / kPrepRows);  // tile_q is a multiple of 32
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int want = (ntasks + 7) / 8;
+    const int blocks = want < sms * 2 ? want : sms * 2;  // every block resident (two per SM)
     prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
         k_bwd_prep<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)o,
-                                                        lse, nlse2, ndvec);
+                                                        lse, nlse2, ndvec, ntasks);
     else
-        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, nlse2, ndvec);
+        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, nlse2, ndvec,
+                                                 ntasks);
     prof_end(s);
     return cudaGetLastError();
 }
@@ -1049,12 +1075,9 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
         !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, kDkItem))
         return cudaErrorInvalidValue;
     dim3 grid(p.nKV * (p.tile_kv / 128), p.Hkv, p.B);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_dkdv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem);
-        cudaFuncSetAttribute(k_dkdv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem);
-        attr = true;
-    }
+    const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_dkdv<__nv_bfloat16>, (int)kDkSmem)
+                                             : ensure_smem_limit((const void *)k_dkdv<__half>, (int)kDkSmem);
+    if (ae != cudaSuccess) return ae;
     prof_begin("bwd_dkdv", s);
     if (p.dtype == T_BF16)
         k_dkdv<__nv_bfloat16><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
@@ -1070,12 +1093,9 @@ cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
         !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
         return cudaErrorInvalidValue;
     dim3 grid(p.nQ * (p.tile_q / 128), p.Hq, p.B);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_dq<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem);
-        cudaFuncSetAttribute(k_dq<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem);
-        attr = true;
-    }
+    const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_dq<__nv_bfloat16>, (int)kDqSmem)
+                                             : ensure_smem_limit((const void *)k_dq<__half>, (int)kDqSmem);
+    if (ae != cudaSuccess) return ae;
     prof_begin("bwd_dq", s);
     if (p.dtype == T_BF16)
         k_dq<__nv_bfloat16><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);

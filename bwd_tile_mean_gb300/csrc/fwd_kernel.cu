@@ -23,13 +23,15 @@
 // Per chunk c the MMAs go S_A(c) = Q_A K_c^T, O_B += P_B(c-1) V_(c-1),
 // S_B(c) = Q_B K_c^T, O_A += P_A(c) V_c, so each group's softmax runs while
 // the tensor core works for the other group. The softmax loads a whole row
-// of S (128 scores) from TMEM with one wait, takes its max, and computes
-// probabilities in the exp2 domain against the running max (keys past the
+// of S (128 scores) from TMEM with one wait and computes probabilities in
+// the exp2 domain against the row's running reference (keys past the
 // chunk's valid count masked; scale-and-subtract and the row sum on paired
-// f32 instructions); only rows whose max grows by more than 2^8 (always the
-// first chunk) move the running max and rescale l and O in TMEM. P goes back
-// into the first 64 columns of the S buffer as packed 16-bit pairs; the PV
-// MMA reads it as its A operand. The epilogue normalises O, adds gate * c
+// f32 instructions). The row max is taken only on the first chunk and when
+// a chunk's row sum shows that an element grew past the 16-bit operand's
+// safe range; only then does the reference move (when the max is more than
+// 2^8 above it) and l and O get rescaled in TMEM. P goes back into the first
+// 64 columns of the S buffer as packed 16-bit pairs; the PV MMA reads it as
+// its A operand. The epilogue normalises O, adds gate * c
 // when gated, and writes O and the LSE.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "sm103_ptx.cuh"
@@ -73,6 +75,41 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t a
         mma_f16_ts_w(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
+// Bound on a row's chunk sum of probabilities that keeps every element a
+// finite 16-bit operand of the PV MMA: bf16 shares fp32's exponent range,
+// fp16 ends at 65504.
+template <typename T> struct SumLimit;
+template <> struct SumLimit<__nv_bfloat16> { static constexpr float value = 0x1p64f; };
+template <> struct SumLimit<__half> { static constexpr float value = 0x1p15f; };
+
+// P = exp2(scale log2e s - m) for the 128 scores of one row, packed to
+// 16-bit pairs into the 64 TMEM columns at taddr; returns the fp32 row sum
+// (scale-and-subtract and the sum on paired f32 instructions).
+template <typename T>
+__device__ __forceinline__ float exp_row(const uint32_t (&sr)[128], float m, float sl2, uint32_t taddr) {
+    const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m, -m);
+    uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t w16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int e = q4 * 32 + 2 * j;
+            const float2 x =
+                f32x2_split(ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nm2));
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            if (j & 1)
+                acc1 = fadd_x2(acc1, f32x2(p0, p1));
+            else
+                acc0 = fadd_x2(acc0, f32x2(p0, p1));
+            w16[j] = pack2<T>(p0, p1);
+        }
+        tmem_st16(taddr + q4 * 16, w16);
+    }
+    const float2 s0 = f32x2_split(acc0), s1 = f32x2_split(acc1);
+    return (s0.x + s0.y) + (s1.x + s1.y);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -102,15 +139,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int r0 = i * p.tile_q + g * 128;
         int n = (g * 128 < p.tile_q) ? 128 : 0;
         if (p.layout == L_TND && n > 0) {
-            n = (p.cu_q[b + 1] - p.cu_q[b]) - r0;
+            n = seq_len(p, true, b) - r0;
             n = n < 0 ? 0 : (n > 128 ? 128 : n);
         }
         nrows[g] = n;
     }
     if (nrows[0] == 0) return;  // the whole tile lies outside its sequence
     const bool has_b = nrows[1] > 0;
-    const int qbase = (p.layout == L_TND ? p.cu_q[b] : 0) + i * p.tile_q;
-    const int kvb = (p.layout == L_TND ? p.cu_kv[b] : 0);
+    const int qbase = (p.layout == L_TND ? seq_start(p, true, b) : 0) + i * p.tile_q;
+    const int kvb = (p.layout == L_TND ? seq_start(p, false, b) : 0);
     const int bc = (p.layout == L_TND ? 0 : b);
     const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
 
@@ -130,8 +167,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_mbar_init();
     }
     if (warp == kFwdProdWarp) {
-        // chunk list: (KV row start within the batch entry, valid keys)
-        const int cnt = a.q_cnt[qrow];
+        // chunk list: (KV row start within the batch entry, valid keys);
+        // counts above idx_cap and tile ids outside [0, nKV) (invalid input,
+        // reported by vsa_check_inputs) are clamped or skipped here
+        const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);
         const int *idx = a.q_idx + qrow * a.cap;
         const int per = p.tile_kv >> 7;
         int total = 0;
@@ -140,7 +179,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             int j = 0, kvv = 0, nc = 0, bits = -1;
             if (n < cnt) {
                 j = idx[n];
-                kvv = kv_valid(p, b, j);
+                kvv = (j >= 0 && j < p.nKV) ? kv_valid(p, b, j) : 0;
                 nc = min(per, (kvv + 127) >> 7);
                 if (a.q_sub) bits = a.q_sub[qrow * a.cap + n];
             }
@@ -260,11 +299,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // query blocks: a row whose block did not select this tile sees no key of it
             if (a.q_sub && !((s_csub[c] >> ((g * 128 + r) / a.block_q)) & 1)) valid = 0;
             // The whole row of S (128 scores) comes into registers with one
-            // wait; its max is taken first (the scale is positive, so on raw
-            // scores). A row whose max exceeds the running max by more than
-            // 2^8 (always the first chunk) raises it and rescales l and O;
-            // otherwise probabilities stay relative to the running max. P
-            // goes, packed, to the first 64 columns of the S buffer.
+            // wait. Probabilities are exp2(scale log2e s - m_ref) against the
+            // row's running reference m_ref, packed into the first 64 columns
+            // of the S buffer. Once the row has a reference, the chunk goes
+            // straight to the exponentials: fp32 and the 16-bit P keep their
+            // relative precision at any magnitude, so m_ref only has to keep
+            // P finite, and a row sum within kSumLimit bounds every element.
+            // The first chunk, and a chunk whose sum passes the limit, take
+            // the row max first (the scale is positive, so on raw scores) and
+            // move m_ref to it when it is more than 2^8 above (rescaling l and
+            // O in TMEM), then redo the exponentials.
             uint32_t sr[128];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tl + cS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + q4 * 32));
@@ -275,49 +319,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int j = 0; j < 128; ++j)
                     if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
             }
-            float mx;
-            {
-                float u[43], v[15], w5[5];
-#pragma unroll
-                for (int k = 0; k < 42; ++k)
-                    u[k] = fmax3(__uint_as_float(sr[3 * k]), __uint_as_float(sr[3 * k + 1]), __uint_as_float(sr[3 * k + 2]));
-                u[42] = fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127]));
-#pragma unroll
-                for (int k = 0; k < 14; ++k) v[k] = fmax3(u[3 * k], u[3 * k + 1], u[3 * k + 2]);
-                v[14] = u[42];
-#pragma unroll
-                for (int k = 0; k < 5; ++k) w5[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
-                mx = fmaxf(fmax3(w5[0], w5[1], w5[2]), fmaxf(w5[3], w5[4])) * sl2;
+            float ls = 0.f, alpha = 1.f;
+            bool slow = m_ref == -INFINITY;
+            if (!__any_sync(0xffffffffu, slow)) {
+                ls = exp_row<T>(sr, m_ref, sl2, tl + cS);
+                slow = !(ls <= SumLimit<T>::value);  // also true for inf / nan
+                if (__any_sync(0xffffffffu, slow)) tmem_wait_st();  // the redo below overwrites these stores
             }
-            float alpha = 1.f;
-            if (mx > m_ref + 8.f) {
-                alpha = ex2(m_ref - mx);  // 0 on the first chunk
-                m_ref = mx;
-            }
-            // (a row that has seen no key yet keeps m_ref = -inf; its scores
-            // are all -inf and must give P = 0, not inf - inf)
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_use, -m_use);
-            uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+            if (__any_sync(0xffffffffu, slow)) {
+                float mx;
+                {
+                    float u[43], v[15], w5[5];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t w16[16];
+                    for (int k = 0; k < 42; ++k)
+                        u[k] = fmax3(__uint_as_float(sr[3 * k]), __uint_as_float(sr[3 * k + 1]),
+                                     __uint_as_float(sr[3 * k + 2]));
+                    u[42] = fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127]));
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int e = q4 * 32 + 2 * j;
-                    const float2 x = f32x2_split(
-                        ffma_x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nm2));
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    if (j & 1)
-                        acc1 = fadd_x2(acc1, f32x2(p0, p1));
-                    else
-                        acc0 = fadd_x2(acc0, f32x2(p0, p1));
-                    w16[j] = pack2<T>(p0, p1);
+                    for (int k = 0; k < 14; ++k) v[k] = fmax3(u[3 * k], u[3 * k + 1], u[3 * k + 2]);
+                    v[14] = u[42];
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) w5[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+                    mx = fmaxf(fmax3(w5[0], w5[1], w5[2]), fmaxf(w5[3], w5[4])) * sl2;
                 }
-                tmem_st16(tl + cS + q4 * 16, w16);
+                if (mx > m_ref + 8.f) {
+                    alpha = ex2(m_ref - mx);  // 0 on the first chunk
+                    m_ref = mx;
+                }
+                // (a row that has seen no key yet keeps m_ref = -inf; its
+                // scores are all -inf and must give P = 0, not inf - inf)
+                ls = exp_row<T>(sr, m_ref == -INFINITY ? 0.f : m_ref, sl2, tl + cS);
             }
-            const float2 s0 = f32x2_split(acc0), s1 = f32x2_split(acc1);
-            const float ls = (s0.x + s0.y) + (s1.x + s1.y);
             const bool resc = alpha != 1.f;
             l = l * alpha + ls;
             // O_g += P_g(c-1) V_(c-1) was issued before S_g(c), which is done
@@ -486,12 +518,9 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     dim3 grid(p.nQ, p.Hq, p.B);
     if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_fwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdSmem);
-        cudaFuncSetAttribute(k_fwd<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdSmem);
-        attr = true;
-    }
+    const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_fwd<__nv_bfloat16>, (int)kFwdSmem)
+                                             : ensure_smem_limit((const void *)k_fwd<__half>, (int)kFwdSmem);
+    if (ae != cudaSuccess) return ae;
     prof_begin("fwd_attn", s);
     if (p.dtype == T_BF16)
         k_fwd<__nv_bfloat16><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a);

@@ -245,15 +245,12 @@ size_t select_smem(int rpw, int nKV) {
 
 cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map, int *q_idx,
                           int *q_cnt, int cap, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_select<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        cudaFuncSetAttribute(k_select<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attr = true;
-    }
     const size_t cap_smem = 227 * 1024;
     // two query tiles per warp: two blocks fit on an SM for the usual tile counts
     const int rpw = select_smem(2, p.nKV) <= cap_smem ? 2 : 1;
+    const cudaError_t ae = rpw == 2 ? ensure_smem_limit((const void *)k_select<2>, (int)cap_smem)
+                                    : ensure_smem_limit((const void *)k_select<1>, (int)cap_smem);
+    if (ae != cudaSuccess) return ae;
     const int R = 8 * rpw;
     dim3 grid((p.nQ + R - 1) / R, p.Hq, p.B);
     prof_begin("select_topk", s);
@@ -366,11 +363,8 @@ cudaError_t launch_transpose(const Prob &p, const uint8_t *map, int *kv_ptr, int
     if (p.B == 0 || p.Hq == 0) return cudaSuccess;
     dim3 grid(p.Hq, p.B);
     const size_t smem = sizeof(int) * (p.nKV + 1);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_transpose, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        attr = true;
-    }
+    const cudaError_t ae = ensure_smem_limit((const void *)k_transpose, 64 * 1024);
+    if (ae != cudaSuccess) return ae;
     prof_begin("transpose_index", s);
     k_transpose<<<grid, 1024, smem, s>>>(p, map, kv_ptr, kv_qidx, cap);
     prof_end(s);
@@ -389,7 +383,7 @@ namespace {
 __device__ __forceinline__ bool block_exists(const Prob &p, int b, int i, int s, int bq, int nQb) {
     const int blk = i * (p.tile_q / bq) + s;
     if (blk >= nQb) return false;
-    if (p.layout == L_TND) return i * p.tile_q + s * bq < p.cu_q[b + 1] - p.cu_q[b];
+    if (p.layout == L_TND) return i * p.tile_q + s * bq < seq_len(p, true, b);
     return true;
 }
 __device__ __forceinline__ int tile_bits(const Prob &p, const uint8_t *__restrict__ bm, int nQb, int bq, int b,

@@ -6,6 +6,8 @@
 
 #include <cmath>
 #include <cstdio>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "vsa.h"
@@ -93,9 +95,63 @@ bool make_tmap_rows(CUtensorMap *map, const Prob &p, bool q_side, const void *ba
     return r == CUDA_SUCCESS;
 }
 
-// -------------------------------------------------------------- validation
+// ------------------------------------------------------ contexts, attributes
 namespace {
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    }
+    return fn;
+}
+PFN_cuCtxGetId_v12000 ctx_id_fn() {
+    static PFN_cuCtxGetId_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+    }
+    return fn;
+}
+std::mutex g_attr_mu;
+std::vector<std::pair<unsigned long long, const void *>> g_attr_done;  // (context id, kernel)
+}  // namespace
 
+unsigned long long current_context_id() {
+    auto cur = ctx_current_fn();
+    auto idf = ctx_id_fn();
+    if (!cur || !idf) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (cur(&c) != CUDA_SUCCESS || !c) return 0;
+    if (idf(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+cudaError_t ensure_smem_limit(const void *kernel, int bytes) {
+    unsigned long long ctx = current_context_id();
+    if (ctx) {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        for (const auto &e : g_attr_done)
+            if (e.first == ctx && e.second == kernel) return cudaSuccess;
+    }
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    ctx = current_context_id();  // the call above brings the context up if it was not yet
+    if (ctx) {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        g_attr_done.emplace_back(ctx, kernel);
+    }
+    return cudaSuccess;
+}
+
+// -------------------------------------------------------------- validation
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 vsa_status to_prob(const vsa_desc *d, Prob *p) {
@@ -134,7 +190,7 @@ vsa_status to_prob(const vsa_desc *d, Prob *p) {
     return VSA_OK;
 }
 
-vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var, Prob *out, bool need_q = true) {
+vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var, Prob *out, bool need_q) {
     *out = p;
     if (p.layout == L_TND) return VSA_OK;
     if ((need_q && !q_var) || !kv_var) return VSA_ERR_NULL;
@@ -142,6 +198,33 @@ vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var,
     out->kv_var = kv_var;
     return VSA_OK;
 }
+
+vsa_status block_map_prob(const vsa_desc *desc, const void *q, const void *k, const int32_t *q_var,
+                          const int32_t *kv_var, int topk, int need_bwd_index, const uint8_t *block_map,
+                          const int32_t *q_idx, const int32_t *q_cnt, int idx_cap, const int32_t *kv_ptr,
+                          const int32_t *kv_qidx, Prob *p) {
+    Prob p0;
+    vsa_status st = to_prob(desc, &p0);
+    if (st != VSA_OK) return st;
+    if ((st = need_vars(p0, q_var, kv_var, p, true)) != VSA_OK) return st;
+    if (!q || !k || !block_map || !q_idx || !q_cnt) return VSA_ERR_NULL;
+    if (need_bwd_index && (!kv_ptr || !kv_qidx)) return VSA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k)) return VSA_ERR_LAYOUT;
+    if (topk < 1 || idx_cap < (topk < p->nKV ? topk : p->nKV)) return VSA_ERR_SHAPE;
+    if (p->nKV > kMaxSelectKV) return VSA_ERR_UNSUPPORTED;
+    return VSA_OK;
+}
+
+vsa_status run_block_map(const Prob &p, const void *q, const void *k, int topk, int need_bwd_index,
+                         uint8_t *block_map, int32_t *q_idx, int32_t *q_cnt, int idx_cap, int32_t *kv_ptr,
+                         int32_t *kv_qidx, float *pq, float *pk, cudaStream_t s) {
+    cudaError_t e = launch_pool_qkv(p, q, pq, k, pk, nullptr, nullptr, s);
+    if (e == cudaSuccess) e = launch_select(p, pq, pk, topk, block_map, q_idx, q_cnt, idx_cap, s);
+    if (e == cudaSuccess && need_bwd_index) e = launch_transpose(p, block_map, kv_ptr, kv_qidx, idx_cap, s);
+    return status_from_cuda(e);
+}
+
+namespace {
 
 struct WsLayout {
     size_t pq, pk, pv, c, nlse2, ndvec, dc, A, ds, dpq, dpk, dpv, total;
@@ -222,22 +305,14 @@ vsa_status vsa_build_block_map(const vsa_desc *desc, const void *q, const void *
                                const int32_t *kv_var, int topk, int need_bwd_index, uint8_t *block_map,
                                int32_t *q_idx, int32_t *q_cnt, int idx_cap, int32_t *kv_ptr, int32_t *kv_qidx,
                                void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
-    Prob p0, p;
-    VSA_TRY(to_prob(desc, &p0));
-    VSA_TRY(need_vars(p0, q_var, kv_var, &p));
-    if (!q || !k || !block_map || !q_idx || !q_cnt) return VSA_ERR_NULL;
-    if (need_bwd_index && (!kv_ptr || !kv_qidx)) return VSA_ERR_NULL;
-    if (!aligned16(q) || !aligned16(k)) return VSA_ERR_LAYOUT;
-    if (topk < 1 || idx_cap < (topk < p.nKV ? topk : p.nKV)) return VSA_ERR_SHAPE;
-    if (p.nKV > kMaxSelectKV) return VSA_ERR_UNSUPPORTED;
+    Prob p;
+    VSA_TRY(block_map_prob(desc, q, k, q_var, kv_var, topk, need_bwd_index, block_map, q_idx, q_cnt, idx_cap,
+                           kv_ptr, kv_qidx, &p));
     VSA_TRY(check_ws(p, false, workspace, workspace_bytes));
     const WsLayout L = ws_layout(p, false);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk);
-    VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, nullptr, nullptr, s));
-    VSA_CUDA(launch_select(p, pq, pk, topk, block_map, q_idx, q_cnt, idx_cap, s));
-    if (need_bwd_index) VSA_CUDA(launch_transpose(p, block_map, kv_ptr, kv_qidx, idx_cap, s));
-    return VSA_OK;
+    return run_block_map(p, q, k, topk, need_bwd_index, block_map, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx,
+                         at<float>(workspace, L.pq), at<float>(workspace, L.pk),
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 vsa_status vsa_mask_to_index(const vsa_desc *desc, const uint8_t *block_map, const int32_t *q_var,
@@ -346,7 +421,7 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
                     void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
-    VSA_TRY(need_vars(p0, q_var, kv_var, &p));
+    VSA_TRY(need_vars(p0, q_var, kv_var, &p, true));
     if (!dO || !q || !k || !v || !o_sparse || !lse || !q_idx || !q_cnt || !kv_ptr || !kv_qidx || !dq || !dk ||
         !dv)
         return VSA_ERR_NULL;
@@ -441,7 +516,7 @@ const char *vsa_status_string(vsa_status st) {
     switch (st) {
         case VSA_OK: return "ok";
         case VSA_ERR_NULL: return "a required pointer is NULL";
-        case VSA_ERR_SHAPE: return "inconsistent sizes";
+        case VSA_ERR_SHAPE: return "inconsistent sizes, or an index or tile fill out of range";
         case VSA_ERR_DTYPE: return "unsupported dtype (bf16 or fp16 only)";
         case VSA_ERR_LAYOUT: return "unknown layout or misaligned pointer";
         case VSA_ERR_UNSUPPORTED: return "unsupported size (D must be 128, tiles 128 or 256)";

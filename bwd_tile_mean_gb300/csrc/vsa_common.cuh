@@ -25,23 +25,29 @@ struct Prob {
     float scale;
 };
 
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// TND: first token and length of sequence b, with the offsets clamped into
+// [0, total tokens] (a decreasing or overlong offset array cannot move an
+// access outside the tensor; vsa_check_inputs reports such arrays).
+__device__ __forceinline__ int seq_start(const Prob &p, bool q_side, int b) {
+    return clampi((q_side ? p.cu_q : p.cu_kv)[b], 0, q_side ? p.Sq : p.Skv);
+}
+__device__ __forceinline__ int seq_len(const Prob &p, bool q_side, int b) {
+    const int s0 = seq_start(p, q_side, b);
+    return clampi((q_side ? p.cu_q : p.cu_kv)[b + 1], s0, q_side ? p.Sq : p.Skv) - s0;
+}
+
 // Valid tokens of KV tile j of batch entry b (padded layouts: kv_var[j]
-// clamped to [0, tile]; TND: the part of the tile inside the sequence).
+// clamped to [0, tile]; a value outside that range is invalid input, which
+// vsa_check_inputs reports; TND: the part of the tile inside the sequence).
 __device__ __forceinline__ int kv_valid(const Prob &p, int b, int j) {
-    if (p.layout == L_TND) {
-        int v = (p.cu_kv[b + 1] - p.cu_kv[b]) - j * p.tile_kv;
-        return v < 0 ? 0 : (v > p.tile_kv ? p.tile_kv : v);
-    }
-    const int v = p.kv_var[j];
-    return v < 0 ? 0 : (v > p.tile_kv ? p.tile_kv : v);
+    if (p.layout == L_TND) return clampi(seq_len(p, false, b) - j * p.tile_kv, 0, p.tile_kv);
+    return clampi(p.kv_var[j], 0, p.tile_kv);
 }
 __device__ __forceinline__ int q_valid(const Prob &p, int b, int i) {
-    if (p.layout == L_TND) {
-        int v = (p.cu_q[b + 1] - p.cu_q[b]) - i * p.tile_q;
-        return v < 0 ? 0 : (v > p.tile_q ? p.tile_q : v);
-    }
-    const int v = p.q_var[i];
-    return v < 0 ? 0 : (v > p.tile_q ? p.tile_q : v);
+    if (p.layout == L_TND) return clampi(seq_len(p, true, b) - i * p.tile_q, 0, p.tile_q);
+    return clampi(p.q_var[i], 0, p.tile_q);
 }
 // Query rows of tile i that exist (all slots in the padded layouts).
 __device__ __forceinline__ int q_rows(const Prob &p, int b, int i) {
@@ -58,12 +64,11 @@ __device__ __forceinline__ long long tok_off(const Prob &p, bool q_side, int b, 
         const int S = q_side ? p.Sq : p.Skv;
         return (((long long)b * S + s) * H + h) * p.D;
     }
-    const int *cu = q_side ? p.cu_q : p.cu_kv;
-    return ((long long)(cu[b] + s) * H + h) * p.D;
+    return ((long long)(seq_start(p, q_side, b) + s) * H + h) * p.D;
 }
 // Offset of the LSE / Dvec entry of (b, h, s): [B, Hq, Sq] or [Hq, T].
 __device__ __forceinline__ long long lse_off(const Prob &p, int b, int h, int s) {
-    if (p.layout == L_TND) return (long long)h * p.Sq + p.cu_q[b] + s;
+    if (p.layout == L_TND) return (long long)h * p.Sq + seq_start(p, true, b) + s;
     return ((long long)b * p.Hq + h) * p.Sq + s;
 }
 

@@ -18,6 +18,32 @@ void prof_end(cudaStream_t s);
 // and returns VSA_ERR_CUDA.
 vsa_status status_from_cuda(cudaError_t e);
 
+// Identity (cuCtxGetId) of the calling thread's current CUDA context, 0 if
+// there is none yet. A device reset gives the device a new context and so
+// a new id, which is how per-device set-up learns it must be redone.
+unsigned long long current_context_id();
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per context
+// (the attribute belongs to the device's context, so every GPU and every
+// context after a reset gets its own call); thread-safe.
+cudaError_t ensure_smem_limit(const void *kernel, int bytes);
+
+// Host-side validation shared by the entry points: descriptor -> Prob
+// (VSA_OK or the status to return; scale 0 becomes 1/sqrt(D)); the tile
+// fills become part of the Prob in the padded layouts (need_q: q_var is
+// required too).
+bool aligned16(const void *ptr);
+vsa_status to_prob(const vsa_desc *d, Prob *p);
+vsa_status need_vars(const Prob &p, const int32_t *q_var, const int32_t *kv_var, Prob *out, bool need_q);
+// Every argument check of vsa_build_block_map except the workspace's.
+vsa_status block_map_prob(const vsa_desc *desc, const void *q, const void *k, const int32_t *q_var,
+                          const int32_t *kv_var, int topk, int need_bwd_index, const uint8_t *block_map,
+                          const int32_t *q_idx, const int32_t *q_cnt, int idx_cap, const int32_t *kv_ptr,
+                          const int32_t *kv_qidx, Prob *p);
+// The block-map step's launches with the tile means in pq / pk.
+vsa_status run_block_map(const Prob &p, const void *q, const void *k, int topk, int need_bwd_index,
+                         uint8_t *block_map, int32_t *q_idx, int32_t *q_cnt, int idx_cap, int32_t *kv_ptr,
+                         int32_t *kv_qidx, float *pq, float *pk, cudaStream_t s);
+
 // Tile pooling (fp32 means of the first var tokens), [B, H, nT, D].
 struct PoolSeg {
     const void *x;     // q, k or v in the problem's layout

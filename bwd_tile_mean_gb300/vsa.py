@@ -32,7 +32,8 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_profile_name", "vsa_profile_ms", "vsa_profile_reset", "vsa_launch_count",
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
            "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
-           "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host", "vsa_step_host_status")
+           "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host", "vsa_step_host_status",
+           "vsa_check_inputs")
 
 
 class VsaError(RuntimeError):
@@ -120,6 +121,9 @@ def lib():
                                           P, C.c_size_t, P]
         L.vsa_step_host_status.restype = C.c_int
         L.vsa_step_host_status.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, C.c_int, P, P, C.POINTER(C.c_int32)]
+        L.vsa_check_inputs.restype = C.c_int
+        L.vsa_check_inputs.argtypes = [C.POINTER(VsaDesc), P, P, P, P, C.c_int, P, P, P, C.c_size_t, P,
+                                       C.POINTER(C.c_int32)]
         L.vsa_fwd_step_host.restype = C.c_int
         L.vsa_fwd_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, C.c_size_t,
                                         P]
@@ -192,6 +196,19 @@ def vsa_gate_grad(desc, dO, q, k, v, q_var, kv_var, dgate, workspace, stream=Non
     _check("vsa_gate_grad", lib().vsa_gate_grad(
         C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(q_var), _p(kv_var), _p(dgate), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def vsa_check_inputs(desc, q_var, kv_var, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx, workspace, stream=None):
+    """Opt-in validation of the device-resident arguments (synchronises).
+    Returns (status, code): status 0 = all in range, 2 = a check failed
+    (code names it), 9 = the status word already held another failure."""
+    code = C.c_int32(0)
+    st = lib().vsa_check_inputs(C.byref(desc), _p(q_var), _p(kv_var), _p(q_idx), _p(q_cnt), int(idx_cap),
+                                _p(kv_ptr), _p(kv_qidx), _p(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream), C.byref(code))
+    if st not in (0, 2, 9):
+        raise VsaError("vsa_check_inputs", st)
+    return int(st), int(code.value)
 
 
 def vsa_device_status(workspace, stream=None) -> int:
@@ -326,6 +343,14 @@ class Plan:
         dgate = torch.empty_like(dO) if dgate is None else dgate
         vsa_gate_grad(self.desc, dO, q, k, v, self.q_var, self.kv_var, dgate, self.workspace, stream)
         return dgate
+
+    def check_inputs(self, with_index=True, with_bwd_index=True, stream=None):
+        """vsa_check_inputs on this plan's tile fills / offsets and (when
+        asked) its index buffers; returns (status, code)."""
+        return vsa_check_inputs(self.desc, self.q_var, self.kv_var, self.q_idx if with_index else None,
+                                self.q_cnt if with_index else None, self.idx_cap,
+                                self.kv_ptr if with_bwd_index else None, self.kv_qidx if with_bwd_index else None,
+                                self.workspace, stream)
 
     def device_status(self, stream=None) -> int:
         return vsa_device_status(self.workspace, stream)

@@ -32,10 +32,17 @@
  *   tile_q tokens and nKV key/value tiles of tile_kv tokens; the first
  *   q_var[i] / kv_var[j] slots of a tile are its valid tokens and the rest
  *   are zero padding ([VSA-test] _zero_pad_tail). q_var / kv_var are device
- *   int32 arrays [nQ] / [nKV], shared by every batch entry and head. In
- *   TND the valid tokens of tile t of sequence b are
+ *   int32 arrays [nQ] / [nKV], shared by every batch entry and head, each
+ *   value in [0, tile] ([FA4-adapt] _vbs_mask_mod reads it as a count of
+ *   valid slots). In TND the valid tokens of tile t of sequence b are
  *   min(tile, len_b - t*tile) (zero past the end) and q_var / kv_var are
  *   ignored (pass NULL).
+ * - Device-resident arguments (tile fills, cu_seqlens_*, the two block
+ *   indices) cannot be checked on the host without a synchronisation, so
+ *   the calls below do not check them; vsa_check_inputs does, on request.
+ *   Given values outside their ranges anyway, the kernels still read and
+ *   write only inside the caller's buffers (fills, offsets, counts and
+ *   entries are clamped into range), but the results are meaningless.
  * - Every query slot of a padded Q tile is a query row (the valid-length
  *   mask applies to keys only, [FA4-adapt] _vbs_mask_mod); in TND only
  *   rows inside a sequence exist and only those are written.
@@ -72,7 +79,8 @@ typedef struct CUstream_st *vsa_stream_t; /* same type as cudaStream_t */
 typedef enum {
     VSA_OK = 0,
     VSA_ERR_NULL = 1,            /* a required pointer is NULL */
-    VSA_ERR_SHAPE = 2,           /* sizes inconsistent, var out of [0, tile], idx_cap too small */
+    VSA_ERR_SHAPE = 2,           /* sizes inconsistent, idx_cap too small; vsa_check_inputs: a fill,
+                                    offset or index entry out of range */
     VSA_ERR_DTYPE = 3,           /* dtype not bf16 / fp16 */
     VSA_ERR_LAYOUT = 4,          /* unknown layout, or a pointer not 16-byte aligned */
     VSA_ERR_UNSUPPORTED = 5,     /* D != 128, tile not 128/256, or a size past a kernel limit */
@@ -129,22 +137,26 @@ vsa_status vsa_build_block_map(const vsa_desc *desc, const void *q, const void *
                                void *workspace, size_t workspace_bytes, vsa_stream_t stream);
 
 /* vsa_build_block_map for callers that cannot allocate device memory.
- * The pages have no counterpart: it exists for callers such as code that
- * runs inside CUDA graph capture, custom allocators that forbid
- * cudaMalloc, or runtimes that own all device memory and cannot hand the
- * library a workspace. Same arguments, results and errors as
- * vsa_build_block_map, minus the workspace: the scratch for the fp32 tile
- * means lives in a fixed array inside libvsa.so (16 MiB, 4,194,304 floats,
- * held on every GPU that loads the library until the process exits). A
- * problem needs B*Hq*nQ*128 + B*Hkv*nKV*128 floats of it (plus alignment
- * padding of at most 63 floats); larger problems return VSA_ERR_SCRATCH.
- * No cudaMalloc, cudaFree or allocating library routine is called. The
- * first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture. Every call shares the one array: calls whose
- * kernels may overlap on the GPU (different streams, or several host
- * threads) race on it and must be serialised by the caller. Nothing in the
- * array needs clearing between calls: each call overwrites what it reads. */
+ * The pages have no counterpart. It exists for callers that may not call
+ * cudaMalloc at all: a runtime or memory pool that owns every byte of the
+ * device and has no workspace to lend, an allocator that forbids outside
+ * allocations, or code on a path where an allocation could synchronise the
+ * device or fail. Same arguments, checks, results and errors as
+ * vsa_build_block_map (the same validation and launches run), minus the
+ * workspace: the scratch for the fp32 tile means lives in a fixed array
+ * inside libvsa.so (16 MiB, 4,194,304 floats, held on every GPU that loads
+ * the library until the process exits). A problem needs B*Hq*nQ*128 +
+ * B*Hkv*nKV*128 floats of it (plus alignment padding of at most 63
+ * floats); larger problems return VSA_ERR_SCRATCH before anything is
+ * launched. No cudaMalloc, cudaFree or allocating library routine is
+ * called. The first call on a device (and the first after a device reset)
+ * looks up the array's device address with that device current
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture. Every call shares the one array, which keeps the last
+ * call's contents: calls whose kernels may overlap on the GPU (different
+ * streams, or several host threads) race on it and must be serialised by
+ * the caller. Nothing in the array needs clearing between calls: each call
+ * writes every element it later reads. */
 vsa_status vsa_build_block_map_static(const vsa_desc *desc, const void *q, const void *k,
                                       const int32_t *q_var, const int32_t *kv_var, int topk,
                                       int need_bwd_index, uint8_t *block_map, int32_t *q_idx,
@@ -196,7 +208,6 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    const void *gate, void *dq, void *dk, void *dv, void *workspace,
                    size_t workspace_bytes, vsa_stream_t stream);
 
-/* Human-readable name of a status. */
 /* Failure-path check: launches one warp that waits, with the library's
  * bounded mbarrier wait, on a barrier that nothing ever arrives on. After
  * limit_ns of wall time (0 < limit_ns <= 10 s) the wait gives up, records
@@ -345,7 +356,43 @@ vsa_status vsa_fwd_step_host(const vsa_desc *desc, int groups, const void *q, co
 vsa_status vsa_step_host_status(const vsa_desc *desc, int groups, int topk, int with_gate, void *device_buf,
                                 vsa_stream_t stream, int32_t *code);
 
+/* Human-readable name of a status. */
 const char *vsa_status_string(vsa_status status);
+
+/* Validation of the device-resident arguments, for debugging and for
+ * callers that build their own indices: opt-in, never run by the other
+ * calls (it synchronises `stream`). Checks, reading only inside the sizes
+ * the descriptor and idx_cap declare:
+ *   tile fills q_var / kv_var within [0, tile] (padded layouts; the key of
+ *     KV tile j is valid iff its slot < kv_var[j], [FA4-adapt]
+ *     _vbs_mask_mod), or, in TND, cu_seqlens_* non-negative, ascending,
+ *     at most the total tokens, and no sequence longer than nQ (nKV)
+ *     tiles ([NPU-test] actual_seq_lengths);
+ *   if q_idx / q_cnt are given: every count within [0, idx_cap], the first
+ *     count's entries within [0, nKV), ascending, each a tile with valid
+ *     tokens ([FA4-adapt] _map_to_index and the vbs > 0 split of
+ *     _build_sparse_tensors);
+ *   if kv_ptr / kv_qidx are given: offsets start at 0, ascend and stay
+ *     within nQ*idx_cap; entries within [0, nQ), ascending per KV tile; and
+ *     with q_idx given too, the KV-owned index is exactly the transpose of
+ *     the Q-owned one ([FA4-adapt] _build_sparse_tensors, KV-owned
+ *     backward metadata).
+ * q_var / kv_var are required in the padded layouts; each index is passed
+ * whole or not at all (both pointers NULL). workspace: 256-byte aligned,
+ * at least 256 bytes; only its status word is used. The first failing
+ * check records its code (0xC001 bad q_var, 0xC002 bad kv_var, 0xC003 /
+ * 0xC004 bad cu_seqlens_q / _kv, 0xC005 bad q_cnt, 0xC006 bad q_idx,
+ * 0xC007 bad kv_ptr, 0xC008 bad kv_qidx, 0xC009 not a transpose) in the
+ * status word; the call then reads and clears the word as
+ * vsa_device_status does, sets *code and returns VSA_ERR_SHAPE for one of
+ * these codes, VSA_ERR_DEVICE when the word already held another failure,
+ * VSA_OK (code 0) when everything is in range. Host-side errors as for
+ * vsa_build_block_map, VSA_ERR_WORKSPACE for the workspace, VSA_ERR_NULL
+ * for code == NULL or half an index. */
+vsa_status vsa_check_inputs(const vsa_desc *desc, const int32_t *q_var, const int32_t *kv_var,
+                            const int32_t *q_idx, const int32_t *q_cnt, int idx_cap, const int32_t *kv_ptr,
+                            const int32_t *kv_qidx, void *workspace, size_t workspace_bytes, vsa_stream_t stream,
+                            int32_t *code);
 
 /* Message of the last CUDA error behind a VSA_ERR_CUDA return, with the
  * name of the last kernel the library launched ("no error" if there was

@@ -72,6 +72,14 @@ class _Bound:
             self.keep.append(x)
             return _ptr(x)
 
+        if p.layout != "tnd":
+            # a tile fill is a count of valid slots in [0, tile] (FastVideo
+            # block_sparse_attn_cute_fwd.py, _vbs_mask_mod: key n valid iff
+            # n mod tile < vbs); the pages give no meaning to other values
+            for name, var, tile in (("q_var", p.q_var, p.tile_q), ("kv_var", p.kv_var, p.tile_kv)):
+                v = np.asarray(var)
+                if v.size and (int(v.min()) < 0 or int(v.max()) > tile):
+                    raise ValueError(f"{name} outside [0, {tile}]")
         self.p = p
         self.d = _Desc(_LAYOUT[p.layout], p.B, p.Hq, p.Hkv, p.D, p.Sq, p.Skv, p.tile_q, p.tile_kv,
                        p.nQ, p.nKV, arr(p.cu_q), arr(p.cu_kv), arr(p.q_var), arr(p.kv_var),

@@ -116,3 +116,42 @@ def test_train_step_host_validation(L):
     code = C.c_int32(0)
     assert L.vsa_step_host_status(C.byref(d), 2, 2, 0, None, None, C.byref(code)) == 1
     assert L.vsa_step_host_status(C.byref(d), 3, 2, 0, FAKE, None, C.byref(code)) == 2
+
+
+def test_static_block_map_checks_like_the_workspace_entry_point(L):
+    # the allocation-free entry point runs the same host validation: every
+    # descriptor or argument error gives the same status from both calls
+    def both(d, topk=2, cap=2, need=0, kv_ptr=None):
+        ws = L.vsa_build_block_map(C.byref(d), FAKE, FAKE, FAKE, FAKE, topk, need, FAKE, FAKE, FAKE, cap, kv_ptr,
+                                   kv_ptr, FAKE, 1 << 30, None)
+        st = L.vsa_build_block_map_static(C.byref(d), FAKE, FAKE, FAKE, FAKE, topk, need, FAKE, FAKE, FAKE, cap,
+                                          kv_ptr, kv_ptr, None)
+        return ws, st
+    cases = [desc(scale=float("inf")), desc(scale=-1.0), desc(scale=float("nan")), desc(D=64), desc(dtype=3),
+             desc(layout=2, Sq=-5, Skv=100, cu_seqlens_q=FAKE, cu_seqlens_kv=FAKE), desc(Sq=700),
+             desc(layout=2, Sq=100, Skv=100), desc(Hq=3, Hkv=2), desc(nKV=4000, Skv=4000 * 256)]
+    for d in cases:
+        ws, st = both(d)
+        assert ws == st != 0, (ws, st)
+    assert both(desc(), topk=0) == (2, 2)
+    assert both(desc(), cap=1) == (2, 2)
+    assert both(desc(), need=1) == (1, 1)
+
+
+def test_check_inputs_host_validation(L):
+    code = C.c_int32(0)
+
+    def call(d=None, q_var=FAKE, kv_var=FAKE, q_idx=None, q_cnt=None, cap=2, kv_ptr=None, kv_qidx=None, ws=FAKE,
+             wsb=256, code_p=C.byref(code)):
+        return L.vsa_check_inputs(C.byref(d or desc()), q_var, kv_var, q_idx, q_cnt, cap, kv_ptr, kv_qidx, ws, wsb,
+                                  None, code_p)
+    assert call(d=desc(D=64)) == 5
+    assert call(kv_var=None) == 1                       # padded layouts need both fills
+    assert call(code_p=None) == 1
+    assert call(q_idx=FAKE) == 1                        # half of the Q-owned index
+    assert call(kv_ptr=FAKE) == 1                       # half of the KV-owned index
+    assert call(q_idx=FAKE, q_cnt=FAKE, cap=0) == 2
+    assert call(q_idx=FAKE, q_cnt=FAKE, cap=5) == 2     # idx_cap > nKV
+    assert call(ws=None) == 7
+    assert call(ws=C.c_void_p((1 << 20) + 16)) == 7
+    assert call(wsb=128) == 7

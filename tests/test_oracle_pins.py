@@ -157,6 +157,18 @@ def test_transpose_round_trips_to_q_lists():
             assert back[i] == qi[0, h, i, :qc[0, h, i]].tolist()
 
 
+@pytest.mark.parametrize("bad", [("kv", 300), ("kv", -1), ("q", 257)])
+def test_tile_fill_outside_the_tile_is_rejected(bad):
+    # a fill counts valid slots (key n valid iff n mod tile < vbs); outside
+    # [0, tile] it has no meaning on the pages, so the oracle refuses it
+    side, v = bad
+    kv, qv = [256, 173, 79], [256, 100]
+    (kv if side == "kv" else qv)[1] = v
+    p = small(kv_var=kv, q_var=qv)
+    with pytest.raises(ValueError):
+        orc.pool_f32(p, np.zeros(p.shape(side == "q"), np.float32), side == "q")
+
+
 def test_mask_index_ignores_blocks_past_sequence_ends():
     p = tnd_problem("t", [130, 5, 300], [20, 400, 129], 2, 1, tile=128)
     mask = np.ones((p.B, p.Hq, p.nQ, p.nKV), dtype=np.uint8)
