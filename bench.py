@@ -9,14 +9,18 @@ C ABI. FLOPs are counted on selected tile pairs only:
 keys of the KV tile.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 1|3|4|5|6] [--shard heads|replicas]
 
-Under torchrun every rank runs its own replica of the workload on its own
-GPU (weak scaling); timing is the max over ranks. --impl reference times
-the CPU oracle on a bounded sample of the same workload (rank 0 only).
+Under torchrun the problem's heads are split over the ranks (vsa_head_slice:
+whole GQA groups per rank, no exchange between ranks; strong scaling), or,
+with --shard replicas, every rank runs its own copy (weak scaling); timing is
+the max over ranks. --impl reference times the CPU oracle on a bounded
+sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -28,18 +32,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fwd+bwd effective TFLOP/s (selected blocks) on 1 GB300; % of bf16 TC peak"
-
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# attention kernel, from one `ncu --set full` capture of the current kernels
-# on this workload cut to 4 heads; every head is an independent problem, so
-# the traffic of a launch scales with the heads. Set an entry to None when its
-# kernel changes after the capture.
-DRAM_BYTES_PER_4_HEADS = {
-    "bwd_dkdv": 397.200128e6 + 141.905152e6,
-    "bwd_dq": 406.098432e6 + 73.191424e6,
-    "fwd_attn": 306.897408e6 + 67.292672e6,
-}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Per-launch DRAM bytes of the attention kernels come from an ncu capture of
+# this workload cut to a few heads (every head is an independent problem, so
+# a launch's traffic scales with the heads). The capture records the hash of
+# the source file that defines each kernel; a kernel whose source changed
+# since then reports no traffic.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_bytes_video_dit_4heads.json")
+KERNEL_SOURCE = {"fwd_attn": "fwd_kernel.cu", "bwd_dkdv": "bwd_kernels.cu", "bwd_dq": "bwd_kernels.cu",
+                 "bwd_prep": "bwd_kernels.cu", "pool": "index_kernels.cu", "select_topk": "index_kernels.cu"}
+CPU_SAMPLE_TILES = 2   # query tiles (forward, dQ) and KV tiles (dK, dV) of the oracle sample
 
 
 def peaks():
@@ -51,6 +53,29 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_sha(kernel):
+    """Hash (first 16 hex digits of SHA-256) of the source file defining a kernel."""
+    path = os.path.join(ROOT, "bwd_tile_mean_gb300", "csrc", KERNEL_SOURCE[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel, heads):
+    """(bytes per launch at `heads` heads, note) from the committed capture,
+    or (None, why not)."""
+    if kernel not in KERNEL_SOURCE or not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu capture of this kernel"
+    with open(TRAFFIC_FILE) as f:
+        cap = json.load(f)
+    k = cap.get("kernels", {}).get(kernel)
+    if k is None:
+        return None, "no ncu capture of this kernel"
+    if k.get("source_sha256") != source_sha(kernel):
+        return None, f"kernel source changed since the capture ({cap.get('captured', '?')})"
+    return (k["dram_bytes_read"] + k["dram_bytes_write"]) * heads / cap["heads"], \
+        f"ncu capture {cap.get('captured', '?')} on {cap['heads']} heads, scaled to {heads}"
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -60,12 +85,21 @@ def dist_env():
 
 def reduce_max(x, world_size, device):
     """Max of a per-rank float over all ranks (identity on one rank)."""
+    return _reduce(x, world_size, device, "max")
+
+
+def reduce_sum(x, world_size, device):
+    """Sum of a per-rank float over all ranks (identity on one rank)."""
+    return _reduce(x, world_size, device, "sum")
+
+
+def _reduce(x, world_size, device, op):
     if world_size == 1:
         return x
     import torch
     import torch.distributed as dist
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -113,14 +147,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(n_tiles=2, seed=42):
+def oracle_sample(n_tiles=CPU_SAMPLE_TILES, seed=42):
     """Time the CPU oracle (block map + forward + backward) on a bounded
     sample of the workload: one head of the same shape (300 tiles, topk 30),
-    forward and dQ for the rows of n_tiles query tiles and dK/dV of n_tiles
-    KV tiles. Credited with the effective FLOPs of the selected pairs of
-    those query tiles. Returns (tflops, seconds, description, threads)."""
+    its whole block map, the forward and dQ rows of n_tiles query tiles and
+    dK/dV of n_tiles KV tiles. Credited with the effective FLOPs (14 D M N)
+    of the selected pairs of those query tiles. Returns a dict: tflops,
+    seconds, the seconds of each part, the sample and the threads used."""
     import numpy as np
-    import torch
     from bwd_tile_mean_gb300.inputs import Problem, make_tensors
     from oracle import oracle as orc
 
@@ -130,40 +164,49 @@ def oracle_sample(n_tiles=2, seed=42):
     t = make_tensors(p)
     q, k, v, dO = (orc._f64(t[n]) for n in ("q", "k", "v", "dO"))
     orc.lib()
+    parts = {}
     t0 = time.perf_counter()
     m, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    t1 = time.perf_counter()
     rows = np.asarray([(0, 0, i * 256 + r) for i in range(n_tiles) for r in range(256)], dtype=np.int32)
     orc.forward_rows(p, q, k, v, qi, qc, p.cap, rows=rows)
+    t2 = time.perf_counter()
     orc.backward_dq_rows(p, dO, q, k, v, qi, qc, p.cap, rows=rows)
+    t3 = time.perf_counter()
     tiles = np.asarray([(0, 0, j) for j in range(n_tiles)], dtype=np.int32)
     orc.backward_dkdv_tiles(p, dO, q, k, v, qi, qc, p.cap, tiles=tiles)
-    dt = time.perf_counter() - t0
+    t4 = time.perf_counter()
+    parts = {"block_map_s": t1 - t0, "forward_s": t2 - t1, "dq_s": t3 - t2, "dkdv_s": t4 - t3}
+    dt = t4 - t0
     pairs = int(qc[0, 0, :n_tiles].sum())
     flops = pairs * 2.0 * 128 * 256 * 256 * 7
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     desc = (f"oracle block map of one 300-tile head + forward and dQ of {n_tiles} query tiles' rows + dK/dV of "
             f"{n_tiles} KV tiles ({pairs} selected pairs credited, 14*D*M*N flops each)")
-    del torch
-    return flops / dt / 1e12, dt, desc, threads
+    return {"tflops": flops / dt / 1e12, "seconds": dt, "parts": parts, "sample": desc, "threads": threads}
 
 
 def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    vals, secs = [], []
-    desc, threads = "", 1
+    vals, secs, parts = [], [], {}
+    r = None
     for it in range(args.warmup + args.steps):
-        v, dt, desc, threads = oracle_sample(n_tiles=1)
+        r = oracle_sample()
         if it >= args.warmup:
-            vals.append(v)
-            secs.append(dt)
+            vals.append(r["tflops"])
+            secs.append(r["seconds"])
+            for n, x in r["parts"].items():
+                parts.setdefault(n, []).append(x)
     value = statistics.mean(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "video-dit-76800 (one-head sample, see cpu_baseline.sample)"},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["threads"], "kind": "oracle",
+                             "sample": r["sample"],
+                             "seconds_by_part": {n: statistics.mean(x) for n, x in parts.items()}},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -200,6 +243,30 @@ def layout_step(q, p, dev, stream, e0, e1):
 
 # ------------------------------------------------------------------ ours
 
+def workload(args):
+    from bwd_tile_mean_gb300 import inputs
+    p = inputs.config(args.config)
+    if args.config == 3 and args.heads != p.Hq:  # smaller copy of the same workload (profiling captures)
+        p = inputs.Problem(p.name, p.layout, p.B, args.heads, args.heads, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV,
+                           q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, seed=p.seed)
+    return p
+
+
+def head_shard(p, t, ws, rank, dev):
+    """This rank's slice of the problem's heads (vsa_head_slice): the slice
+    problem and its tensors, cut from the whole problem's seeded tensors."""
+    from bwd_tile_mean_gb300 import inputs, vsa
+    full = vsa.describe(p.layout, inputs.DTYPES[p.dtype], p.B, p.Hq, p.Hkv, p.D, p.Sq, p.Skv, p.tile_q, p.tile_kv,
+                        p.nQ, p.nKV)
+    sd, q0, kv0 = vsa.vsa_head_slice(full, ws, rank)
+    ps = inputs.Problem(p.name, p.layout, p.B, sd.Hq, sd.Hkv, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV, dtype=p.dtype,
+                        q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, gate=p.gate, seed=p.seed, backward=p.backward)
+    hd = 1 if p.layout == "bhsd" else 2
+    ts = {n: x.narrow(hd, q0 if n in ("q", "dO", "gate") else kv0,
+                      sd.Hq if n in ("q", "dO", "gate") else sd.Hkv).contiguous() for n, x in t.items()}
+    return ps, ts, (q0, sd.Hq)
+
+
 def ours(args):
     import torch
 
@@ -211,14 +278,17 @@ def ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    p = inputs.config(args.config)
-    if args.config == 3 and args.heads != p.Hq:  # smaller replica of the same workload (profiling captures)
-        p = inputs.Problem(p.name, p.layout, p.B, args.heads, args.heads, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV,
-                           q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, seed=p.seed)
+    shard = ws > 1 and args.shard == "heads"
+    p_full = workload(args)
+    t = inputs.make_tensors(p_full, device=dev)
+    heads = (0, p_full.Hq)
+    if shard:
+        p, t, heads = head_shard(p_full, t, ws, rank, dev)
+    else:
+        p = p_full
     gated = p.gate is not None
     train = p.backward
     T = inputs.DTYPES[p.dtype]
-    t = inputs.make_tensors(p, device=dev)
     q, k, v, dO = t["q"], t["k"], t["v"], t["dO"]
     i32 = dict(dtype=torch.int32, device=dev)
     plan = vsa.Plan(p.layout, T, p.B, p.Hq, p.Hkv, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV, p.Sq, p.Skv, p.cap,
@@ -243,21 +313,21 @@ def ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(x):
-        return reduce_max(x, ws, dev)
-
     for _ in range(args.warmup):
         step(q, k, v, dO)
     barrier()
-    # effective FLOPs from the selection actually made
+    # effective FLOPs from the selection actually made (this rank's heads)
     qc = plan.q_cnt.long()
     qidx = plan.q_idx.long().clamp(min=0)
     kvv = torch.as_tensor(p.kv_var, device=dev).long()
-    valid_keys = torch.where(plan.q_idx >= 0, kvv[qidx], torch.zeros_like(qidx)).sum()
+    valid_keys = float(torch.where(plan.q_idx >= 0, kvv[qidx], torch.zeros_like(qidx)).sum().item())
     pairs = int(qc.sum().item())
     flop_unit = 2.0 * p.D * p.tile_q  # x N x 7 per pair
-    fwd_flops = flop_unit * float(valid_keys.item()) * 2
-    step_flops = flop_unit * float(valid_keys.item()) * (7 if train else 2)
+    fwd_flops = flop_unit * valid_keys * 2
+    step_flops = flop_unit * valid_keys * (7 if train else 2)
+    # whole-job work: every rank's own heads (sharded) or copies (replicas)
+    job_flops = reduce_sum(step_flops, ws, dev)
+    job_pairs = int(reduce_sum(pairs, ws, dev))
 
     bus = None
     try:
@@ -274,8 +344,7 @@ def ours(args):
     e1.record(stream)
     barrier()
     launches = vsa.vsa_launch_count() - n0
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms)
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, ws, dev)
     clocks = sampler.stop() if sampler else None
 
     # per-kernel times over a second, instrumented pass of the same steps
@@ -317,7 +386,8 @@ def ours(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e_steps, ws, dev)
+    job_h2d, job_d2h = int(reduce_sum(h2d, ws, dev)), int(reduce_sum(d2h, ws, dev))
 
     # the layout step on either side of the attention: 3D tiling of the
     # latent [1, 20, 48, 80, heads, 128] into the attention's token order and
@@ -334,45 +404,47 @@ def ours(args):
     for v_ in layout.values():
         v_["frac_of_hbm"] = v_["GB_per_s"] / pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tensor_peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    value = step_flops * ws / (ms * 1e-3) / 1e12
+    value = job_flops / (ms * 1e-3) / 1e12
     dominant = max(kern.items(), key=lambda kv_: kv_[1]["total_ms_per_step"]) if kern else None
     roof = None
     if dominant:
         name, info = dominant
         unit_flops = {"bwd_dkdv": 8.0, "bwd_dq": 6.0, "fwd_attn": 4.0}.get(name)
         if unit_flops is not None:
-            launch_flops = 2.0 * p.D * p.tile_q * float(valid_keys.item()) * unit_flops / 2.0
+            launch_flops = 2.0 * p.D * p.tile_q * valid_keys * unit_flops / 2.0
             achieved = launch_flops / (info["avg_ms"] * 1e-3) / 1e12
-            dram = DRAM_BYTES_PER_4_HEADS.get(name)
-            traffic = dram * p.Hq / 4.0 if dram is not None else None
+            traffic, note = measured_traffic(name, p.Hq)
             roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
                     "unit": "TFLOP/s", "frac": achieved / tensor_peak, "traffic": traffic,
-                    "traffic_unit": "bytes per launch (ncu, 4-head capture scaled to the heads)",
-                    "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
-                    "flops_per_launch": launch_flops}
+                    "traffic_unit": "bytes per launch", "traffic_source": note,
+                    "peak_kind": f"bf16_tflops_sustained ({pk_kind})", "flops_per_launch": launch_flops}
     cpu = None
     if not args.no_cpu_baseline and args.config == 3:
-        v_cpu, dt, desc, threads = oracle_sample(n_tiles=2)
-        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+        r = oracle_sample()
+        cpu = {"value": r["tflops"], "unit": "TFLOP/s", "cores": r["threads"], "kind": "oracle",
+               "sample": r["sample"], "seconds": r["seconds"], "seconds_by_part": r["parts"]}
+    if args.config == 3 and not shard:
+        wl = ("video-dit-76800: latent 20x48x80 tiled 4x8x8 -> 300 tiles, 76,800 tokens; "
+              f"B=1, H={p.Hq}, D=128, bf16, BSHD; topk 30 (10% density)")
+    else:
+        wl = (f"{p_full.name}: B={p_full.B}, H={p_full.Hq}/{p_full.Hkv}, D=128, {p_full.dtype}, {p_full.layout}, "
+              f"{p_full.nQ} Q x {p_full.nKV} KV tiles of {p_full.tile_q}/{p_full.tile_kv}, topk {p_full.topk}"
+              + (", gated" if gated else "") + ("" if train else ", forward only"))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": ("video-dit-76800: latent 20x48x80 tiled 4x8x8 -> 300 tiles, 76,800 tokens; "
-                                f"B=1, H={p.Hq}, D=128, bf16, BSHD; topk 30 (10% density)") if args.config == 3 else
-                               (f"{p.name}: B={p.B}, H={p.Hq}/{p.Hkv}, D=128, {p.dtype}, {p.layout}, "
-                                f"{p.nQ} Q x {p.nKV} KV tiles of {p.tile_q}/{p.tile_kv}, topk {p.topk}"
-                                + (", gated" if gated else "") + ("" if train else ", forward only")),
-                   "selected_pairs": pairs, "tflop_per_step": step_flops / 1e12,
-                   "fwd_tflop_per_step": fwd_flops / 1e12,
-                   "l2": "inputs larger than L2 (each of q, k, v, dO is 786 MB vs 126 MB L2); no flush",
-                   "parallelism": f"replicas x{ws}"},
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
+        "config": {"workload": wl, "selected_pairs": job_pairs, "tflop_per_step": job_flops / 1e12,
+                   "fwd_tflop_per_step": fwd_flops * (job_flops / step_flops) / 1e12,
+                   "l2": "inputs larger than L2 (each of q, k, v, dO is 786 MB vs 126 MB L2); no flush"
+                   if args.config == 3 and not shard else "see workload sizes; no flush",
+                   "parallelism": (f"heads split over {ws} GPUs ({heads[1]} query heads each, no exchange)" if shard
+                                   else f"replicas x{ws}")},
         "pct_of_peak": {"bf16_burst": value / ws / pk.get("bf16_tflops", 1900.0),
                         "bf16_sustained": value / ws / tensor_peak, "peaks": pk_kind},
         "roofline": roof, "cpu_baseline": cpu,
-        "e2e": {"value": step_flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": job_h2d, "d2h_bytes_per_step": job_d2h,
                 "path": f"{'vsa_train_step_host' if train else 'vsa_fwd_step_host'}: {groups} head slices, "
                         "copies overlapped with the kernels"},
         "gpu_launches": launches, "clocks": clocks,
@@ -393,9 +465,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=40, help="heads of the workload (40; fewer only for profiling)")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 3, 4, 5],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 3, 4, 5, 6],
                     help="workload: 3 = video DiT 76,800 tokens (the headline); 1 tiny, 4 gated ragged, "
-                         "5 long-video forward only")
+                         "5 long-video forward only, 6 the long-video grid taken literally (1,024 tiles)")
+    ap.add_argument("--shard", choices=["heads", "replicas"], default="heads",
+                    help="with several GPUs: split the problem's heads over them (default) or run copies")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

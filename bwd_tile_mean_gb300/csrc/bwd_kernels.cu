@@ -42,76 +42,131 @@ constexpr int kProdWarp = 8, kMmaWarp = 9;
 // rowsum(P dP) of the softmax backward); both are stored negated so the
 // consumers add them. Slots that are not query rows (past a varlen
 // sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there.
-// A warp takes 32 consecutive slots of one (b, h): each half-warp reads a
-// 256-byte row of dO and of O (16 bytes per lane), 16 rows in flight per
-// lane, reduces it, and the 32 row sums gather into lane r, so the LSE read
-// and both writes are one coalesced 128-byte access each. Warps visit the
-// 32-row groups in memory order of dO and O (heads of a token adjacent in
-// BSHD and TND, tokens of a head in BHSD) in a grid-stride loop sized to
-// the GPU.
-constexpr int kPrepRows = 32;  // slots per warp task
+// HBM-bound streaming: a task is 32 consecutive slots of one (b, h). One
+// producer lane per CTA streams each task's dO and O rows ([32 x 128]
+// 16-bit tiles, two 64-column TMA boxes each, 128-byte swizzle) into a ring
+// of kPrepStages shared-memory stages; four consumer warps take the tasks
+// in turn, one lane per row, so a row's sum stays in its lane and the LSE
+// read and both writes are one coalesced 128-byte access each. Tasks are
+// numbered in memory order of dO and O (heads of a token adjacent in BSHD
+// and TND, tokens of a head in BHSD) and dealt to the CTAs round robin, so
+// the CTAs in flight read neighbouring memory.
+constexpr int kPrepRows = 32;                     // slots per task
+constexpr int kPrepStages = 12;
+constexpr int kPrepBox = kPrepRows * 128;         // one 64-column box of 32 rows (bytes)
+constexpr int kPrepStage = 4 * kPrepBox;          // dO and O, two boxes each
+constexpr int kPrepConsumers = 4;
+constexpr size_t kPrepSmem = (size_t)kPrepStages * kPrepStage + 256;
+enum : unsigned { kSitePrepProd = 0x401, kSitePrepCons = 0x402 };
+
+__device__ __forceinline__ void prep_task(const Prob &p, int task, int groups, int &b, int &h, int &s0) {
+    int g;
+    if (p.layout == L_BHSD) {
+        g = task % groups;
+        const int bh = task / groups;
+        h = bh % p.Hq;
+        b = bh / p.Hq;
+    } else {
+        h = task % p.Hq;
+        const int bg = task / p.Hq;
+        g = bg % groups;
+        b = bg / groups;
+    }
+    s0 = g * kPrepRows;
+}
 
 template <typename T>
-__global__ void __launch_bounds__(256, 2) k_bwd_prep(Prob p, const T *__restrict__ dO, const T *__restrict__ O,
-                                                  const float *__restrict__ lse, float *__restrict__ nlse2,
-                                                  float *__restrict__ ndvec, int ntasks) {
-    const int per = p.nQ * p.tile_q;
-    const int groups = per / kPrepRows;
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int nwarps = gridDim.x * (blockDim.x >> 5);
-    for (int task = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks; task += nwarps) {
-        int b, h, g;
-        if (p.layout == L_BHSD) {
-            g = task % groups;
-            const int bh = task / groups;
-            h = bh % p.Hq;
-            b = bh / p.Hq;
-        } else {
-            h = task % p.Hq;
-            const int bg = task / p.Hq;
-            g = bg % groups;
-            b = bg / groups;
+__global__ void __launch_bounds__(32 * (kPrepConsumers + 1), 1)
+    k_bwd_prep(const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap to, const Prob p,
+               const float *__restrict__ lse, float *__restrict__ nlse2, float *__restrict__ ndvec, int ntasks,
+               unsigned *err) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled boxes need 1024-byte alignment
+        if (threadIdx.x == 0) set_error(err, 0x4FF);
+        return;
+    }
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kPrepStages * kPrepStage);
+    uint64_t *empty = full + kPrepStages;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(empty + kPrepStages);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = p.nQ * p.tile_q, groups = per / kPrepRows;
+    const int mine = ntasks > (int)blockIdx.x ? (ntasks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPrepStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
         }
-        const int s0 = g * kPrepRows;
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int issued[kPrepStages];
+#pragma unroll
+    for (int s = 0; s < kPrepStages; ++s) issued[s] = 0;
+    if (warp == kPrepConsumers) {
+        if (lane == 0) {
+            // ---------------------------------------------------- producer
+            tma_prefetch_desc(&tdo);
+            tma_prefetch_desc(&to);
+            for (int k = 0; k < mine; ++k) {
+                const int st = k % kPrepStages;
+                if (k >= kPrepStages &&
+                    !mbar_wait(empty + st, ((k / kPrepStages) - 1) & 1, s_abort, err, kSitePrepProd))
+                    break;
+                int b, h, s0;
+                prep_task(p, (int)blockIdx.x + k * (int)gridDim.x, groups, b, h, s0);
+                const int row = (p.layout == L_TND ? seq_start(p, true, b) : 0) + s0;
+                const int bc = p.layout == L_TND ? 0 : b;
+                uint8_t *dst = sm + st * kPrepStage;
+                mbar_expect_tx(full + st, kPrepStage);
+                tma_load_4d(dst, &tdo, full + st, 0, row, h, bc);
+                tma_load_4d(dst + kPrepBox, &tdo, full + st, 64, row, h, bc);
+                tma_load_4d(dst + 2 * kPrepBox, &to, full + st, 0, row, h, bc);
+                tma_load_4d(dst + 3 * kPrepBox, &to, full + st, 64, row, h, bc);
+                issued[st]++;
+            }
+            if (*s_abort) {  // drain this CTA's copies before it exits (bounded)
+                int never = 0;
+                for (int s = 0; s < kPrepStages; ++s)
+                    if (issued[s]) mbar_wait(full + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+            }
+        }
+        return;
+    }
+    // ------------------------------------------------------------ consumers
+    for (int k = warp; k < mine; k += kPrepConsumers) {
+        const int st = k % kPrepStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(full + st, (k / kPrepStages) & 1, s_abort, err, kSitePrepCons)))
+            break;
+        int b, h, s0;
+        prep_task(p, (int)blockIdx.x + k * (int)gridDim.x, groups, b, h, s0);
+        // row `lane` of the task: the two 64-column halves of dO and O
+        const uint8_t *base = sm + st * kPrepStage;
+        float acc = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t off = hf * kPrepBox + sw128_off(lane, u);
+                const uint4 x = *reinterpret_cast<const uint4 *>(base + off);
+                const uint4 y = *reinterpret_cast<const uint4 *>(base + 2 * kPrepBox + off);
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 a2 = unpack2<T>(xw[e]), c2 = unpack2<T>(yw[e]);
+                    acc = fmaf(a2.x, c2.x, acc);
+                    acc = fmaf(a2.y, c2.y, acc);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + st);  // the stage's rows are in registers
         const int len = p.layout == L_TND ? seq_len(p, true, b) : per;
-        float mine = 0.f;  // dO . O of slot s0 + lane
-#pragma unroll
-        for (int batch = 0; batch < 2; ++batch) {
-            uint4 av[8], cv[8];
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int s = s0 + batch * 16 + it * 2 + half;
-                av[it] = make_uint4(0, 0, 0, 0);
-                cv[it] = make_uint4(0, 0, 0, 0);
-                if (s < len) {
-                    const long long o = tok_off(p, true, b, s, h) + hl * 8;
-                    av[it] = __ldg(reinterpret_cast<const uint4 *>(dO + o));
-                    cv[it] = __ldg(reinterpret_cast<const uint4 *>(O + o));
-                }
-            }
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
-                const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
-                float acc = 0.f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 x = unpack2<T>(aw[u]), y = unpack2<T>(cw[u]);
-                    acc = fmaf(x.x, y.x, acc);
-                    acc = fmaf(x.y, y.y, acc);
-                }
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                const int r0 = batch * 16 + it * 2;  // half 0 summed row r0, half 1 row r0 + 1
-                const float v0 = __shfl_sync(0xffffffffu, acc, 0), v1 = __shfl_sync(0xffffffffu, acc, 16);
-                if (lane == r0) mine = v0;
-                if (lane == r0 + 1) mine = v1;
-            }
-        }
         const int s = s0 + lane;
         const bool ex = s < len;
         const long long slot = ((long long)b * p.Hq + h) * per + s;
-        ndvec[slot] = ex ? -mine : 0.f;
+        ndvec[slot] = ex ? -acc : 0.f;
         const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
         nlse2[slot] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
     }
@@ -1048,23 +1103,29 @@ cudaError_t launch_gate_grad(const Prob &p, const void *dO, const float *c, void
 }
 
 cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *nlse2,
-                            float *ndvec, cudaStream_t s) {
+                            float *ndvec, unsigned *err, cudaStream_t s) {
     const long long slots = (long long)p.B * p.Hq * p.nQ * p.tile_q;
     if (slots == 0) return cudaSuccess;
     if (slots > (long long)INT_MAX) return cudaErrorInvalidValue;
+    CUtensorMap tdo, to;
+    if (!make_tmap_rows(&tdo, p, true, dO, p.Hq, kPrepRows) || !make_tmap_rows(&to, p, true, o, p.Hq, kPrepRows))
+        return cudaErrorInvalidValue;
     const int ntasks = (int)(slots / kPrepRows);  // tile_q is a multiple of 32
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int want = (ntasks + 7) / 8;
-    const int blocks = want < sms * 2 ? want : sms * 2;  // every block resident (two per SM)
+    const int blocks = ntasks < sms ? ntasks : sms;  // one CTA per SM (the ring fills its shared memory)
+    const cudaError_t ae = p.dtype == T_BF16
+                               ? ensure_smem_limit((const void *)k_bwd_prep<__nv_bfloat16>, (int)kPrepSmem)
+                               : ensure_smem_limit((const void *)k_bwd_prep<__half>, (int)kPrepSmem);
+    if (ae != cudaSuccess) return ae;
     prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
-        k_bwd_prep<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)o,
-                                                        lse, nlse2, ndvec, ntasks);
+        k_bwd_prep<__nv_bfloat16><<<blocks, 32 * (kPrepConsumers + 1), kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec,
+                                                                                      ntasks, err);
     else
-        k_bwd_prep<__half><<<blocks, 256, 0, s>>>(p, (const __half *)dO, (const __half *)o, lse, nlse2, ndvec,
-                                                 ntasks);
+        k_bwd_prep<__half><<<blocks, 32 * (kPrepConsumers + 1), kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec,
+                                                                               ntasks, err);
     prof_end(s);
     return cudaGetLastError();
 }

@@ -111,14 +111,11 @@ cudaError_t copy_out(void *host, const void *src, const Strided &r, cudaStream_t
 }
 
 vsa_status check_groups(const vsa_desc *d, int groups, int topk, vsa_desc *slice, int *cap) {
-    if (!d) return VSA_ERR_NULL;
-    if (groups < 1 || d->Hkv < 1 || d->Hkv % groups != 0 || d->Hq % d->Hkv != 0) return VSA_ERR_SHAPE;
-    if (topk < 1 || d->nKV < 1) return VSA_ERR_SHAPE;
-    *slice = *d;
-    slice->Hq = d->Hq / groups;
-    slice->Hkv = d->Hkv / groups;
+    int q0 = 0, kv0 = 0;
+    const vsa_status st = vsa_head_slice(d, groups, 0, slice, &q0, &kv0);
+    if (st != VSA_OK) return st;
+    if (topk < 1) return VSA_ERR_SHAPE;
     *cap = topk < d->nKV ? topk : d->nKV;
-    if (vsa_workspace_size(slice, 0) == 0) return VSA_ERR_SHAPE;  // the rest of the descriptor checks
     return VSA_OK;
 }
 
@@ -126,6 +123,21 @@ vsa_status check_groups(const vsa_desc *d, int groups, int topk, vsa_desc *slice
 }  // namespace vsa
 
 using namespace vsa;
+
+extern "C" vsa_status vsa_head_slice(const vsa_desc *desc, int groups, int g, vsa_desc *slice, int32_t *q_head0,
+                                     int32_t *kv_head0) {
+    if (!desc || !slice || !q_head0 || !kv_head0) return VSA_ERR_NULL;
+    Prob p;
+    const vsa_status st = to_prob(desc, &p);  // every descriptor check of the other calls
+    if (st != VSA_OK) return st;
+    if (groups < 1 || desc->Hkv % groups != 0 || g < 0 || g >= groups) return VSA_ERR_SHAPE;
+    *slice = *desc;
+    slice->Hq = desc->Hq / groups;
+    slice->Hkv = desc->Hkv / groups;
+    *q_head0 = g * slice->Hq;
+    *kv_head0 = g * slice->Hkv;
+    return VSA_OK;
+}
 
 extern "C" size_t vsa_train_step_host_size(const vsa_desc *desc, int groups, int topk, int with_gate) {
     vsa_desc s;

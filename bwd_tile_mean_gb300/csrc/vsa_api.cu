@@ -453,7 +453,7 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
     float *ndvec = at<float>(workspace, L.ndvec), *nlse2 = at<float>(workspace, L.nlse2);
     a.ndvec = ndvec;
     a.nlse2 = nlse2;
-    VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, nlse2, ndvec, s));
+    VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, nlse2, ndvec, a.err, s));
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
         VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));

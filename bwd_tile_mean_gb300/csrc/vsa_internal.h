@@ -108,7 +108,7 @@ cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk,
 // dP - Dvec = dP + ndvec are single adds (slots past a varlen sequence's
 // end get nlse2 = -inf, ndvec = 0).
 cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const float *lse, float *nlse2,
-                            float *ndvec, cudaStream_t s);
+                            float *ndvec, unsigned *err, cudaStream_t s);
 struct BwdArgs {
     const void *dO, *q, *k, *v;
     const float *nlse2, *ndvec;   // padded tile layout, see launch_bwd_prep

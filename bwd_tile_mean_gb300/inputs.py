@@ -222,7 +222,8 @@ def tnd_problem(name, q_lens, kv_lens, Hq, Hkv, dtype="fp16", tile=128, seed=42,
 
 def config(n: int) -> Problem:
     """The five workloads (1: tiny VSA-256, 2: GQA varlen, 3: video DiT,
-    4: gated + ragged tiles, 5: long-video forward only)."""
+    4: gated + ragged tiles, 5: long-video forward only) and 6, the
+    long-video grid taken literally (1,024 tiles, ragged, forward only)."""
     if n == 1:
         return Problem("tiny-vsa256", "bhsd", 1, 2, 2, 128, 256, 256, 3, 4,
                        q_var=[256] * 3, kv_var=[256, 173, 79, 256], topk=2,
@@ -246,6 +247,15 @@ def config(n: int) -> Problem:
         return Problem("long-video-fwd", "bshd", 1, 24, 24, 128, 256, 256, 480, 480,
                        q_var=[256] * 480, kv_var=[256] * 480, topk=24, backward=False,
                        note="480 full tiles, 122,880 tokens, H24 D128 bf16 BSHD, topk 24, forward only")
+    if n == 6:
+        # the long-video grid taken literally: 32 x 60 x 128 tiled 4 x 8 x 8 is
+        # 8 x 8 x 16 = 1,024 tiles (H = 60 leaves a last row of half tiles:
+        # 896 tiles of 256 tokens, 128 of 128), 245,760 tokens
+        var = _video_tile_fill((32, 60, 128))
+        return Problem("long-video-literal-fwd", "bshd", 1, 24, 24, 128, 256, 256, len(var), len(var),
+                       q_var=var, kv_var=var, topk=24, backward=False,
+                       note="grid 32x60x128 -> 1,024 tiles (128 half tiles), 245,760 tokens, H24 D128 bf16 BSHD, "
+                            "topk 24, forward only")
     raise ValueError(n)
 
 

@@ -33,7 +33,7 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
            "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
            "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host", "vsa_step_host_status",
-           "vsa_check_inputs")
+           "vsa_check_inputs", "vsa_head_slice")
 
 
 class VsaError(RuntimeError):
@@ -124,6 +124,9 @@ def lib():
         L.vsa_check_inputs.restype = C.c_int
         L.vsa_check_inputs.argtypes = [C.POINTER(VsaDesc), P, P, P, P, C.c_int, P, P, P, C.c_size_t, P,
                                        C.POINTER(C.c_int32)]
+        L.vsa_head_slice.restype = C.c_int
+        L.vsa_head_slice.argtypes = [C.POINTER(VsaDesc), C.c_int, C.c_int, C.POINTER(VsaDesc), C.POINTER(C.c_int32),
+                                     C.POINTER(C.c_int32)]
         L.vsa_fwd_step_host.restype = C.c_int
         L.vsa_fwd_step_host.argtypes = [C.POINTER(VsaDesc), C.c_int, P, P, P, P, P, P, C.c_int, P, P, P, C.c_size_t,
                                         P]
@@ -211,6 +214,15 @@ def vsa_check_inputs(desc, q_var, kv_var, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx
     return int(st), int(code.value)
 
 
+def vsa_head_slice(desc, groups, g):
+    """Slice g of a problem's heads cut into `groups` (GQA groups whole):
+    returns (slice descriptor, first query head, first key/value head)."""
+    out, q0, kv0 = VsaDesc(), C.c_int32(0), C.c_int32(0)
+    _check("vsa_head_slice", lib().vsa_head_slice(C.byref(desc), int(groups), int(g), C.byref(out), C.byref(q0),
+                                                  C.byref(kv0)))
+    return out, int(q0.value), int(kv0.value)
+
+
 def vsa_device_status(workspace, stream=None) -> int:
     code = C.c_int32(0)
     lib().vsa_device_status(_p(workspace), _stream(stream), C.byref(code))
@@ -242,6 +254,15 @@ class profile:
 
 # ----------------------------------------------------------------------- Plan
 
+def describe(layout, dtype, B, Hq, Hkv, D, Sq, Skv, tile_q, tile_kv, nQ, nKV, cu_seqlens_q=None, cu_seqlens_kv=None,
+             scale=0.0) -> VsaDesc:
+    """A vsa_desc: layout "bhsd" | "bshd" | "tnd", dtype torch.bfloat16 |
+    torch.float16, sizes as in include/vsa.h (TND offsets: int32 device
+    tensors)."""
+    return VsaDesc(LAYOUTS[layout], DTYPES[dtype], B, Hq, Hkv, D, Sq, Skv, tile_q, tile_kv, nQ, nKV,
+                   _p(cu_seqlens_q), _p(cu_seqlens_kv), float(scale))
+
+
 class Plan:
     """Descriptor, workspace and index buffers of one problem.
 
@@ -259,8 +280,8 @@ class Plan:
         self.cu_q, self.cu_kv = cu_seqlens_q, cu_seqlens_kv
         self.q_var, self.kv_var = q_var, kv_var
         self.device = torch.device(device)
-        self.desc = VsaDesc(LAYOUTS[layout], DTYPES[dtype], B, Hq, Hkv, D, Sq, Skv, tile_q, tile_kv, nQ, nKV,
-                            _p(cu_seqlens_q), _p(cu_seqlens_kv), float(scale))
+        self.desc = describe(layout, dtype, B, Hq, Hkv, D, Sq, Skv, tile_q, tile_kv, nQ, nKV, cu_seqlens_q,
+                             cu_seqlens_kv, scale)
         ws = vsa_workspace_size(self.desc, gate)
         if ws == 0:
             raise ValueError("invalid problem description")

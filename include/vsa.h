@@ -289,6 +289,24 @@ vsa_status vsa_tile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH
 vsa_status vsa_untile_3d(int B, int T, int H, int W, int row_bytes, int tT, int tH, int tW,
                          const void *tiled, void *latent, vsa_stream_t stream);
 
+/* Head slices: every (batch, head) is an independent problem (the
+ * per-(batch, head) loops of [NPU-test]'s TND/GQA golden, with key/value
+ * head h / (Hq / Hkv) for query head h), so one problem's heads can be cut
+ * into `groups` equal slices, each with Hq/groups query heads and
+ * Hkv/groups key/value heads (Hkv % groups == 0, so every GQA group stays
+ * whole inside one slice). Slice g (0 <= g < groups) holds query heads
+ * [*q_head0, *q_head0 + slice->Hq) and key/value heads [*kv_head0,
+ * *kv_head0 + slice->Hkv); *slice is desc with those head counts. Running
+ * the calls above on each slice's tensors (the head slices of q, k, v, dO
+ * and of every output, LSE and block index included) gives results
+ * bit-identical to the whole problem's; this is how the host-buffer steps
+ * below pipeline a problem and how a problem is split over GPUs with no
+ * exchange between them. Host-only (no CUDA call). Errors: VSA_ERR_NULL,
+ * the descriptor errors of the other calls, VSA_ERR_SHAPE for groups < 1,
+ * Hkv % groups != 0 or g outside [0, groups). */
+vsa_status vsa_head_slice(const vsa_desc *desc, int groups, int g, vsa_desc *slice, int32_t *q_head0,
+                          int32_t *kv_head0);
+
 /* One training step (block map, forward, backward; with gate != NULL also
  * the gated compression branch) from HOST buffers, with the copies
  * overlapped with the kernels. Every head is an independent problem (the

@@ -106,7 +106,7 @@ def test_train_step_host_validation(L):
     assert call(buf=C.c_void_p((1 << 20) + 16)) == 7   # staging not 256-byte aligned
     assert call(nbytes=two - 1) == 7
     assert call(gate=FAKE) == 7                        # a gate needs the larger staging buffer
-    assert call(dd=desc(Hq=4, Hkv=2, dtype=5)) == 2    # the slice descriptor is checked too
+    assert call(dd=desc(Hq=4, Hkv=2, dtype=5)) == 3    # the descriptor is checked too (VSA_ERR_DTYPE)
     # the forward-only pipeline: out is required, the rest as above
     fwd = lambda out=FAKE, buf=C.c_void_p(1 << 20): L.vsa_fwd_step_host(C.byref(d), 2, FAKE, FAKE, FAKE, None, FAKE,
                                                                          FAKE, 2, out, None, buf, two, None)
@@ -155,3 +155,21 @@ def test_check_inputs_host_validation(L):
     assert call(ws=None) == 7
     assert call(ws=C.c_void_p((1 << 20) + 16)) == 7
     assert call(wsb=128) == 7
+
+
+def test_head_slice_host_logic(L):
+    d = desc(Hq=12, Hkv=3, Sq=768, Skv=1024)
+    seen = []
+    for g in range(3):
+        s, q0, kv0 = vsa.vsa_head_slice(d, 3, g)
+        assert (s.Hq, s.Hkv, q0, kv0) == (4, 1, 4 * g, g)
+        assert (s.B, s.D, s.Sq, s.Skv, s.nQ, s.nKV, s.tile_q) == (d.B, d.D, d.Sq, d.Skv, d.nQ, d.nKV, d.tile_q)
+        seen += list(range(q0, q0 + s.Hq))
+    assert seen == list(range(12))
+    for groups, g, code in ((2, 0, 2), (0, 0, 2), (3, 3, 2), (3, -1, 2)):   # Hkv % 2 != 0; groups < 1; g out of range
+        with pytest.raises(vsa.VsaError) as e:
+            vsa.vsa_head_slice(d, groups, g)
+        assert e.value.code == code
+    with pytest.raises(vsa.VsaError) as e:
+        vsa.vsa_head_slice(desc(D=64), 1, 0)
+    assert e.value.code == 5

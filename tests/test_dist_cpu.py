@@ -1,6 +1,7 @@
-"""Multi-rank host logic of bench.py on CPU (gloo, world size 2): every
-rank runs its own replica and the step time is the max over ranks; only
-rank 0 reports. Ranks are spawned as separate processes."""
+"""Multi-rank host logic on CPU (gloo, world size 2): the step time is the
+max over ranks and only rank 0 reports (bench.py); a problem's heads split
+over the ranks with vsa_head_slice cover every head exactly once with each
+GQA group inside one rank. Ranks are spawned as separate processes."""
 import os
 import socket
 
@@ -57,3 +58,41 @@ def test_reference_arm_other_ranks_print_nothing(capsys, monkeypatch):
 def test_single_rank_reduce_is_identity():
     import bench
     assert bench.reduce_max(3.5, 1, None) == 3.5
+
+
+def _slice_worker(rank, world, port, hq, hkv, out):
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from bwd_tile_mean_gb300 import vsa
+    d = vsa.VsaDesc(1, 0, 1, hq, hkv, 128, 76800, 76800, 256, 256, 300, 300, None, None, 0.0)
+    s, q0, kv0 = vsa.vsa_head_slice(d, world, rank)
+    mine = torch.tensor([q0, s.Hq, kv0, s.Hkv], dtype=torch.int64)
+    every = [torch.zeros(4, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(every, mine)
+    out.put((rank, [x.tolist() for x in every]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("hq,hkv", [(40, 40), (12, 2)])
+def test_head_slices_cover_every_head_once_over_two_gloo_ranks(hq, hkv):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_slice_worker, args=(r, 2, port, hq, hkv, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res[0] == res[1]                       # every rank sees the same split
+    g = hq // hkv
+    qheads, kvheads = [], []
+    for q0, nq, kv0, nkv in res[0]:
+        qheads += range(q0, q0 + nq)
+        kvheads += range(kv0, kv0 + nkv)
+        assert nq == nkv * g and q0 == kv0 * g    # whole GQA groups: query head h reads KV head h // g
+    assert sorted(qheads) == list(range(hq)) and sorted(kvheads) == list(range(hkv))

@@ -2,8 +2,11 @@
 benchmark times (one block-map + forward + backward step through the C
 ABI). The whole block map and both indices are compared bit for bit with
 the oracle; outputs are compared on samples the oracle computes one by one:
-query rows (O, LSE, dQ) and whole KV tiles (dK, dV) of two heads, each
-head checked on a one-head slice of the problem (heads are independent)."""
+query rows (O, LSE, dQ; random tiles plus the last two query tiles) and
+whole KV tiles (dK, dV: the most-selected, a median and the least-selected
+tile, and the most-selected partial one when tiles are ragged) of the first
+and the last head, each head checked on a one-head slice of the problem
+(heads are independent)."""
 import numpy as np
 import pytest
 import torch
@@ -32,8 +35,13 @@ def _one_head(p, t, h):
 
 
 def _sample_rows(p, rng, n):
+    """n rows of distinct random query tiles, plus the first and last rows
+    of the last two query tiles (the end of the grid)."""
     tiles = rng.choice(p.nQ, size=min(n, p.nQ), replace=False)
-    return np.asarray([(0, 0, int(i) * p.tile_q + int(rng.integers(p.tile_q))) for i in tiles], dtype=np.int32)
+    rows = [int(i) * p.tile_q + int(rng.integers(p.tile_q)) for i in tiles]
+    for i in (p.nQ - 2, p.nQ - 1):
+        rows += [i * p.tile_q, i * p.tile_q + p.tile_q - 1]
+    return np.asarray([(0, 0, s) for s in sorted(set(rows))], dtype=np.int32)
 
 
 def _pick(x, p, h, s):
@@ -83,32 +91,50 @@ def _run_full_size(p, heads, backward=True, n_rows=48):
         check_tol(f"{p.name} h{h} dq", rdq, got_dq, GRAD_TOL)
         if h % (p.Hq // p.Hkv):
             continue
-        # the least-selected non-empty KV tile keeps the oracle's work small
+        # KV tiles of this head's KV-owned index: the most-selected one (the
+        # longest KV-owned work list, many barrier-phase wraps), a median one
+        # and the least-selected non-empty one; with ragged tiles also the
+        # most-selected partial tile
         kp1, _ = orc.transpose(ph, qih, qch, ph.cap)
         cnt = np.diff(kp1[0, 0])
-        cand = [j for j in range(ph.nKV) if cnt[j] > 0 and ph.kv_var[j] > 0]
-        j = min(cand, key=lambda jj: cnt[jj])
+        cand = sorted((j for j in range(ph.nKV) if cnt[j] > 0 and ph.kv_var[j] > 0), key=lambda jj: (cnt[jj], jj))
+        picks = [cand[-1], cand[len(cand) // 2], cand[0]]
+        ragged = [j for j in cand if ph.kv_var[j] < ph.tile_kv]
+        if ragged:
+            picks.append(ragged[-1])
+        picks = list(dict.fromkeys(picks))
         rdk, rdv = orc.backward_dkdv_tiles(ph, th["dO"], th["q"], th["k"], th["v"], qih, qch, ph.cap,
-                                           gate=th.get("gate"), tiles=np.asarray([(0, 0, j)]), cgrads=cg)
+                                           gate=th.get("gate"), tiles=np.asarray([(0, 0, j) for j in picks]),
+                                           cgrads=cg)
         hk = h // (p.Hq // p.Hkv)
-        keys = range(j * p.tile_kv, (j + 1) * p.tile_kv)
-        got_dk = np.stack([_pick(dk, p, hk, s) for s in keys])
-        got_dv = np.stack([_pick(dv, p, hk, s) for s in keys])
-        check_tol(f"{p.name} h{h} dk tile {j}", rdk[0], got_dk, GRAD_TOL)
-        check_tol(f"{p.name} h{h} dv tile {j}", rdv[0], got_dv, GRAD_TOL)
+        for n, j in enumerate(picks):
+            keys = range(j * p.tile_kv, (j + 1) * p.tile_kv)
+            got_dk = np.stack([_pick(dk, p, hk, s) for s in keys])
+            got_dv = np.stack([_pick(dv, p, hk, s) for s in keys])
+            tag = f"{p.name} h{h} tile {j} ({cnt[j]} query tiles, {ph.kv_var[j]} keys)"
+            check_tol(f"{tag} dk", rdk[n], got_dk, GRAD_TOL)
+            check_tol(f"{tag} dv", rdv[n], got_dv, GRAD_TOL)
 
 
 def test_video_dit_76800_full_size():
-    _run_full_size(config(3), heads=[0, 23])
+    _run_full_size(config(3), heads=[0, 39])
 
 
 def test_gated_ragged_full_size():
-    _run_full_size(config(4), heads=[0, 13])
+    _run_full_size(config(4), heads=[0, 23])
 
 
 def test_long_video_inference_full_size():
     p = config(5)
-    _run_full_size(p, heads=[5], backward=False)
+    _run_full_size(p, heads=[5, 23], backward=False)
+
+
+def test_long_video_literal_grid_full_size():
+    # 32 x 60 x 128 tiled 4 x 8 x 8: 1,024 tiles, the last tile row of every
+    # frame block half full (128 tokens)
+    p = config(6)
+    assert p.nKV == 1024 and sorted(set(p.kv_var.tolist())) == [128, 256] and int((p.kv_var == 128).sum()) == 128
+    _run_full_size(p, heads=[0, 23], backward=False)
 
 
 def test_all_kv_tiles_empty():
