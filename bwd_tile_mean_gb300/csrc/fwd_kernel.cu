@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
+    if (a.redo_only && !a.redo[((long long)blockIdx.z * p.Hq + blockIdx.y) * p.nQ + blockIdx.x]) return;
     if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
         if (threadIdx.x == 0) set_error(a.err, 0x1FF);
         return;
@@ -456,6 +457,355 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
+// ------------------------------------------------ forward on a CTA pair
+// 256-token query tiles without query-block masks: a cluster of two CTAs
+// takes one tile, CTA r (its cluster rank) the 128-row group r. The even
+// CTA issues M = 256 MMAs (tcgen05 cta_group::2) for both: each CTA holds
+// its own 128 rows of Q, S, P and O, keys [64r, 64r + 64) of each 128-key
+// K chunk and head dims [64r, 64r + 64) of each V chunk, so a chunk costs
+// each SM 32 KB of loads for its 128 rows and six K/V stages fit beside Q.
+// TMEM holds three S buffers and O, so S(c+3) is issued right after
+// O += P(c) V(c). The loads of both CTAs complete on the even CTA's
+// barriers; every MMA commit arrives in both CTAs.
+// Softmax: the two warps of a TMEM lane quarter (32 rows) take alternate
+// chunks, each whole rows, so one warp's waits overlap the other's
+// exponentials. Every row's reference is its max over chunk 0, kept for
+// all chunks: fp32 and the 16-bit P keep their relative precision at any
+// magnitude, so nothing is rescaled. A chunk whose row sum passes
+// SumLimit (an element that the 16-bit P cannot hold) marks the tile in
+// `redo`; the single-CTA kernel, which moves its reference, recomputes
+// exactly those tiles right after.
+// Warp roles (each CTA): warps 0-7 softmax (warp w: TMEM lanes 32 (w % 4),
+// chunks of parity w / 4, and in the epilogue O columns [64 (w / 4), +64)),
+// warp 8 loads, warp 9 owns TMEM and (even CTA) issues the MMAs.
+// TMEM columns: S buffers [0,128), [128,256), [256,384) (P packed into the
+// first 64 columns of its S buffer), O [384,512).
+constexpr int kF2Stages = 6;
+constexpr int kF2Q = 32 * 1024;   // Q of the CTA's 128 rows: two 64-column boxes of 128 rows
+constexpr int kF2KH = 16 * 1024;  // half a K chunk: 64 keys x 128 dims, two 64-column boxes of 64 rows
+constexpr int kF2VH = 16 * 1024;  // half a V chunk: 128 keys x 64 dims, one box
+constexpr int kF2OffK = kF2Q, kF2OffV = kF2OffK + kF2Stages * kF2KH, kF2OffCtl = kF2OffV + kF2Stages * kF2VH;
+constexpr size_t kF2Smem = kF2OffCtl + 2560;
+constexpr int kF2Threads = 320, kF2ProdWarp = 8, kF2MmaWarp = 9;
+enum : unsigned { kSite2Prod = 0x111, kSite2Mma = 0x112, kSite2Soft = 0x113, kSite2Epi = 0x114 };
+
+// S = Q K_half^T for one chunk on the pair: A = the CTA's Q (boxes 16 KB
+// apart), B = its 64 keys (boxes 8 KB apart); 8 MMAs of K = 16.
+__device__ __forceinline__ void issue_qk2(uint32_t d, uint32_t aQ, uint32_t aK, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma2_ss_w(d, sdesc_sw128(aQ + (kk >> 2) * (kF2Q / 2) + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(aK + (kk >> 2) * (kF2KH / 2) + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
+}
+// O += P V_half on the pair: A = P in TMEM (128 keys packed in the S
+// buffer's first 64 columns, 8 per K = 16 step), B = the CTA's 64 head
+// dims of the chunk's 128 keys, read MN-major (8-key groups 1 KB apart).
+__device__ __forceinline__ void issue_pv2(uint32_t d, uint32_t p_tmem, uint32_t aV, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma2_ts_w(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kF2VH, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+template <typename T>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
+    k_fwd2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+           const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    const uint32_t rank = cluster_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x >> 1, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    // both CTAs of the pair take the same early exits, before any cluster interaction
+    const int tile_rows = p.layout == L_TND ? clampi(seq_len(p, true, b) - i * p.tile_q, 0, p.tile_q) : p.tile_q;
+    if (tile_rows == 0) {  // the whole tile lies outside its sequence
+        if (threadIdx.x == 0 && rank == 0 && a.redo) a.redo[((long long)b * p.Hq + h) * p.nQ + i] = 0;
+        return;
+    }
+    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_error(a.err, 0x1FE);
+        return;
+    }
+    const int nrows = clampi(tile_rows - (int)rank * 128, 0, 128);
+    const bool leader = rank == 0;
+    uint8_t *sQ = sm, *sK = sm + kF2OffK, *sV = sm + kF2OffV;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kF2OffCtl);
+    uint64_t *b_q = bars, *b_kv = bars + 1, *b_free = b_kv + kF2Stages, *b_s = b_free + kF2Stages;
+    uint64_t *b_p = b_s + 3, *b_o = b_p + 3, *b_fin = b_o + 1, *b_mref = b_fin + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 22 barriers (176 bytes)
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
+    volatile int *s_over = reinterpret_cast<volatile int *>(s_tmem + 3);       // a chunk passed SumLimit here
+    volatile int *s_over_peer = reinterpret_cast<volatile int *>(s_tmem + 4);  // the odd CTA's flag (even CTA)
+    float *s_mref = reinterpret_cast<float *>(sm + kF2OffCtl + 512);           // [128] rows' references
+    float *s_lsum = reinterpret_cast<float *>(sm + kF2OffCtl + 1024);          // [2][128] row-sum parts
+
+    const int qbase = (p.layout == L_TND ? seq_start(p, true, b) : 0) + i * p.tile_q + (int)rank * 128;
+    const int kvb = (p.layout == L_TND ? seq_start(p, false, b) : 0);
+    const int bc = (p.layout == L_TND ? 0 : b);
+    const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
+    const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);  // counts past idx_cap are invalid input
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_q, 1);
+        for (int s = 0; s < kF2Stages; ++s) {
+            mbar_init(b_kv + s, 1);
+            mbar_init(b_free + s, 1);
+        }
+        for (int x = 0; x < 3; ++x) {
+            mbar_init(b_s + x, 1);
+            mbar_init(b_p + x, 8);  // the 4 softmax warps of the chunk's parity in each CTA
+        }
+        mbar_init(b_o, 1);
+        mbar_init(b_fin, 1);
+        mbar_init(b_mref, 4);  // the four warps that take chunk 0
+        *s_abort = 0;
+        *s_over = 0;
+        *s_over_peer = 0;
+        fence_mbar_init();
+    }
+    if (warp == kF2ProdWarp) {
+        // number of 128-key chunks with valid keys (tile ids outside [0, nKV) skipped, as the walk does)
+        const int *idx = a.q_idx + qrow * a.cap;
+        const int per = p.tile_kv >> 7;
+        int total = 0;
+        for (int n = lane; n < cnt; n += 32) {
+            const int j = idx[n];
+            total += (j >= 0 && j < p.nKV) ? min(per, (kv_valid(p, b, j) + 127) >> 7) : 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+        if (lane == 0) *s_nchunk = total;
+    } else if (warp == kF2MmaWarp) {
+        tmem_alloc2(s_tmem, 512);
+        tmem_relinquish2();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tbase = *s_tmem;
+    const int N = *s_nchunk;
+    const bool bf16 = (p.dtype == T_BF16);
+    int issued_kv = 0, mma_started = 0;
+
+    if (warp == kF2ProdWarp && N > 0) {
+        // ------------------------------------------------------ producer (whole warp walks the chunks)
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, cnt, lane);
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const uint32_t cq = cluster_addr(smem_addr(b_q), 0);
+            if (leader) mbar_expect_tx(b_q, 2 * kF2Q);
+            tma_load_4d_pair(sQ, &tq, cq, 0, qbase, h, bc);
+            tma_load_4d_pair(sQ + kF2Q / 2, &tq, cq, 64, qbase, h, bc);
+        }
+        for (int c = 0; c < N; ++c) {
+            int crow = 0, cval = 0, cbits = -1;
+            if (!win_chunk(p, b, cw, c, lane, crow, cval, cbits)) break;
+            const int st = c % kF2Stages;
+            // the stage is free once O += P V of its previous chunk is done (in both CTAs)
+            if (c >= kF2Stages &&
+                !mbar_wait_warp(b_free + st, ((c / kF2Stages) - 1) & 1, s_abort, a.err, kSite2Prod))
+                break;
+            if (lane == 0) {
+                // one barrier round per chunk for K and V together (both CTAs' halves)
+                const uint32_t ckv = cluster_addr(smem_addr(b_kv + st), 0);
+                if (leader) mbar_expect_tx(b_kv + st, 2 * (kF2KH + kF2VH));
+                const int kr = kvb + crow;
+                uint8_t *dK = sK + st * kF2KH, *dV = sV + st * kF2VH;
+                tma_load_4d_pair(dK, &tk, ckv, 0, kr + (int)rank * 64, hk, bc);
+                tma_load_4d_pair(dK + kF2KH / 2, &tk, ckv, 64, kr + (int)rank * 64, hk, bc);
+                tma_load_4d_pair(dV, &tv, ckv, (int)rank * 64, kr, hk, bc);
+            }
+            issued_kv = c + 1;
+        }
+    } else if (warp == kF2MmaWarp && leader && N > 0) {
+        // ------------------------------------------- MMA issuer of the pair (whole warp, one lane issues)
+        const uint32_t idS = idesc_f16(bf16, 256, 128, false, false);
+        const uint32_t idO = idesc_f16(bf16, 256, 128, false, true);
+        const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
+        const uint32_t tO = tbase + 384;
+        bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSite2Mma);
+        for (int c = 0; ok && c < 3 && c < N; ++c) {
+            const int st = c % kF2Stages;
+            if (!(ok = mbar_wait_warp(b_kv + st, (c / kF2Stages) & 1, s_abort, a.err, kSite2Mma))) break;
+            tc_fence_after();
+            issue_qk2(tbase + c * 128, aQ, aK + st * kF2KH, idS);
+            mma2_commit_mc_w(b_s + c, 3);
+            mma_started = 1;
+        }
+        for (int c = 0; ok && c < N; ++c) {
+            const int st = c % kF2Stages, x = c % 3;
+            if (!(ok = mbar_wait_warp(b_p + x, (c / 3) & 1, s_abort, a.err, kSite2Mma))) break;
+            tc_fence_after();
+            issue_pv2(tO, tbase + x * 128, aV + st * kF2VH, idO, c > 0);  // O += P(c) V(c)
+            mma2_commit_mc_w(b_free + st, 3);  // K(c), V(c) read; O holds chunks 0..c
+            const int n = c + 3;
+            if (n < N) {
+                const int sn = n % kF2Stages;
+                if (!(ok = mbar_wait_warp(b_kv + sn, (n / kF2Stages) & 1, s_abort, a.err, kSite2Mma))) break;
+                tc_fence_after();
+                issue_qk2(tbase + x * 128, aQ, aK + sn * kF2KH, idS);  // S(c+3) over P(c), read by the PV above
+                mma2_commit_mc_w(b_s + x, 3);
+            }
+        }
+        if (ok) mma2_commit_mc_w(b_o, 3);
+    } else if (warp < 8) {
+        // ------------------------------------------------------ softmax + epilogue
+        const int lg = warp & 3, grp = warp >> 2;  // lane quarter, parity of the chunks this warp takes
+        const int r = lg * 32 + lane;             // row within the CTA's group
+        const uint32_t tl = tbase + ((uint32_t)(lg * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        float m_ref = -INFINITY, l = 0.f;  // l: the part of the row sum from this warp's chunks
+        bool ok = true, over = false;
+        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, cnt, lane);
+        const uint32_t cp0 = cluster_addr(smem_addr(b_p), 0);
+        for (int c = grp; c < N; c += 2) {
+            const int x = c % 3;
+            int crow = 0, valid = 0, cbits = -1;
+            win_chunk(p, b, cw, c, lane, crow, valid, cbits);
+            if (!(ok = mbar_wait_warp(b_s + x, (c / 3) & 1, s_abort, a.err, kSite2Soft))) break;
+            tc_fence_after();
+            uint32_t sr[128];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld32(tl + x * 128 + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + q4 * 32));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(sr + q4 * 32));
+            if (valid < 128) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+            }
+            if (c == 0) {
+                // the row's reference: its max over the first chunk (every
+                // chunk holds at least one valid key, so it is finite)
+                float u[43], v[15], w5[5];
+#pragma unroll
+                for (int k = 0; k < 42; ++k)
+                    u[k] = fmax3(__uint_as_float(sr[3 * k]), __uint_as_float(sr[3 * k + 1]),
+                                 __uint_as_float(sr[3 * k + 2]));
+                u[42] = fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127]));
+#pragma unroll
+                for (int k = 0; k < 14; ++k) v[k] = fmax3(u[3 * k], u[3 * k + 1], u[3 * k + 2]);
+                v[14] = u[42];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) w5[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+                m_ref = fmaxf(fmax3(w5[0], w5[1], w5[2]), fmaxf(w5[3], w5[4])) * sl2;
+                s_mref[r] = m_ref;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_mref);
+            } else if (m_ref == -INFINITY) {  // this warp's first chunk: take chunk 0's reference
+                if (!(ok = mbar_wait_warp(b_mref, 0, s_abort, a.err, kSite2Soft))) break;
+                m_ref = s_mref[r];
+            }
+            const float ls = exp_row<T>(sr, m_ref, sl2, tl + x * 128);
+            over = over || !(ls <= SumLimit<T>::value);
+            l += ls;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cp0 + 8u * x);
+        }
+        if (__any_sync(0xffffffffu, over) && lane == 0) *s_over = 1;
+        if (ok && N > 0) {
+            ok = mbar_wait_warp(b_o, 0, s_abort, a.err, kSite2Epi);
+            if (ok) tc_fence_after();
+        }
+        // the row sum: both warps' parts (every softmax warp comes here once)
+        s_lsum[grp * 128 + r] = l;
+        named_sync(1, 256);
+        const float lt = s_lsum[r] + s_lsum[128 + r];
+        // the O columns of this warp: [64 grp, 64 grp + 64)
+        const int ch = grp;
+        const bool have = ok && N > 0;                  // warp-uniform: TMEM holds O
+        const bool row_has = have && lt > 0.f;          // lt = 0: the row saw no key (O = 0, LSE = -inf)
+        const float inv_l = row_has ? 1.f / lt : 0.f;
+        const float lse_v = row_has ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
+        const bool row_ok = r < nrows;
+        const int row = i * p.tile_q + (int)rank * 128 + r;  // within the batch entry
+        const long long ro = tok_off(p, true, b, row, h) + ch * 64;
+        T *osp = a.o_sparse ? reinterpret_cast<T *>(a.o_sparse) + ro : nullptr;
+        T *out = reinterpret_cast<T *>(a.out) + ro;
+        const T *gt = a.gate ? reinterpret_cast<const T *>(a.gate) + ro : nullptr;
+        const float *cc = a.gate ? a.c + qrow * 128 + ch * 64 : nullptr;
+#pragma unroll 1
+        for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t o[32];
+            if (have) {
+                tmem_ld32(tl + 384 + ch * 64 + q2 * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = 0u;
+            }
+            if (!row_ok) continue;
+            float vals[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(o[j]) * inv_l;
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pack2<T>(vals[2 * j], vals[2 * j + 1]);
+            if (osp) {
+                uint4 *dst = reinterpret_cast<uint4 *>(osp + q2 * 32);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+            if (gt) {
+                const uint4 *gsrc = reinterpret_cast<const uint4 *>(gt + q2 * 32);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 gv = gsrc[u];
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 g2 = unpack2<T>(gw[t]);
+                        const int e = q2 * 32 + u * 8 + t * 2;
+                        w[u * 4 + t] = pack2<T>(vals[u * 8 + t * 2] + g2.x * cc[e],
+                                                vals[u * 8 + t * 2 + 1] + g2.y * cc[e + 1]);
+                    }
+                }
+            }
+            if (gt || out != osp) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + q2 * 32);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+        }
+        if (row_ok && ch == 0 && a.lse) a.lse[lse_off(p, b, h, row)] = lse_v;
+    }
+
+    // ------------------------------------------------------------ teardown
+    if (*s_abort) {
+        // Loads of both CTAs complete on the even CTA's barriers, which a
+        // half-fed phase never completes: give copies in flight time to land
+        // before this CTA's shared memory can be released.
+        if (warp == kF2ProdWarp && lane == 0 && issued_kv + 1 > 0) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 100000ull) {
+            }
+        }
+        if (warp == kF2MmaWarp && mma_started) {  // the pair's MMAs finish before TMEM is released
+            int never = 0;
+            mma2_commit_mc_w(b_fin, 1);
+            __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
+        }
+    }
+    // the odd CTA's overflow flag goes to the even CTA, which records the tile
+    if (!leader && threadIdx.x == 0) {
+        const uint32_t dst = cluster_addr(smem_addr(const_cast<int *>(s_over_peer)), 0);
+        const int v = *s_over;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(v) : "memory");
+    }
+    tc_fence_before();
+    cluster_sync();  // neither CTA leaves while the other may still touch its barriers or TMEM
+    if (leader && threadIdx.x == 0 && a.redo) a.redo[qrow] = (*s_over || *s_over_peer) ? 1 : 0;
+    if (warp == kF2MmaWarp) {
+        tc_fence_after();
+        tmem_dealloc2(tbase, 512);
+    }
+}
+
 // ----------------------------------------------------- compression fwd
 // One block per (b, h, query tile): a_j = scale pq . pk_j over non-empty
 // KV tiles, A = softmax(a), c[e] = sum_j A_j pv_j[e] (fp32).
@@ -516,16 +866,38 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
         !make_tmap_rows(&tv, p, false, a.v, p.Hkv))
         return cudaErrorInvalidValue;
+    if (p.nQ == 0 || p.Hq == 0 || p.B == 0) return cudaSuccess;
+    FwdArgs a1 = a;
+    a1.redo_only = 0;
+    if (p.tile_q == 256 && !a.q_sub && a.redo) {
+        // a CTA pair per 256-token query tile; the tiles it marks in redo
+        // are then recomputed by the single-CTA kernel below
+        CUtensorMap tk2;
+        if (!make_tmap_rows(&tk2, p, false, a.k, p.Hkv, 64)) return cudaErrorInvalidValue;
+        dim3 grid2(2 * p.nQ, p.Hq, p.B);
+        const cudaError_t ae = p.dtype == T_BF16
+                                   ? ensure_smem_limit((const void *)k_fwd2<__nv_bfloat16>, (int)kF2Smem)
+                                   : ensure_smem_limit((const void *)k_fwd2<__half>, (int)kF2Smem);
+        if (ae != cudaSuccess) return ae;
+        prof_begin("fwd_attn", s);
+        if (p.dtype == T_BF16)
+            k_fwd2<__nv_bfloat16><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, p, a1);
+        else
+            k_fwd2<__half><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, p, a1);
+        prof_end(s);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        a1.redo_only = 1;
+    }
     dim3 grid(p.nQ, p.Hq, p.B);
-    if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
     const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_fwd<__nv_bfloat16>, (int)kFwdSmem)
                                              : ensure_smem_limit((const void *)k_fwd<__half>, (int)kFwdSmem);
     if (ae != cudaSuccess) return ae;
-    prof_begin("fwd_attn", s);
+    prof_begin(a1.redo_only ? "fwd_redo" : "fwd_attn", s);
     if (p.dtype == T_BF16)
-        k_fwd<__nv_bfloat16><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a);
+        k_fwd<__nv_bfloat16><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a1);
     else
-        k_fwd<__half><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a);
+        k_fwd<__half><<<grid, kFwdThreads, kFwdSmem, s>>>(tq, tk, tv, p, a1);
     prof_end(s);
     return cudaGetLastError();
 }

@@ -227,7 +227,7 @@ vsa_status run_block_map(const Prob &p, const void *q, const void *k, int topk, 
 namespace {
 
 struct WsLayout {
-    size_t pq, pk, pv, c, nlse2, ndvec, dc, A, ds, dpq, dpk, dpv, total;
+    size_t pq, pk, pv, c, nlse2, ndvec, redo, dc, A, ds, dpq, dpk, dpv, total;
 };
 
 WsLayout ws_layout(const Prob &p, bool gate) {
@@ -244,6 +244,7 @@ WsLayout ws_layout(const Prob &p, bool gate) {
     L.pk = take(fk);
     L.nlse2 = take(slots * 4);
     L.ndvec = take(slots * 4);
+    L.redo = take((size_t)p.B * p.Hq * p.nQ);
     if (gate) {
         L.pv = take(fk);
         L.c = take(fq);
@@ -363,6 +364,7 @@ vsa_status fwd_impl(const vsa_desc *desc, const void *q, const void *k, const vo
     a.q_sub = q_sub;
     a.block_q = block_q;
     a.err = at<unsigned>(workspace, 0);
+    a.redo = at<uint8_t>(workspace, L.redo);
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
         VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));

@@ -97,6 +97,68 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
     return __half22float2(*reinterpret_cast<__half2 *>(&w));
 }
 
+// The 128-key chunks of a query tile's selected KV tiles, walked by a whole
+// warp: a window of up to 32 selected tiles sits one tile per lane (tile
+// id, valid key count, chunk count and first chunk within the window), so
+// the index is read once per 32 tiles rather than once per chunk, and a
+// chunk's tile is found with a ballot. All lanes call with the same c.
+struct ChunkWin {
+    const int *idx, *sub;  // sub: query-block bit masks of the entries (NULL: whole tiles)
+    int cnt, per;
+    int n0, c0, chunks;  // first tile and first chunk of the window; chunks in it
+    int j, kvv, nch, first, bits;  // this lane's tile
+};
+__device__ __forceinline__ void win_load(const Prob &p, int b, ChunkWin &w, int lane) {
+    const int n = w.n0 + lane;
+    w.j = n < w.cnt ? w.idx[n] : 0;
+    // tile ids outside [0, nKV) (invalid input) contribute no chunk
+    w.kvv = (n < w.cnt && w.j >= 0 && w.j < p.nKV) ? kv_valid(p, b, w.j) : 0;
+    w.bits = (n < w.cnt && w.sub) ? w.sub[n] : -1;
+    w.nch = min(w.per, (w.kvv + 127) >> 7);
+    int inc = w.nch;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    w.first = inc - w.nch;
+    w.chunks = __shfl_sync(0xffffffffu, inc, 31);
+}
+__device__ __forceinline__ ChunkWin win_begin(const Prob &p, int b, const int *idx, const int *sub, int cnt,
+                                               int lane) {
+    ChunkWin w;
+    w.idx = idx;
+    w.sub = sub;
+    w.cnt = cnt;  // already clamped into [0, idx_cap] by the caller
+    w.per = p.tile_kv >> 7;
+    w.n0 = 0;
+    w.c0 = 0;
+    win_load(p, b, w, lane);
+    return w;
+}
+// Row (of the KV tile's first key, within the batch entry) and valid key
+// count of chunk c; chunks are visited in increasing order.
+__device__ __forceinline__ bool win_chunk(const Prob &p, int b, ChunkWin &w, int c, int lane, int &row, int &valid,
+                                          int &bits) {
+    while (c >= w.c0 + w.chunks) {
+        if (w.n0 + 32 >= w.cnt) return false;
+        w.c0 += w.chunks;
+        w.n0 += 32;
+        win_load(p, b, w, lane);
+    }
+    const int cw = c - w.c0;
+    const unsigned m = __ballot_sync(0xffffffffu, w.nch > 0 && w.first <= cw);
+    const int L = 31 - __clz(m);
+    const int first = __shfl_sync(0xffffffffu, w.first, L);
+    const int kvv = __shfl_sync(0xffffffffu, w.kvv, L);
+    const int j = __shfl_sync(0xffffffffu, w.j, L);
+    bits = __shfl_sync(0xffffffffu, w.bits, L);
+    const int sub = cw - first;
+    row = j * p.tile_kv + sub * 128;
+    valid = min(128, kvv - sub * 128);
+    return true;
+}
+
 // Device status word (first bytes of the caller's workspace).
 __device__ __forceinline__ void set_error(unsigned *err, unsigned code) {
     if (err) atomicCAS(err, 0u, code);

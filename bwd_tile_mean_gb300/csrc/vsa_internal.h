@@ -92,6 +92,8 @@ struct FwdArgs {
     const int *q_sub;   // per-entry query-block bit masks (NULL: whole tiles)
     int block_q;        // rows per query block when q_sub != NULL
     unsigned *err;
+    uint8_t *redo;      // [B, Hq, nQ] tiles the CTA-pair kernel hands to the single-CTA one
+    int redo_only;      // single-CTA kernel: compute only the tiles marked in redo
 };
 cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s);
 

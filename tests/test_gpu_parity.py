@@ -178,6 +178,30 @@ def test_forward_parity(p):
     _fwd_check(p, t, plan, g, qi, qc)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_scores_far_above_the_first_chunk(dtype):
+    # Every row's scores on the last KV tile lie far above its max over the
+    # first chunk (q has a common component, that tile's keys are 6 plus half
+    # their drawn values), by more than a 16-bit P relative to that max can
+    # hold: the forward must move its reference (the tiles are recomputed by
+    # the kernel that does) and the outputs and gradients still match the
+    # oracle.
+    p = Problem(f"far-scores-{dtype}", "bshd", 1, 2, 2, 128, 256, 256, 2, 4, q_var=[256, 256],
+                kv_var=[256, 256, 200, 256], topk=4, seed=81, dtype=dtype)
+    t = make_tensors(p)
+    T = t["q"].dtype
+    t["q"] = (t["q"].float() * 0.5 + 1.0).to(T)
+    k = t["k"].float()
+    k[:, 3 * 256:] = 6.0 + 0.5 * k[:, 3 * 256:]
+    t["k"] = k.to(T)
+    plan, g = run_map(p, t)
+    _, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    assert np.all(qc == 4)  # every query tile attends to every KV tile, the far one last
+    _fwd_check(p, t, plan, g, qi, qc)
+    ref = orc.run_full(p, t)
+    _bwd_check(p, t, plan, g, ref)
+
+
 @pytest.mark.parametrize("p", [config(2)] + [npu_problem(c) for c in load_golden("npu_tnd_cases.json")["cases"]],
                          ids=lambda p: p.name)
 def test_forward_parity_varlen_mask(p):
