@@ -267,6 +267,40 @@ def head_shard(p, t, ws, rank, dev):
     return ps, ts, (q0, sd.Hq)
 
 
+def host_link(h_in, d_in, h_out, d_out, dev, stream, e0, e1, reps=3):
+    """This machine's host<->device copy rates (GB/s) for one contiguous tensor
+    from / to pinned memory: each direction alone and both at once (the
+    host-buffer step moves its inputs and outputs through this link)."""
+    import torch
+    nb = h_in.numel() * h_in.element_size()
+    side = torch.cuda.Stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    def both():
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            h_out.copy_(d_out, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        stream.wait_stream(side)
+
+    scratch = torch.empty_like(d_in)
+    h2d = timed(lambda: scratch.copy_(h_in, non_blocking=True))
+    d2h = timed(lambda: h_out.copy_(d_out, non_blocking=True))
+    d_in, scratch = scratch, d_in  # both(): write the scratch copy, leave the input tensor as it is
+    bi = timed(both)
+    return {"h2d": round(nb / h2d / 1e6, 1), "d2h": round(nb / d2h / 1e6, 1),
+            "both_each_way": round(nb / bi / 1e6, 1), "bytes_per_copy": nb}
+
+
 def ours(args):
     import torch
 
@@ -379,14 +413,22 @@ def ours(args):
             plan.fwd_step_host(host_in["q"], host_in["k"], host_in["v"], p.topk, groups, gate=host_in.get("gate"),
                                out=host_out["out"], stream=stream)
 
-    e2e_step()
-    barrier()
-    e0.record(stream)
-    for _ in range(e_steps):
+    link = host_link(host_in["q"], q, host_out["out"], out, dev, stream, e0, e1)
+    for _ in range(args.warmup):
         e2e_step()
+    barrier()
+    # one event per call as well, so that a call stalled by the host link
+    # shows up in the line (the value stays the mean over all calls)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps + 1)]
+    e0.record(stream)
+    marks[0].record(stream)
+    for i in range(e_steps):
+        e2e_step()
+        marks[i + 1].record(stream)
     e1.record(stream)
     barrier()
     e2e_ms = reduce_max(e0.elapsed_time(e1) / e_steps, ws, dev)
+    per_call = [marks[i].elapsed_time(marks[i + 1]) for i in range(e_steps)]
     job_h2d, job_d2h = int(reduce_sum(h2d, ws, dev)), int(reduce_sum(d2h, ws, dev))
 
     # the layout step on either side of the attention: 3D tiling of the
@@ -446,7 +488,10 @@ def ours(args):
         "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": job_h2d, "d2h_bytes_per_step": job_d2h,
                 "path": f"{'vsa_train_step_host' if train else 'vsa_fwd_step_host'}: {groups} head slices, "
-                        "copies overlapped with the kernels"},
+                        "copies overlapped with the kernels",
+                "host_link_GB_per_s": link, "calls": e_steps,
+                "call_ms": {"median": round(statistics.median(per_call), 3), "min": round(min(per_call), 3),
+                            "max": round(max(per_call), 3)}},
         "gpu_launches": launches, "clocks": clocks,
         "layout_step": {"bound": "hbm", "peak_GB_per_s": pk.get("hbm_gbs"), **layout},
         "kernels": {n: {"avg_ms": round(x["avg_ms"], 4), "launches_per_step": x["launches"] // args.steps,

@@ -24,9 +24,12 @@
 // layout (BSHD/TND: a run of Hs*D elements per token; BHSD: a run of
 // Hs*S*D per batch entry), copied with cudaMemcpy2DAsync. The step per
 // slice calls the same entry points as a device caller (vsa_build_block_map,
-// vsa_fwd, vsa_bwd on the slice's descriptor), so results are bit-identical
-// to running the whole problem on the device; with a gate, the gated
-// compression branch runs too (its tile means are per head as well). No
+// vsa_fwd_reuse, vsa_bwd_reuse on the slice's descriptor), so results are
+// bit-identical to running the whole problem on the device; with a gate, the
+// gated compression branch runs too (its tile means are per head as well,
+// and the three calls of a slice share its staging workspace, so q's and
+// k's means are pooled once, by the block map, and v's once, by the
+// forward). No
 // device memory is allocated here: the caller provides the staging buffer.
 #include <cstdint>
 
@@ -221,14 +224,14 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
         ok = vs(vsa_build_block_map(&sd, base + L.q, base + L.k, q_var, kv_var, topk, train ? 1 : 0, base + L.map,
                                     qidx, qcnt, cap, train ? kvptr : nullptr, train ? kvqidx : nullptr, ws,
                                     L.ws_bytes, stream)) &&
-             vs(vsa_fwd(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, g_d, base + L.out,
-                        lse_d, osp_d, ws, L.ws_bytes, stream)) &&
+             vs(vsa_fwd_reuse(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, g_d,
+                              base + L.out, lse_d, osp_d, VSA_REUSE_QK_MEANS, ws, L.ws_bytes, stream)) &&
              cu(cudaEventRecord(ev_fwd[slot], sc));
         if (ok && train)
             ok = cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
-                 vs(vsa_bwd(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out, lse_d,
-                            qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk, base + L.dv,
-                            ws, L.ws_bytes, stream));
+                 vs(vsa_bwd_reuse(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out,
+                                  lse_d, qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk,
+                                  base + L.dv, VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS, ws, L.ws_bytes, stream));
         ok = ok && cu(cudaEventRecord(ev_comp[slot], sc));
         // outputs of slice g: O and LSE are final after the forward, the
         // gradients after the backward

@@ -94,11 +94,12 @@ cudaError_t launch_pools(const Prob &p, const PoolSegs &segs_in, cudaStream_t s)
 
 cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
                             float *pv, cudaStream_t s) {
+    // a tensor given as NULL is not pooled (its means are kept from an earlier call)
     PoolSegs segs{};
-    segs.s[0] = PoolSeg{q, pq, 1, 0};
-    segs.s[1] = PoolSeg{k, pk, 0, 0};
-    segs.s[2] = PoolSeg{v, pv, 0, 0};
-    segs.n = v ? 3 : 2;
+    if (q) segs.s[segs.n++] = PoolSeg{q, pq, 1, 0};
+    if (k) segs.s[segs.n++] = PoolSeg{k, pk, 0, 0};
+    if (v) segs.s[segs.n++] = PoolSeg{v, pv, 0, 0};
+    if (segs.n == 0) return cudaSuccess;
     return launch_pools(p, segs, s);
 }
 

@@ -335,8 +335,9 @@ vsa_status vsa_mask_to_index(const vsa_desc *desc, const uint8_t *block_map, con
 namespace {
 vsa_status fwd_impl(const vsa_desc *desc, const void *q, const void *k, const void *v, const int32_t *q_idx,
                     const int32_t *q_cnt, const int32_t *q_sub, int block_q, int idx_cap, const int32_t *q_var,
-                    const int32_t *kv_var, const void *gate, void *out, float *lse, void *o_sparse,
+                    const int32_t *kv_var, const void *gate, void *out, float *lse, void *o_sparse, int reuse,
                     void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
+    if ((reuse & ~(VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS)) != 0) return VSA_ERR_SHAPE;
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
     VSA_TRY(need_vars(p0, q_var, kv_var, &p, gate != nullptr));
@@ -367,7 +368,8 @@ vsa_status fwd_impl(const vsa_desc *desc, const void *q, const void *k, const vo
     a.redo = at<uint8_t>(workspace, L.redo);
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
-        VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));
+        const bool qk = (reuse & VSA_REUSE_QK_MEANS) == 0, vv = (reuse & VSA_REUSE_V_MEANS) == 0;
+        VSA_CUDA(launch_pool_qkv(p, qk ? q : nullptr, pq, qk ? k : nullptr, pk, vv ? v : nullptr, pv, s));
         a.c = at<float>(workspace, L.c);
         VSA_CUDA(launch_compress_fwd(p, pq, pk, pv, const_cast<float *>(a.c), s));
     }
@@ -380,8 +382,16 @@ vsa_status vsa_fwd(const vsa_desc *desc, const void *q, const void *k, const voi
                    const int32_t *q_cnt, int idx_cap, const int32_t *q_var, const int32_t *kv_var,
                    const void *gate, void *out, float *lse, void *o_sparse, void *workspace,
                    size_t workspace_bytes, vsa_stream_t stream) {
-    return fwd_impl(desc, q, k, v, q_idx, q_cnt, nullptr, 0, idx_cap, q_var, kv_var, gate, out, lse, o_sparse,
+    return fwd_impl(desc, q, k, v, q_idx, q_cnt, nullptr, 0, idx_cap, q_var, kv_var, gate, out, lse, o_sparse, 0,
                     workspace, workspace_bytes, stream);
+}
+
+vsa_status vsa_fwd_reuse(const vsa_desc *desc, const void *q, const void *k, const void *v, const int32_t *q_idx,
+                         const int32_t *q_cnt, int idx_cap, const int32_t *q_var, const int32_t *kv_var,
+                         const void *gate, void *out, float *lse, void *o_sparse, int reuse, void *workspace,
+                         size_t workspace_bytes, vsa_stream_t stream) {
+    return fwd_impl(desc, q, k, v, q_idx, q_cnt, nullptr, 0, idx_cap, q_var, kv_var, gate, out, lse, o_sparse,
+                    reuse, workspace, workspace_bytes, stream);
 }
 
 vsa_status vsa_fwd_blocks(const vsa_desc *desc, int block_q, const void *q, const void *k, const void *v,
@@ -392,7 +402,7 @@ vsa_status vsa_fwd_blocks(const vsa_desc *desc, int block_q, const void *q, cons
     if (block_q < 32 || block_q > desc->tile_q || desc->tile_q % block_q != 0 || block_q % 32 != 0)
         return VSA_ERR_SHAPE;
     return fwd_impl(desc, q, k, v, q_idx, q_cnt, q_sub, block_q, idx_cap, q_var, kv_var, nullptr, out, lse,
-                    nullptr, workspace, workspace_bytes, stream);
+                    nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 vsa_status vsa_gate_grad(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
@@ -420,7 +430,9 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
                     const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt,
                     const int32_t *q_sub, int block_q, int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx,
                     const int32_t *kv_qsub, const int32_t *q_var, const int32_t *kv_var, const void *gate,
-                    void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
+                    void *dq, void *dk, void *dv, int reuse, void *workspace, size_t workspace_bytes,
+                    vsa_stream_t stream) {
+    if ((reuse & ~(VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS)) != 0) return VSA_ERR_SHAPE;
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
     VSA_TRY(need_vars(p0, q_var, kv_var, &p, true));
@@ -458,7 +470,8 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
     VSA_CUDA(launch_bwd_prep(p, dO, o_sparse, lse, nlse2, ndvec, a.err, s));
     if (gate) {
         float *pq = at<float>(workspace, L.pq), *pk = at<float>(workspace, L.pk), *pv = at<float>(workspace, L.pv);
-        VSA_CUDA(launch_pool_qkv(p, q, pq, k, pk, v, pv, s));
+        const bool qk = (reuse & VSA_REUSE_QK_MEANS) == 0, vv = (reuse & VSA_REUSE_V_MEANS) == 0;
+        VSA_CUDA(launch_pool_qkv(p, qk ? q : nullptr, pq, qk ? k : nullptr, pk, vv ? v : nullptr, pv, s));
         float *dpq = at<float>(workspace, L.dpq), *dpk = at<float>(workspace, L.dpk),
               *dpv = at<float>(workspace, L.dpv);
         VSA_CUDA(launch_compress_bwd(p, dO, gate, pq, pk, pv, at<float>(workspace, L.dc), at<float>(workspace, L.A),
@@ -479,7 +492,16 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    const void *gate, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
                    vsa_stream_t stream) {
     return bwd_impl(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, nullptr, 0, idx_cap, kv_ptr, kv_qidx, nullptr,
-                    q_var, kv_var, gate, dq, dk, dv, workspace, workspace_bytes, stream);
+                    q_var, kv_var, gate, dq, dk, dv, 0, workspace, workspace_bytes, stream);
+}
+
+vsa_status vsa_bwd_reuse(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                         const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt,
+                         int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var,
+                         const int32_t *kv_var, const void *gate, void *dq, void *dk, void *dv, int reuse,
+                         void *workspace, size_t workspace_bytes, vsa_stream_t stream) {
+    return bwd_impl(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, nullptr, 0, idx_cap, kv_ptr, kv_qidx, nullptr,
+                    q_var, kv_var, gate, dq, dk, dv, reuse, workspace, workspace_bytes, stream);
 }
 
 vsa_status vsa_bwd_blocks(const vsa_desc *desc, int block_q, const void *dO, const void *q, const void *k,
@@ -492,7 +514,7 @@ vsa_status vsa_bwd_blocks(const vsa_desc *desc, int block_q, const void *dO, con
     if (block_q < 32 || block_q > desc->tile_q || desc->tile_q % block_q != 0 || block_q % 32 != 0)
         return VSA_ERR_SHAPE;
     return bwd_impl(desc, dO, q, k, v, out, lse, q_idx, q_cnt, q_sub, block_q, idx_cap, kv_ptr, kv_qidx, kv_qsub,
-                    q_var, kv_var, nullptr, dq, dk, dv, workspace, workspace_bytes, stream);
+                    q_var, kv_var, nullptr, dq, dk, dv, 0, workspace, workspace_bytes, stream);
 }
 
 vsa_status vsa_mask_to_index_blocks(const vsa_desc *desc, int block_q, int nQb, const uint8_t *block_mask,

@@ -56,7 +56,8 @@ struct PoolSegs {
     int n;
 };
 cudaError_t launch_pools(const Prob &p, const PoolSegs &segs, cudaStream_t s);
-// q and k (v == NULL) or q, k and v in one launch.
+// Any of q, k, v in one launch; a NULL tensor is skipped (nothing launched
+// when all three are NULL).
 cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void *k, float *pk, const void *v,
                             float *pv, cudaStream_t s);
 // Coarse scores + per-row top-k -> block map and Q-owned index.

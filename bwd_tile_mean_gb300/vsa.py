@@ -13,6 +13,7 @@ from __future__ import annotations
 import ctypes as C
 import math
 import os
+import weakref
 from typing import Optional
 
 import torch
@@ -33,7 +34,9 @@ EXPORTS = ("vsa_workspace_size", "vsa_build_block_map", "vsa_build_block_map_sta
            "vsa_tile_3d_count", "vsa_tile_3d", "vsa_untile_3d", "vsa_gate_grad",
            "vsa_mask_to_index_blocks", "vsa_fwd_blocks", "vsa_bwd_blocks", "vsa_check_wait_timeout",
            "vsa_train_step_host_size", "vsa_train_step_host", "vsa_fwd_step_host", "vsa_step_host_status",
-           "vsa_check_inputs", "vsa_head_slice")
+           "vsa_check_inputs", "vsa_head_slice", "vsa_fwd_reuse", "vsa_bwd_reuse")
+
+REUSE_QK_MEANS, REUSE_V_MEANS = 1, 2  # vsa_fwd_reuse / vsa_bwd_reuse mask bits
 
 
 class VsaError(RuntimeError):
@@ -83,6 +86,12 @@ def lib():
         L.vsa_bwd.restype = C.c_int
         L.vsa_bwd.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P, P, P, P, P,
                               C.c_size_t, P]
+        L.vsa_fwd_reuse.restype = C.c_int
+        L.vsa_fwd_reuse.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, C.c_int, P, P, P, P, P, P, C.c_int, P,
+                                    C.c_size_t, P]
+        L.vsa_bwd_reuse.restype = C.c_int
+        L.vsa_bwd_reuse.argtypes = [C.POINTER(VsaDesc), P, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P, P, P, P,
+                                    C.c_int, P, C.c_size_t, P]
         L.vsa_status_string.restype = C.c_char_p
         L.vsa_status_string.argtypes = [C.c_int]
         L.vsa_last_cuda_error.restype = C.c_char_p
@@ -180,19 +189,27 @@ def vsa_mask_to_index(desc, block_map, q_var, kv_var, need_bwd_index, q_idx, q_c
 
 
 def vsa_fwd(desc, q, k, v, q_idx, q_cnt, idx_cap, q_var, kv_var, gate, out, lse, o_sparse, workspace,
-            stream=None):
-    _check("vsa_fwd", lib().vsa_fwd(
-        C.byref(desc), _p(q), _p(k), _p(v), _p(q_idx), _p(q_cnt), int(idx_cap), _p(q_var), _p(kv_var), _p(gate),
-        _p(out), _p(lse), _p(o_sparse), _p(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+            stream=None, reuse=0):
+    """vsa_fwd (reuse = 0) or vsa_fwd_reuse (reuse: REUSE_* bits)."""
+    args = (C.byref(desc), _p(q), _p(k), _p(v), _p(q_idx), _p(q_cnt), int(idx_cap), _p(q_var), _p(kv_var),
+            _p(gate), _p(out), _p(lse), _p(o_sparse))
+    tail = (_p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if reuse:
+        _check("vsa_fwd_reuse", lib().vsa_fwd_reuse(*args, int(reuse), *tail))
+    else:
+        _check("vsa_fwd", lib().vsa_fwd(*args, *tail))
 
 
 def vsa_bwd(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, idx_cap, kv_ptr, kv_qidx, q_var, kv_var, gate,
-            dq, dk, dv, workspace, stream=None):
-    _check("vsa_bwd", lib().vsa_bwd(
-        C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(o_sparse), _p(lse), _p(q_idx), _p(q_cnt), int(idx_cap),
-        _p(kv_ptr), _p(kv_qidx), _p(q_var), _p(kv_var), _p(gate), _p(dq), _p(dk), _p(dv), _p(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+            dq, dk, dv, workspace, stream=None, reuse=0):
+    """vsa_bwd (reuse = 0) or vsa_bwd_reuse (reuse: REUSE_* bits)."""
+    args = (C.byref(desc), _p(dO), _p(q), _p(k), _p(v), _p(o_sparse), _p(lse), _p(q_idx), _p(q_cnt),
+            int(idx_cap), _p(kv_ptr), _p(kv_qidx), _p(q_var), _p(kv_var), _p(gate), _p(dq), _p(dk), _p(dv))
+    tail = (_p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if reuse:
+        _check("vsa_bwd_reuse", lib().vsa_bwd_reuse(*args, int(reuse), *tail))
+    else:
+        _check("vsa_bwd", lib().vsa_bwd(*args, *tail))
 
 
 def vsa_gate_grad(desc, dO, q, k, v, q_var, kv_var, dgate, workspace, stream=None):
@@ -269,6 +286,12 @@ class Plan:
     layout: "bhsd" | "bshd" | "tnd"; sizes as in vsa_desc. For TND pass
     cu_seqlens_q / cu_seqlens_kv (int32 device tensors, [B+1]) and
     max_seqlen_q / max_seqlen_kv (host ints) instead of Sq / Skv per batch.
+
+    With a gate, the plan's methods keep the tile means in its workspace
+    between calls (vsa_fwd_reuse / vsa_bwd_reuse): it tracks what its own
+    calls pooled, so a module-level call that writes plan.workspace with
+    other tensors must be followed by build_block_map before the next gated
+    forward or backward.
     """
 
     def __init__(self, layout, dtype, B, Hq, Hkv, D, tile_q, tile_kv, nQ, nKV, Sq, Skv, idx_cap, gate=False,
@@ -292,14 +315,40 @@ class Plan:
         self.q_cnt = torch.empty((B, Hq, nQ), **i32)
         self.kv_ptr = torch.empty((B, Hq, nKV + 1), **i32)
         self.kv_qidx = torch.empty((B, Hq, nQ * idx_cap), **i32)
+        # Tile means the workspace holds: {"qk": key of (q, k), "v": key of v}
+        # as left by the last call that pooled them. A later gated call
+        # passes the matching reuse bit only for the same tensor objects,
+        # unmodified since: torch bumps a tensor's version counter on every
+        # in-place write, through any view of it.
+        self._means = {}
+
+    @staticmethod
+    def _key(*ts):
+        return tuple((weakref.ref(t), t._version) for t in ts)
+
+    def _holds(self, which, *ts):
+        key = self._means.get(which)
+        return key is not None and len(key) == len(ts) and all(
+            r() is t and ver == t._version for (r, ver), t in zip(key, ts))
+
+    def _reuse(self, q, k, v):
+        return (REUSE_QK_MEANS if self._holds("qk", q, k) else 0) | (REUSE_V_MEANS if self._holds("v", v) else 0)
+
+    def _pooled(self, q=None, k=None, v=None):
+        if q is not None:
+            self._means["qk"] = self._key(q, k)
+        if v is not None:
+            self._means["v"] = self._key(v)
 
     def lse_shape(self):
         return (self.Hq, self.Sq) if self.layout == "tnd" else (self.B, self.Hq, self.Sq)
 
     def build_block_map(self, q, k, topk, need_bwd_index=True, stream=None):
+        self._means.clear()  # a step starts here: only the means this call pools are kept
         vsa_build_block_map(self.desc, q, k, self.q_var, self.kv_var, topk, need_bwd_index, self.block_map,
                             self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr if need_bwd_index else None,
                             self.kv_qidx if need_bwd_index else None, self.workspace, stream)
+        self._pooled(q, k)
 
     def mask_to_index(self, block_map, need_bwd_index=True, stream=None):
         self.block_map = block_map
@@ -312,16 +361,26 @@ class Plan:
         lse = torch.empty(self.lse_shape(), dtype=torch.float32, device=q.device) if lse is None else lse
         if gate is not None and o_sparse is None:
             o_sparse = torch.empty_like(q)
+        reuse = self._reuse(q, k, v) if gate is not None else 0
+        if gate is not None:
+            self._means.clear()
         vsa_fwd(self.desc, q, k, v, self.q_idx, self.q_cnt, self.idx_cap, self.q_var, self.kv_var, gate, out, lse,
-                o_sparse, self.workspace, stream)
+                o_sparse, self.workspace, stream, reuse=reuse)
+        if gate is not None:
+            self._pooled(q, k, v)
         return out, lse, (o_sparse if o_sparse is not None else out)
 
     def backward(self, dO, q, k, v, o_sparse, lse, gate=None, dq=None, dk=None, dv=None, stream=None):
         dq = torch.empty_like(q) if dq is None else dq
         dk = torch.empty_like(k) if dk is None else dk
         dv = torch.empty_like(v) if dv is None else dv
+        reuse = self._reuse(q, k, v) if gate is not None else 0
+        if gate is not None:
+            self._means.clear()
         vsa_bwd(self.desc, dO, q, k, v, o_sparse, lse, self.q_idx, self.q_cnt, self.idx_cap, self.kv_ptr,
-                self.kv_qidx, self.q_var, self.kv_var, gate, dq, dk, dv, self.workspace, stream)
+                self.kv_qidx, self.q_var, self.kv_var, gate, dq, dk, dv, self.workspace, stream, reuse=reuse)
+        if gate is not None:
+            self._pooled(q, k, v)
         return dq, dk, dv
 
     def mask_to_index_blocks(self, block_q, block_mask, need_bwd_index=True, stream=None):
@@ -362,7 +421,9 @@ class Plan:
     def gate_grad(self, dO, q, k, v, dgate=None, stream=None):
         """dgate = dO (*) c (the plan must have been made with gate=True)."""
         dgate = torch.empty_like(dO) if dgate is None else dgate
+        self._means.clear()
         vsa_gate_grad(self.desc, dO, q, k, v, self.q_var, self.kv_var, dgate, self.workspace, stream)
+        self._pooled(q, k, v)
         return dgate
 
     def check_inputs(self, with_index=True, with_bwd_index=True, stream=None):

@@ -208,6 +208,39 @@ vsa_status vsa_bwd(const vsa_desc *desc, const void *dO, const void *q, const vo
                    const void *gate, void *dq, void *dk, void *dv, void *workspace,
                    size_t workspace_bytes, vsa_stream_t stream);
 
+/* Tile means kept between the calls of one step. The gated compression
+ * branch ([VSA-test] test_vsa256_cute_backward_with_compress_gate) reads
+ * the fp32 tile means of q, k and v, and the block map already computed
+ * those of q and k; vsa_fwd and vsa_bwd recompute every mean they read.
+ * vsa_fwd_reuse / vsa_bwd_reuse are the same calls with a `reuse` mask
+ * that names the means the workspace already holds for this call's inputs,
+ * which are then read from it instead of recomputed (the pooling kernel
+ * skips them; with every mean kept it is not launched):
+ *   VSA_REUSE_QK_MEANS  pq, pk: the last vsa_build_block_map, vsa_fwd* or
+ *                       vsa_bwd* run on this workspace had the same
+ *                       descriptor, q, k, q_var and kv_var, unchanged since;
+ *   VSA_REUSE_V_MEANS   pv: the last gated vsa_fwd* or vsa_bwd* run on this
+ *                       workspace had the same v and kv_var, unchanged since.
+ * The means are computed by one kernel in a fixed order, so a kept mean is
+ * bit-identical to a recomputed one and the results do not depend on the
+ * mask. The library cannot check the claim: a mask that names means the
+ * workspace does not hold gives results computed from stale means (no
+ * error). Without a gate the mask has no effect. Bits other than these two
+ * give VSA_ERR_SHAPE. reuse = 0 is vsa_fwd / vsa_bwd exactly. */
+enum { VSA_REUSE_QK_MEANS = 1, VSA_REUSE_V_MEANS = 2 };
+vsa_status vsa_fwd_reuse(const vsa_desc *desc, const void *q, const void *k, const void *v,
+                         const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
+                         const int32_t *q_var, const int32_t *kv_var, const void *gate, void *out,
+                         float *lse, void *o_sparse, int reuse, void *workspace,
+                         size_t workspace_bytes, vsa_stream_t stream);
+vsa_status vsa_bwd_reuse(const vsa_desc *desc, const void *dO, const void *q, const void *k,
+                         const void *v, const void *o_sparse, const float *lse,
+                         const int32_t *q_idx, const int32_t *q_cnt, int idx_cap,
+                         const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var,
+                         const int32_t *kv_var, const void *gate, void *dq, void *dk, void *dv,
+                         int reuse, void *workspace, size_t workspace_bytes,
+                         vsa_stream_t stream);
+
 /* Failure-path check: launches one warp that waits, with the library's
  * bounded mbarrier wait, on a barrier that nothing ever arrives on. After
  * limit_ns of wall time (0 < limit_ns <= 10 s) the wait gives up, records

@@ -308,3 +308,51 @@ def test_gate_grad_parity(p):
     if p.layout == "tnd":
         assert got.shape[0] == p.cu_q[-1]
     check_tol(f"{p.name} dgate", ref, got, GRAD_TOL)
+
+
+@pytest.mark.parametrize("p", gated_cases(), ids=lambda p: p.name)
+def test_gated_step_pools_once(p):
+    """A gated step through the plan pools q and k once (block map) and v
+    once (forward); the backward pools nothing. Outputs are bitwise those of
+    the calls that recompute every tile mean (reuse = 0). After an in-place
+    write to q the plan recomputes q's and k's means, again bitwise equal to
+    reuse = 0 on the new q."""
+    from bwd_tile_mean_gb300 import vsa
+    t = make_tensors(p)
+    plan, g = run_map(p, t)
+    q, k, v, dO, gate = g["q"], g["k"], g["v"], g["dO"], g["gate"]
+
+    def recompute(qq):
+        out, lse, osp = torch.empty_like(qq), torch.empty(plan.lse_shape(), dtype=torch.float32, device="cuda"), \
+            torch.empty_like(qq)
+        vsa.vsa_fwd(plan.desc, qq, k, v, plan.q_idx, plan.q_cnt, plan.idx_cap, plan.q_var, plan.kv_var, gate, out,
+                    lse, osp, plan.workspace)
+        grads = [torch.empty_like(x) for x in (qq, k, v)]
+        vsa.vsa_bwd(plan.desc, dO, qq, k, v, osp, lse, plan.q_idx, plan.q_cnt, plan.idx_cap, plan.kv_ptr,
+                    plan.kv_qidx, plan.q_var, plan.kv_var, gate, *grads, plan.workspace)
+        return [out, lse, osp] + grads
+
+    ref = recompute(q)
+    plan.build_block_map(q, k, p.topk)
+    with vsa.profile() as prof:
+        out, lse, osp = plan.forward(q, k, v, gate=gate)
+        grads = plan.backward(dO, q, k, v, osp, lse, gate=gate)
+    torch.cuda.synchronize()
+    assert [n for n, _ in prof.records].count("pool") == 1  # v, in the forward
+    for a, b in zip(ref, [out, lse, osp] + list(grads)):
+        assert torch.equal(a, b)
+
+    q.mul_(-0.5)  # new q: its means (and so c and the gated outputs) change
+    ref2 = recompute(q)
+    plan.build_block_map(q, k, p.topk)
+    q.add_(0.25)  # written again after the block map pooled it
+    ref3 = recompute(q)
+    with vsa.profile() as prof:
+        out, lse, osp = plan.forward(q, k, v, gate=gate)
+        grads = plan.backward(dO, q, k, v, osp, lse, gate=gate)
+    torch.cuda.synchronize()
+    assert [n for n, _ in prof.records].count("pool") == 1  # q and k, in the forward (v's means are kept)
+    assert not torch.equal(ref2[0], ref3[0])
+    for a, b in zip(ref3, [out, lse, osp] + list(grads)):
+        assert torch.equal(a, b)
+    assert plan.device_status() == 0
