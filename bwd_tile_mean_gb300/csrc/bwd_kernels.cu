@@ -42,21 +42,31 @@ constexpr int kProdWarp = 8, kMmaWarp = 9;
 // rowsum(P dP) of the softmax backward); both are stored negated so the
 // consumers add them. Slots that are not query rows (past a varlen
 // sequence's end) get nlse2 = -inf and ndvec = 0, so P = 0 there.
-// HBM-bound streaming: a task is 32 consecutive slots of one (b, h). One
-// producer lane per CTA streams each task's dO and O rows ([32 x 128]
-// 16-bit tiles, two 64-column TMA boxes each, 128-byte swizzle) into a ring
-// of kPrepStages shared-memory stages; four consumer warps take the tasks
-// in turn, one lane per row, so a row's sum stays in its lane and the LSE
-// read and both writes are one coalesced 128-byte access each. Tasks are
-// numbered in memory order of dO and O (heads of a token adjacent in BSHD
-// and TND, tokens of a head in BHSD) and dealt to the CTAs round robin, so
-// the CTAs in flight read neighbouring memory.
-constexpr int kPrepRows = 32;                     // slots per task
-constexpr int kPrepStages = 12;
-constexpr int kPrepBox = kPrepRows * 128;         // one 64-column box of 32 rows (bytes)
+// HBM-bound streaming: a task is 64 consecutive slots of one (b, h). Two
+// producer warps (one lane each) stream the tasks' dO and O rows ([64 x
+// 128] 16-bit tiles, two 64-column TMA boxes each, 128-byte swizzle) into
+// a ring of kPrepStages shared-memory stages, alternating stages between
+// them: a producer completes about one barrier round per ~900 cycles
+// whatever the ring depth, so the bytes per round (32 KB) and the number
+// of producers set the rate an SM can pull. Three consumer warps take the
+// tasks in turn, each lane two rows (lane and lane + 32), so a row's sum
+// stays in its lane and the LSE read and both writes are coalesced
+// 128-byte accesses. Tasks are numbered in memory order of dO and O
+// (heads of a token adjacent in BSHD and TND, tokens of a head in BHSD)
+// and dealt to the CTAs round robin, so the CTAs in flight read
+// neighbouring memory.
+constexpr int kPrepRows = 64;                     // slots per task
+constexpr int kPrepStages = 6;
+constexpr int kPrepBox = kPrepRows * 128;         // one 64-column box of 64 rows (bytes)
 constexpr int kPrepStage = 4 * kPrepBox;          // dO and O, two boxes each
-constexpr int kPrepConsumers = 4;
+constexpr int kPrepConsumers = 3, kPrepProducers = 2;
+constexpr int kPrepThreads = 32 * (kPrepConsumers + kPrepProducers);
 constexpr size_t kPrepSmem = (size_t)kPrepStages * kPrepStage + 256;
+// A thread that takes every n-th task meets a stage again after
+// lcm(n, kPrepStages) tasks; that must be exactly one barrier phase later
+// (kPrepStages tasks), or its parity wait could pass on an older phase.
+static_assert(kPrepStages % kPrepProducers == 0, "each producer returns to a stage one phase later");
+static_assert(kPrepStages % kPrepConsumers == 0, "each consumer returns to a stage one phase later");
 enum : unsigned { kSitePrepProd = 0x401, kSitePrepCons = 0x402 };
 
 __device__ __forceinline__ void prep_task(const Prob &p, int task, int groups, int &b, int &h, int &s0) {
@@ -76,7 +86,29 @@ __device__ __forceinline__ void prep_task(const Prob &p, int task, int groups, i
 }
 
 template <typename T>
-__global__ void __launch_bounds__(32 * (kPrepConsumers + 1), 1)
+__device__ __forceinline__ float prep_row_dot(const uint8_t *base, uint32_t r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t off = hf * kPrepBox + sw128_off(r, u);
+            const uint4 x = *reinterpret_cast<const uint4 *>(base + off);
+            const uint4 y = *reinterpret_cast<const uint4 *>(base + 2 * kPrepBox + off);
+            const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a2 = unpack2<T>(xw[e]), c2 = unpack2<T>(yw[e]);
+                acc = fmaf(a2.x, c2.x, acc);
+                acc = fmaf(a2.y, c2.y, acc);
+            }
+        }
+    }
+    return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPrepThreads, 1)
     k_bwd_prep(const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap to, const Prob p,
                const float *__restrict__ lse, float *__restrict__ nlse2, float *__restrict__ ndvec, int ntasks,
                unsigned *err) {
@@ -101,15 +133,17 @@ __global__ void __launch_bounds__(32 * (kPrepConsumers + 1), 1)
         fence_mbar_init();
     }
     __syncthreads();
-    int issued[kPrepStages];
-#pragma unroll
-    for (int s = 0; s < kPrepStages; ++s) issued[s] = 0;
-    if (warp == kPrepConsumers) {
+    if (warp >= kPrepConsumers) {
         if (lane == 0) {
-            // ---------------------------------------------------- producer
+            // --------------------------------------------------- producers
+            // producer j issues tasks j, j + 2, ... into stages of parity j
+            const int j = warp - kPrepConsumers;
+            int issued[kPrepStages / kPrepProducers];
+#pragma unroll
+            for (int s = 0; s < kPrepStages / kPrepProducers; ++s) issued[s] = 0;
             tma_prefetch_desc(&tdo);
             tma_prefetch_desc(&to);
-            for (int k = 0; k < mine; ++k) {
+            for (int k = j; k < mine; k += kPrepProducers) {
                 const int st = k % kPrepStages;
                 if (k >= kPrepStages &&
                     !mbar_wait(empty + st, ((k / kPrepStages) - 1) & 1, s_abort, err, kSitePrepProd))
@@ -124,12 +158,14 @@ __global__ void __launch_bounds__(32 * (kPrepConsumers + 1), 1)
                 tma_load_4d(dst + kPrepBox, &tdo, full + st, 64, row, h, bc);
                 tma_load_4d(dst + 2 * kPrepBox, &to, full + st, 0, row, h, bc);
                 tma_load_4d(dst + 3 * kPrepBox, &to, full + st, 64, row, h, bc);
-                issued[st]++;
+                issued[st / kPrepProducers]++;
             }
-            if (*s_abort) {  // drain this CTA's copies before it exits (bounded)
+            if (*s_abort) {  // drain this producer's copies before the CTA exits (bounded)
                 int never = 0;
-                for (int s = 0; s < kPrepStages; ++s)
-                    if (issued[s]) mbar_wait(full + s, (issued[s] - 1) & 1, &never, nullptr, 0, 200000000ull);
+                for (int s = 0; s < kPrepStages / kPrepProducers; ++s)
+                    if (issued[s])
+                        mbar_wait(full + s * kPrepProducers + j, (issued[s] - 1) & 1, &never, nullptr, 0,
+                                  200000000ull);
             }
         }
         return;
@@ -141,34 +177,22 @@ __global__ void __launch_bounds__(32 * (kPrepConsumers + 1), 1)
             break;
         int b, h, s0;
         prep_task(p, (int)blockIdx.x + k * (int)gridDim.x, groups, b, h, s0);
-        // row `lane` of the task: the two 64-column halves of dO and O
+        // rows `lane` and `lane + 32` of the task: the two 64-column halves of dO and O
         const uint8_t *base = sm + st * kPrepStage;
-        float acc = 0.f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t off = hf * kPrepBox + sw128_off(lane, u);
-                const uint4 x = *reinterpret_cast<const uint4 *>(base + off);
-                const uint4 y = *reinterpret_cast<const uint4 *>(base + 2 * kPrepBox + off);
-                const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 a2 = unpack2<T>(xw[e]), c2 = unpack2<T>(yw[e]);
-                    acc = fmaf(a2.x, c2.x, acc);
-                    acc = fmaf(a2.y, c2.y, acc);
-                }
-            }
-        }
+        const float acc0 = prep_row_dot<T>(base, (uint32_t)lane);
+        const float acc1 = prep_row_dot<T>(base, (uint32_t)lane + 32u);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + st);  // the stage's rows are in registers
         const int len = p.layout == L_TND ? seq_len(p, true, b) : per;
-        const int s = s0 + lane;
-        const bool ex = s < len;
-        const long long slot = ((long long)b * p.Hq + h) * per + s;
-        ndvec[slot] = ex ? -acc : 0.f;
-        const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
-        nlse2[slot] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
+        const long long slot0 = ((long long)b * p.Hq + h) * per + s0;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int s = s0 + r * 32 + lane;
+            const bool ex = s < len;
+            ndvec[slot0 + r * 32 + lane] = ex ? -(r ? acc1 : acc0) : 0.f;
+            const float lv = ex ? lse[lse_off(p, b, h, s)] : -INFINITY;
+            nlse2[slot0 + r * 32 + lane] = lv == -INFINITY ? -INFINITY : -lv * kLog2e;  // a row with no key: P = 0
+        }
     }
 }
 
@@ -1048,7 +1072,7 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
     CUtensorMap tdo, to;
     if (!make_tmap_rows(&tdo, p, true, dO, p.Hq, kPrepRows) || !make_tmap_rows(&to, p, true, o, p.Hq, kPrepRows))
         return cudaErrorInvalidValue;
-    const int ntasks = (int)(slots / kPrepRows);  // tile_q is a multiple of 32
+    const int ntasks = (int)(slots / kPrepRows);  // tile_q is a multiple of 64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1059,11 +1083,9 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
     if (ae != cudaSuccess) return ae;
     prof_begin("bwd_prep", s);
     if (p.dtype == T_BF16)
-        k_bwd_prep<__nv_bfloat16><<<blocks, 32 * (kPrepConsumers + 1), kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec,
-                                                                                      ntasks, err);
+        k_bwd_prep<__nv_bfloat16><<<blocks, kPrepThreads, kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec, ntasks, err);
     else
-        k_bwd_prep<__half><<<blocks, 32 * (kPrepConsumers + 1), kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec,
-                                                                               ntasks, err);
+        k_bwd_prep<__half><<<blocks, kPrepThreads, kPrepSmem, s>>>(tdo, to, p, lse, nlse2, ndvec, ntasks, err);
     prof_end(s);
     return cudaGetLastError();
 }
