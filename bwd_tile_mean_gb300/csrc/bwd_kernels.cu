@@ -196,6 +196,74 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
 }
 
+// ------------------------------------------------------ dK/dV order
+// The dK/dV units differ in work by their KV-owned list lengths (a popular
+// tile is listed by many query tiles), and the CTAs of one launch start in
+// grid order. The units of one (batch entry, key/value head) share that
+// head's Q and dO in L2, so the heads keep their grid order; within each
+// head the longest units start first, which leaves the last head's short
+// units for the end of the launch, where they fill the SMs that finish
+// early (longest processing time first). A unit's key is the summed list
+// length of its GQA group's heads (0 for a chunk without valid keys); a
+// counting sort over kOrderBins bins of decreasing key (keys past the last
+// bin share it) writes each head's part of the permutation. The order
+// within a bin is the order of the atomics, which changes no result: each
+// unit writes only its own dK, dV.
+constexpr int kOrderBins = 1024, kOrderThreads = 1024;
+
+// One CTA per (b, key/value head): units [seg * units_x, + units_x).
+__global__ void __launch_bounds__(kOrderThreads) k_dk_order(const Prob p, const int *__restrict__ kv_ptr, int cap,
+                                                           int *__restrict__ order, int *__restrict__ keys) {
+    __shared__ int hist[kOrderBins];
+    __shared__ int warp_sum[kOrderThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int subs_kv = p.tile_kv >> 7, units_x = p.nKV * subs_kv, g = p.Hq / p.Hkv;
+    const int seg = blockIdx.x, hk = seg % p.Hkv, b = seg / p.Hkv;
+    const long long base = (long long)seg * units_x;
+    const int cap_all = p.nQ * cap;
+    hist[t] = 0;
+    __syncthreads();
+    for (int x = t; x < units_x; x += kOrderThreads) {
+        const int j = x / subs_kv, ck = x % subs_kv;
+        int key = 0;
+        if (kv_valid(p, b, j) > ck * 128)
+            for (int h = hk * g; h < hk * g + g; ++h) {
+                const int *ptr = kv_ptr + ((long long)b * p.Hq + h) * (p.nKV + 1);
+                const int pos = clampi(ptr[j], 0, cap_all);
+                key += clampi(ptr[j + 1], pos, cap_all) - pos;
+            }
+        const int bin = kOrderBins - 1 - min(key, kOrderBins - 1);  // bin 0: the longest
+        keys[base + x] = bin;
+        atomicAdd(&hist[bin], 1);
+    }
+    __syncthreads();
+    // exclusive scan of the histogram (one bin per thread)
+    const int v = hist[t];
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    if (lane == 31) warp_sum[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        int s = warp_sum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        warp_sum[lane] = s;  // inclusive over warps
+    }
+    __syncthreads();
+    hist[t] = inc - v + (w > 0 ? warp_sum[w - 1] : 0);
+    __syncthreads();
+    for (int x = t; x < units_x; x += kOrderThreads)
+        order[base + atomicAdd(&hist[keys[base + x]], 1)] = (int)(base + x);
+}
+static_assert(kOrderBins == kOrderThreads, "the scan takes one bin per thread");
+
 // ----------------------------------------------------------- MMA helpers
 // Measured on GB300 (all SMs busy, M = 128, K = 16 per instruction): an
 // MMA with N = 128 takes 64 cycles with A from shared memory or from TMEM;
@@ -337,8 +405,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int subs_kv = p.tile_kv >> 7;
-    const int j = blockIdx.x / subs_kv, ck = blockIdx.x % subs_kv;
-    const int hk = blockIdx.y, b = blockIdx.z, g = p.Hq / p.Hkv;
+    // this CTA's unit: the launch order is longest work first (an order
+    // entry out of range is invalid input and is clamped into the grid)
+    const int units_x = p.nKV * subs_kv;
+    const int u = a.dk_order ? clampi(a.dk_order[blockIdx.x], 0, (int)gridDim.x - 1) : (int)blockIdx.x;
+    const int x = u % units_x, j = x / subs_kv, ck = x % subs_kv;
+    const int hk = (u / units_x) % p.Hkv, b = u / (units_x * p.Hkv), g = p.Hq / p.Hkv;
     const int h0 = hk * g, h_end = h0 + g;
     const int kvalid_tile = kv_valid(p, b, j);
     int kvalid = kvalid_tile - ck * 128;
@@ -1090,12 +1162,27 @@ cudaError_t launch_bwd_prep(const Prob &p, const void *dO, const void *o, const 
     return cudaGetLastError();
 }
 
+long long dk_units(const Prob &p) { return (long long)p.B * p.Hkv * p.nKV * (p.tile_kv / 128); }
+
+cudaError_t launch_dk_order(const Prob &p, const int *kv_ptr, int cap, int *order, int *keys, cudaStream_t s) {
+    const long long units = dk_units(p);
+    if (units == 0) return cudaSuccess;
+    if (units > (long long)INT_MAX) return cudaErrorInvalidValue;
+    prof_begin("dkdv_order", s);
+    k_dk_order<<<p.B * p.Hkv, kOrderThreads, 0, s>>>(p, kv_ptr, cap, order, keys);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tv, tdo;
     if (!make_tmap_rows(&tq, p, true, a.q, p.Hq, kDkItem) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
         !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, kDkItem))
         return cudaErrorInvalidValue;
-    dim3 grid(p.nKV * (p.tile_kv / 128), p.Hkv, p.B);
+    const long long units = dk_units(p);
+    if (units == 0) return cudaSuccess;
+    if (units > (long long)INT_MAX) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)units);
     const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_dkdv<__nv_bfloat16>, (int)kDkSmem)
                                              : ensure_smem_limit((const void *)k_dkdv<__half>, (int)kDkSmem);
     if (ae != cudaSuccess) return ae;

@@ -227,7 +227,7 @@ vsa_status run_block_map(const Prob &p, const void *q, const void *k, int topk, 
 namespace {
 
 struct WsLayout {
-    size_t pq, pk, pv, c, nlse2, ndvec, redo, dc, A, ds, dpq, dpk, dpv, total;
+    size_t pq, pk, pv, c, nlse2, ndvec, redo, order, okeys, dc, A, ds, dpq, dpk, dpv, total;
 };
 
 WsLayout ws_layout(const Prob &p, bool gate) {
@@ -245,6 +245,8 @@ WsLayout ws_layout(const Prob &p, bool gate) {
     L.nlse2 = take(slots * 4);
     L.ndvec = take(slots * 4);
     L.redo = take((size_t)p.B * p.Hq * p.nQ);
+    L.order = take((size_t)dk_units(p) * 4);
+    L.okeys = take((size_t)dk_units(p) * 4);
     if (gate) {
         L.pv = take(fk);
         L.c = take(fq);
@@ -480,6 +482,9 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
         a.dpk = dpk;
         a.dpv = dpv;
     }
+    int *order = at<int>(workspace, L.order);
+    VSA_CUDA(launch_dk_order(p, kv_ptr, idx_cap, order, at<int>(workspace, L.okeys), s));
+    a.dk_order = order;
     VSA_CUDA(launch_bwd_dkdv(p, a, s));
     VSA_CUDA(launch_bwd_dq(p, a, s));
     return VSA_OK;

@@ -123,7 +123,16 @@ struct BwdArgs {
     const int *q_sub, *kv_qsub;     // query-block bit masks of both indices (NULL: whole tiles)
     int block_q;
     unsigned *err;
+    const int *dk_order;            // dK/dV units, longest work first (launch_dk_order)
 };
+// Units of the dK/dV pass: one per (batch entry, key/value head, 128-key
+// chunk), numbered ((b * Hkv + hk) * nKV + j) * (tile_kv / 128) + chunk.
+long long dk_units(const Prob &p);
+// Writes order[dk_units], a permutation of the units: the (b, key/value
+// head) segments in grid order, each segment's units by decreasing work
+// (the summed KV-owned list lengths of the unit's GQA group, from kv_ptr);
+// keys[dk_units] is scratch. One CTA per segment.
+cudaError_t launch_dk_order(const Prob &p, const int *kv_ptr, int cap, int *order, int *keys, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s);
 // Compression branch, backward: dc, then A / ds per row, then the

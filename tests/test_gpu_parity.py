@@ -356,3 +356,26 @@ def test_gated_step_pools_once(p):
     for a, b in zip(ref3, [out, lse, osp] + list(grads)):
         assert torch.equal(a, b)
     assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("p", [extra_cases()[1], gated_cases()[0], topk_varlen()], ids=lambda p: p.name)
+def test_backward_writes_every_key_row(p):
+    """The dK/dV pass runs its units longest first (a permutation computed
+    on the device from kv_ptr): every unit must run exactly once. dQ, dK and
+    dV start as NaN and must come back finite everywhere, equal to a second
+    run (keys no query selected, and padded slots, get 0)."""
+    t = make_tensors(p)
+    plan, g = run_map(p, t)
+    gate = g.get("gate")
+    out, lse, osp = plan.forward(g["q"], g["k"], g["v"], gate=gate)
+    runs = []
+    for _ in range(2):
+        dq, dk, dv = (torch.full_like(x, float("nan")) for x in (g["q"], g["k"], g["v"]))
+        plan.backward(g["dO"], g["q"], g["k"], g["v"], osp, lse, gate=gate, dq=dq, dk=dk, dv=dv)
+        runs.append((dq, dk, dv))
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    for x in runs[0]:
+        assert torch.isfinite(x).all()
+    for a_, b_ in zip(*runs):
+        assert torch.equal(a_, b_)
