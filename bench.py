@@ -39,8 +39,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the source file that defines each kernel; a kernel whose source changed
 # since then reports no traffic.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_bytes_video_dit_4heads.json")
-KERNEL_SOURCE = {"fwd_attn": "fwd_kernel.cu", "bwd_dkdv": "bwd_kernels.cu", "bwd_dq": "bwd_kernels.cu",
-                 "bwd_prep": "bwd_kernels.cu", "pool": "index_kernels.cu", "select_topk": "index_kernels.cu"}
+KERNEL_SOURCE = {"fwd_attn": "fwd_kernel.cu", "fwd_redo": "fwd_kernel.cu", "bwd_dkdv": "bwd_kernels.cu",
+                 "bwd_dq": "bwd_kernels.cu", "bwd_prep": "bwd_kernels.cu", "dkdv_order": "bwd_kernels.cu",
+                 "pool": "index_kernels.cu", "select_topk": "index_kernels.cu",
+                 "transpose_index": "index_kernels.cu"}
+# CUDA kernel function -> the name the library's launch records use
+KERNEL_FUNCTION = {"k_fwd2": "fwd_attn", "k_fwd": "fwd_redo", "k_dkdv": "bwd_dkdv", "k_dq": "bwd_dq",
+                   "k_bwd_prep": "bwd_prep", "k_dk_order": "dkdv_order", "k_pool": "pool",
+                   "k_select": "select_topk", "k_transpose": "transpose_index"}
 CPU_SAMPLE_TILES = 2   # query tiles (forward, dQ) and KV tiles (dK, dV) of the oracle sample
 
 
@@ -74,6 +80,43 @@ def measured_traffic(kernel, heads):
         return None, f"kernel source changed since the capture ({cap.get('captured', '?')})"
     return (k["dram_bytes_read"] + k["dram_bytes_write"]) * heads / cap["heads"], \
         f"ncu capture {cap.get('captured', '?')} on {cap['heads']} heads, scaled to {heads}"
+
+
+def write_traffic(csv_path, heads, command):
+    """Per-launch DRAM bytes of each kernel from an ncu CSV (--metrics
+    dram__bytes_read.sum,dram__bytes_write.sum --csv --log-file) of one step
+    at `heads` heads, written to TRAFFIC_FILE with the source hashes."""
+    import csv
+    import re
+    scale = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+    launches = {}  # (ncu launch id, kernel) -> {metric: bytes}
+    with open(csv_path, newline="") as fh:
+        lines = [ln for ln in fh if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        name = row.get("Kernel Name", "")
+        kern = next((v for k, v in KERNEL_FUNCTION.items() if re.search(rf"\b{k}\b", name)), None)
+        metric = row.get("Metric Name", "")
+        if kern is None or metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(row["Metric Value"].replace(",", "")) * scale[row["Metric Unit"].strip().lower()]
+        launches.setdefault((row["ID"], kern), {})[metric] = val
+    out = {}
+    for (_, kern), m in launches.items():
+        k = out.setdefault(kern, {"launches": 0, "dram_bytes_read": 0.0, "dram_bytes_write": 0.0})
+        k["launches"] += 1
+        k["dram_bytes_read"] += m.get("dram__bytes_read.sum", 0.0)
+        k["dram_bytes_write"] += m.get("dram__bytes_write.sum", 0.0)
+    for kern, k in out.items():
+        n = k["launches"]
+        k["dram_bytes_read"] = round(k["dram_bytes_read"] / n)
+        k["dram_bytes_write"] = round(k["dram_bytes_write"] / n)
+        k["source_sha256"] = source_sha(kern)
+    cap = {"heads": heads, "captured": time.strftime("%Y-%m-%d"), "command": command,
+           "note": "bytes per launch, averaged over the captured launches of each kernel", "kernels": out}
+    with open(TRAFFIC_FILE, "w") as fh:
+        json.dump(cap, fh, indent=1, sort_keys=True)
+        fh.write("\n")
+    print(json.dumps(cap, indent=1, sort_keys=True))
 
 
 def dist_env():
@@ -455,7 +498,8 @@ def ours(args):
         if unit_flops is not None:
             launch_flops = 2.0 * p.D * p.tile_q * valid_keys * unit_flops / 2.0
             achieved = launch_flops / (info["avg_ms"] * 1e-3) / 1e12
-            traffic, note = measured_traffic(name, p.Hq)
+            traffic, note = measured_traffic(name, p.Hq) if args.config == 3 else \
+                (None, "no ncu capture of this workload")
             roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
                     "unit": "TFLOP/s", "frac": achieved / tensor_peak, "traffic": traffic,
                     "traffic_unit": "bytes per launch", "traffic_source": note,
@@ -515,7 +559,13 @@ def main():
                          "5 long-video forward only, 6 the long-video grid taken literally (1,024 tiles)")
     ap.add_argument("--shard", choices=["heads", "replicas"], default="heads",
                     help="with several GPUs: split the problem's heads over them (default) or run copies")
+    ap.add_argument("--write-traffic", metavar="CSV",
+                    help="write the committed per-kernel DRAM-bytes file from this ncu CSV and exit")
+    ap.add_argument("--traffic-command", default="", help="the capture command, recorded with --write-traffic")
     args = ap.parse_args()
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.heads, args.traffic_command)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

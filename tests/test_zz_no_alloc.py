@@ -1,7 +1,8 @@
 """vsa_build_block_map_static: the block-map entry point for callers that
-cannot allocate device memory (code running under graph capture, custom
-allocators that forbid cudaMalloc, runtimes that own all device memory).
-Its scratch is a fixed array inside the library. It must give the same
+may not allocate device memory (a runtime or memory pool that owns all of
+it, an allocator that forbids outside allocations, a path where an
+allocation could synchronise or fail). Its scratch is a fixed array inside
+the library. It must give the same
 block map and indices as vsa_build_block_map, bit for bit, on two calls in
 a row (the array keeps the previous call's contents)."""
 import pytest
