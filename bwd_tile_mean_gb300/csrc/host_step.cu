@@ -5,15 +5,19 @@
 // Pages: every head is an independent problem (Ascend
 // test_npu_block_sparse_attention_backward.py, the per-(batch, head) loops of
 // the TND/GQA golden; FastVideo test_vsa256_backward.py runs the step on
-// [B, S, H, D] tensors). So the heads are cut into `groups` slices of
-// Hq / groups query heads (and Hkv / groups key/value heads, keeping every
-// GQA group whole), each slice is copied into a compact device staging
-// slot, and while slice g computes, slice g+1 streams in and slice g-1
-// streams out:
+// [B, S, H, D] tensors). So the heads are cut into slices of whole GQA
+// groups, each slice is copied into a compact device staging slot, and
+// while slice g computes, slice g+1 streams in and slice g-1 streams out:
 //
 //   in-stream:      H2D(0)  H2D(1)  H2D(2) ...
 //   caller stream:          step(0) step(1) step(2) ...
 //   out-stream:                     D2H(0)  D2H(1) ...
+//
+// Every slice holds Hkv / groups key/value heads and their query heads.
+// Nothing overlaps the first slice's copy in or the last slice's copy out,
+// but slices of fewer heads do not shorten them: a BSHD head slice is a 2D
+// copy of runs of heads*D*2 bytes, and the copy engines move 256-byte runs
+// (one head) at about a third of the link's rate, 1,280-byte runs at ~80%.
 //
 // vsa_fwd_step_host is the same pipeline for inference (block map without
 // the KV-owned index, forward; O and LSE come back).
@@ -32,6 +36,7 @@
 // forward). No
 // device memory is allocated here: the caller provides the staging buffer.
 #include <cstdint>
+#include <vector>
 
 #include "vsa.h"
 #include "vsa_internal.h"
@@ -40,7 +45,7 @@ namespace vsa {
 namespace {
 
 struct SlotLayout {
-    size_t q, k, v, dO, out, dq, dk, dv, lse, map, qidx, qcnt, kvptr, kvqidx, ws, ws_bytes, bytes;
+    size_t ws, q, k, v, dO, out, dq, dk, dv, lse, map, qidx, qcnt, kvptr, kvqidx, ws_bytes, bytes;
     size_t gate, osp;  // gated compression branch only
 };
 
@@ -60,6 +65,10 @@ SlotLayout slot_layout(const vsa_desc &s, int cap, bool gated) {
         off += align256(bytes);
         return o;
     };
+    // the workspace first: its status word sits at the slot's start for
+    // slices of every size
+    L.ws_bytes = vsa_workspace_size(&s, gated ? 1 : 0);
+    L.ws = take(L.ws_bytes);
     L.q = take(qb);
     L.k = take(kb);
     L.v = take(kb);
@@ -78,11 +87,12 @@ SlotLayout slot_layout(const vsa_desc &s, int cap, bool gated) {
         L.gate = take(qb);
         L.osp = take(qb);
     }
-    L.ws_bytes = vsa_workspace_size(&s, gated ? 1 : 0);
-    L.ws = take(L.ws_bytes);
     L.bytes = off;
     return L;
 }
+
+// Key/value heads per slice, in order (they sum to hkv).
+std::vector<int> slice_plan(int hkv, int per_slice) { return std::vector<int>(hkv / per_slice, per_slice); }
 
 // The slice of heads [h0, h0 + hs) of a [.., H, ..] tensor as a 2D copy:
 // `rows` runs of `width` bytes, `pitch` bytes apart in the full tensor,
@@ -195,52 +205,60 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
     ok = ok && cu(cudaEventRecord(ev_start, sc)) && cu(cudaStreamWaitEvent(s_in, ev_start, 0)) &&
          cu(cudaStreamWaitEvent(s_out, ev_start, 0));
 
-    const int hq = sd.Hq, hk = sd.Hkv;
+    const int qpk = desc->Hq / desc->Hkv;     // query heads per key/value head
     const size_t row = (size_t)desc->D * 2;  // bytes per (token, head)
-    for (int g = 0; ok && g < groups; ++g) {
+    const std::vector<int> plan = slice_plan(desc->Hkv, sd.Hkv);
+    int hk0 = 0;  // first key/value head of slice g
+    for (int g = 0; ok && g < (int)plan.size(); hk0 += plan[g], ++g) {
         const int slot = g & 1;
         uint8_t *base = static_cast<uint8_t *>(device_buf) + slot * L.bytes;
-        const Strided rq = head_slice(*desc, true, g * hq, hq, row), rk = head_slice(*desc, false, g * hk, hk, row);
+        vsa_desc sg = sd;  // this slice's problem
+        sg.Hkv = plan[g];
+        sg.Hq = plan[g] * qpk;
+        const SlotLayout Lg = slot_layout(sg, cap, gated);
+        const Strided rq = head_slice(*desc, true, hk0 * qpk, sg.Hq, row),
+                      rk = head_slice(*desc, false, hk0, sg.Hkv, row);
         // inputs of slice g; the slot's previous inputs were read by step g-2
         if (g >= 2) ok = cu(cudaStreamWaitEvent(s_in, ev_comp[slot], 0));
         // (q, k, v first: the block map and the forward start before dO lands)
-        ok = ok && cu(copy_in(base + L.q, q, rq, s_in)) && cu(copy_in(base + L.k, k, rk, s_in)) &&
-             cu(copy_in(base + L.v, v, rk, s_in));
-        if (ok && gated) ok = cu(copy_in(base + L.gate, gate, rq, s_in));
+        ok = ok && cu(copy_in(base + Lg.q, q, rq, s_in)) && cu(copy_in(base + Lg.k, k, rk, s_in)) &&
+             cu(copy_in(base + Lg.v, v, rk, s_in));
+        if (ok && gated) ok = cu(copy_in(base + Lg.gate, gate, rq, s_in));
         ok = ok && cu(cudaEventRecord(ev_in[slot], s_in));
-        if (ok && train) ok = cu(copy_in(base + L.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
+        if (ok && train) ok = cu(copy_in(base + Lg.dO, dO, rq, s_in)) && cu(cudaEventRecord(ev_do[slot], s_in));
         // step g on the caller's stream; the slot's previous outputs were copied back
         ok = ok && cu(cudaStreamWaitEvent(sc, ev_in[slot], 0));
         if (ok && g >= 2) ok = cu(cudaStreamWaitEvent(sc, ev_out[slot], 0));
         if (!ok) break;
-        uint8_t *ws = base + L.ws;
-        int32_t *qidx = reinterpret_cast<int32_t *>(base + L.qidx), *qcnt = reinterpret_cast<int32_t *>(base + L.qcnt);
-        int32_t *kvptr = reinterpret_cast<int32_t *>(base + L.kvptr);
-        int32_t *kvqidx = reinterpret_cast<int32_t *>(base + L.kvqidx);
-        float *lse_d = reinterpret_cast<float *>(base + L.lse);
+        uint8_t *ws = base + Lg.ws;
+        int32_t *qidx = reinterpret_cast<int32_t *>(base + Lg.qidx), *qcnt = reinterpret_cast<int32_t *>(base + Lg.qcnt);
+        int32_t *kvptr = reinterpret_cast<int32_t *>(base + Lg.kvptr);
+        int32_t *kvqidx = reinterpret_cast<int32_t *>(base + Lg.kvqidx);
+        float *lse_d = reinterpret_cast<float *>(base + Lg.lse);
         // gated: O (the sparse attention output) stays in its own buffer, out = O + gate (*) c
-        const void *g_d = gated ? base + L.gate : nullptr;
-        void *osp_d = gated ? base + L.osp : nullptr;
-        ok = vs(vsa_build_block_map(&sd, base + L.q, base + L.k, q_var, kv_var, topk, train ? 1 : 0, base + L.map,
-                                    qidx, qcnt, cap, train ? kvptr : nullptr, train ? kvqidx : nullptr, ws,
-                                    L.ws_bytes, stream)) &&
-             vs(vsa_fwd_reuse(&sd, base + L.q, base + L.k, base + L.v, qidx, qcnt, cap, q_var, kv_var, g_d,
-                              base + L.out, lse_d, osp_d, VSA_REUSE_QK_MEANS, ws, L.ws_bytes, stream)) &&
+        const void *g_d = gated ? base + Lg.gate : nullptr;
+        void *osp_d = gated ? base + Lg.osp : nullptr;
+        ok = vs(vsa_build_block_map(&sg, base + Lg.q, base + Lg.k, q_var, kv_var, topk, train ? 1 : 0,
+                                    base + Lg.map, qidx, qcnt, cap, train ? kvptr : nullptr, train ? kvqidx : nullptr,
+                                    ws, Lg.ws_bytes, stream)) &&
+             vs(vsa_fwd_reuse(&sg, base + Lg.q, base + Lg.k, base + Lg.v, qidx, qcnt, cap, q_var, kv_var, g_d,
+                              base + Lg.out, lse_d, osp_d, VSA_REUSE_QK_MEANS, ws, Lg.ws_bytes, stream)) &&
              cu(cudaEventRecord(ev_fwd[slot], sc));
         if (ok && train)
             ok = cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
-                 vs(vsa_bwd_reuse(&sd, base + L.dO, base + L.q, base + L.k, base + L.v, gated ? osp_d : base + L.out,
-                                  lse_d, qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var, g_d, base + L.dq, base + L.dk,
-                                  base + L.dv, VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS, ws, L.ws_bytes, stream));
+                 vs(vsa_bwd_reuse(&sg, base + Lg.dO, base + Lg.q, base + Lg.k, base + Lg.v,
+                                  gated ? osp_d : base + Lg.out, lse_d, qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var,
+                                  g_d, base + Lg.dq, base + Lg.dk, base + Lg.dv,
+                                  VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS, ws, Lg.ws_bytes, stream));
         ok = ok && cu(cudaEventRecord(ev_comp[slot], sc));
         // outputs of slice g: O and LSE are final after the forward, the
         // gradients after the backward
         ok = ok && cu(cudaStreamWaitEvent(s_out, ev_fwd[slot], 0));
-        if (ok && out) ok = cu(copy_out(out, base + L.out, rq, s_out));
-        if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, g * hq, hq), s_out));
+        if (ok && out) ok = cu(copy_out(out, base + Lg.out, rq, s_out));
+        if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, hk0 * qpk, sg.Hq), s_out));
         if (ok && train)
-            ok = cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + L.dq, rq, s_out)) &&
-                 cu(copy_out(dk, base + L.dk, rk, s_out)) && cu(copy_out(dv, base + L.dv, rk, s_out));
+            ok = cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + Lg.dq, rq, s_out)) &&
+                 cu(copy_out(dk, base + Lg.dk, rk, s_out)) && cu(copy_out(dv, base + Lg.dv, rk, s_out));
         ok = ok && cu(cudaEventRecord(ev_out[slot], s_out));
     }
     // the caller's stream completes after the last copy back (and after the

@@ -60,9 +60,10 @@
  * - workspace is caller-allocated device scratch of at least
  *   vsa_workspace_size() bytes, 256-byte aligned. Its first 256 bytes hold
  *   a device status word that kernels set if an internal wait times out
- *   (read it with vsa_device_status). The rest is scratch that one call
- *   does not pass to the next. Calls that share a workspace must not run
- *   concurrently.
+ *   (read it with vsa_device_status). The rest is scratch; the only values
+ *   one call passes to the next are the tile means that vsa_fwd_reuse /
+ *   vsa_bwd_reuse are told to keep. Calls that share a workspace must not
+ *   run concurrently.
  */
 #ifndef VSA_H
 #define VSA_H
@@ -352,8 +353,9 @@ vsa_status vsa_head_slice(const vsa_desc *desc, int groups, int g, vsa_desc *sli
  * soon as they are final (O and LSE after the forward, the gradients after
  * the backward); two staging slots alternate.
  * Each slice runs vsa_build_block_map (topk, with the KV-owned index),
- * vsa_fwd and vsa_bwd on its own descriptor, so every output is
- * bit-identical to those calls on the whole problem.
+ * vsa_fwd_reuse and vsa_bwd_reuse (the tile means pooled once per slice)
+ * on its own descriptor, so every output is bit-identical to vsa_fwd and
+ * vsa_bwd on the whole problem.
  *   q, k, v, dO:   host, in desc's layout and dtype (page-locked memory
  *                  lets the copies run asynchronously and overlap);
  *   gate:          host, q-shaped, or NULL (no compression branch); with a

@@ -26,6 +26,8 @@ def cases():
                  topk=2, seed=74), 1),
         (Problem("host-gated-ragged", "bshd", 1, 4, 4, 128, 256, 256, 3, 5, q_var=[256, 160, 256],
                  kv_var=[256, 160, 64, 40, 256], topk=3, gate="uniform_token_head", seed=75), 2),
+        (Problem("host-twelve-heads", "bshd", 1, 12, 12, 128, 256, 256, 2, 4, q_var=[256, 256],
+                 kv_var=[256, 256, 100, 256], topk=2, seed=76), 4),
     ]
 
 
