@@ -24,7 +24,8 @@
 // Two staging slots alternate; a slot's inputs are refilled once the step
 // that read them is done, and its outputs are rewritten once their copy
 // back is done (events). Within a slice the forward starts once q, k, v
-// have landed (dO follows during it), and O goes back during the backward. A head slice is a strided 2D region of every
+// have landed (dO follows during it), O goes back during the backward and
+// dk, dv during the dQ pass. A head slice is a strided 2D region of every
 // layout (BSHD/TND: a run of Hs*D elements per token; BHSD: a run of
 // Hs*S*D per batch entry), copied with cudaMemcpy2DAsync. The step per
 // slice calls the same entry points as a device caller (vsa_build_block_map,
@@ -181,9 +182,9 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
 
     cudaStream_t sc = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    // per slot: q/k/v landed, dO landed, forward done, step done, copies back done
-    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[2] = {}, ev_do[2] = {}, ev_fwd[2] = {}, ev_comp[2] = {},
-                ev_out[2] = {};
+    // per slot: q/k/v landed, dO landed, forward done, dk/dv final, step done, copies back done
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[2] = {}, ev_do[2] = {}, ev_fwd[2] = {}, ev_dkv[2] = {},
+                ev_comp[2] = {}, ev_out[2] = {};
     vsa_status rc = VSA_OK;
     auto cu = [&](cudaError_t e) {
         if (e != cudaSuccess && rc == VSA_OK) rc = status_from_cuda(e);
@@ -199,8 +200,8 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
               cu(cudaEventCreateWithFlags(&ev_start, evf)) && cu(cudaEventCreateWithFlags(&ev_end, evf));
     for (int i = 0; ok && i < 2; ++i)
         ok = cu(cudaEventCreateWithFlags(&ev_in[i], evf)) && cu(cudaEventCreateWithFlags(&ev_do[i], evf)) &&
-             cu(cudaEventCreateWithFlags(&ev_fwd[i], evf)) && cu(cudaEventCreateWithFlags(&ev_comp[i], evf)) &&
-             cu(cudaEventCreateWithFlags(&ev_out[i], evf));
+             cu(cudaEventCreateWithFlags(&ev_fwd[i], evf)) && cu(cudaEventCreateWithFlags(&ev_dkv[i], evf)) &&
+             cu(cudaEventCreateWithFlags(&ev_comp[i], evf)) && cu(cudaEventCreateWithFlags(&ev_out[i], evf));
     // both side streams start after what the caller queued before this call
     ok = ok && cu(cudaEventRecord(ev_start, sc)) && cu(cudaStreamWaitEvent(s_in, ev_start, 0)) &&
          cu(cudaStreamWaitEvent(s_out, ev_start, 0));
@@ -246,19 +247,21 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
              cu(cudaEventRecord(ev_fwd[slot], sc));
         if (ok && train)
             ok = cu(cudaStreamWaitEvent(sc, ev_do[slot], 0)) &&
-                 vs(vsa_bwd_reuse(&sg, base + Lg.dO, base + Lg.q, base + Lg.k, base + Lg.v,
-                                  gated ? osp_d : base + Lg.out, lse_d, qidx, qcnt, cap, kvptr, kvqidx, q_var, kv_var,
-                                  g_d, base + Lg.dq, base + Lg.dk, base + Lg.dv,
-                                  VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS, ws, Lg.ws_bytes, stream));
+                 vs(bwd_reuse_event(&sg, base + Lg.dO, base + Lg.q, base + Lg.k, base + Lg.v,
+                                    gated ? osp_d : base + Lg.out, lse_d, qidx, qcnt, cap, kvptr, kvqidx, q_var,
+                                    kv_var, g_d, base + Lg.dq, base + Lg.dk, base + Lg.dv,
+                                    VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS, ws, Lg.ws_bytes, stream, ev_dkv[slot]));
         ok = ok && cu(cudaEventRecord(ev_comp[slot], sc));
-        // outputs of slice g: O and LSE are final after the forward, the
-        // gradients after the backward
+        // outputs of slice g: O and LSE are final after the forward, dk and
+        // dv after the dK/dV pass (they go back while dQ is computed), dq at
+        // the end of the step
         ok = ok && cu(cudaStreamWaitEvent(s_out, ev_fwd[slot], 0));
         if (ok && out) ok = cu(copy_out(out, base + Lg.out, rq, s_out));
         if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, hk0 * qpk, sg.Hq), s_out));
         if (ok && train)
-            ok = cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) && cu(copy_out(dq, base + Lg.dq, rq, s_out)) &&
-                 cu(copy_out(dk, base + Lg.dk, rk, s_out)) && cu(copy_out(dv, base + Lg.dv, rk, s_out));
+            ok = cu(cudaStreamWaitEvent(s_out, ev_dkv[slot], 0)) && cu(copy_out(dk, base + Lg.dk, rk, s_out)) &&
+                 cu(copy_out(dv, base + Lg.dv, rk, s_out)) && cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) &&
+                 cu(copy_out(dq, base + Lg.dq, rq, s_out));
         ok = ok && cu(cudaEventRecord(ev_out[slot], s_out));
     }
     // the caller's stream completes after the last copy back (and after the
@@ -272,6 +275,7 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
         if (ev_in[i]) cudaEventDestroy(ev_in[i]);
         if (ev_do[i]) cudaEventDestroy(ev_do[i]);
         if (ev_fwd[i]) cudaEventDestroy(ev_fwd[i]);
+        if (ev_dkv[i]) cudaEventDestroy(ev_dkv[i]);
         if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
         if (ev_out[i]) cudaEventDestroy(ev_out[i]);
     }

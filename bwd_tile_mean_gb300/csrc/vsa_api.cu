@@ -433,7 +433,7 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
                     const int32_t *q_sub, int block_q, int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx,
                     const int32_t *kv_qsub, const int32_t *q_var, const int32_t *kv_var, const void *gate,
                     void *dq, void *dk, void *dv, int reuse, void *workspace, size_t workspace_bytes,
-                    vsa_stream_t stream) {
+                    vsa_stream_t stream, cudaEvent_t dkdv_done = nullptr) {
     if ((reuse & ~(VSA_REUSE_QK_MEANS | VSA_REUSE_V_MEANS)) != 0) return VSA_ERR_SHAPE;
     Prob p0, p;
     VSA_TRY(to_prob(desc, &p0));
@@ -486,6 +486,7 @@ vsa_status bwd_impl(const vsa_desc *desc, const void *dO, const void *q, const v
     VSA_CUDA(launch_dk_order(p, kv_ptr, idx_cap, order, at<int>(workspace, L.okeys), s));
     a.dk_order = order;
     VSA_CUDA(launch_bwd_dkdv(p, a, s));
+    if (dkdv_done) VSA_CUDA(cudaEventRecord(dkdv_done, s));  // dk, dv final before dQ's pass
     VSA_CUDA(launch_bwd_dq(p, a, s));
     return VSA_OK;
 }
@@ -508,6 +509,21 @@ vsa_status vsa_bwd_reuse(const vsa_desc *desc, const void *dO, const void *q, co
     return bwd_impl(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, nullptr, 0, idx_cap, kv_ptr, kv_qidx, nullptr,
                     q_var, kv_var, gate, dq, dk, dv, reuse, workspace, workspace_bytes, stream);
 }
+
+}  // extern "C"
+
+namespace vsa {
+vsa_status bwd_reuse_event(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                           const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt,
+                           int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var,
+                           const int32_t *kv_var, const void *gate, void *dq, void *dk, void *dv, int reuse,
+                           void *workspace, size_t workspace_bytes, vsa_stream_t stream, cudaEvent_t dkdv_done) {
+    return bwd_impl(desc, dO, q, k, v, o_sparse, lse, q_idx, q_cnt, nullptr, 0, idx_cap, kv_ptr, kv_qidx, nullptr,
+                    q_var, kv_var, gate, dq, dk, dv, reuse, workspace, workspace_bytes, stream, dkdv_done);
+}
+}  // namespace vsa
+
+extern "C" {
 
 vsa_status vsa_bwd_blocks(const vsa_desc *desc, int block_q, const void *dO, const void *q, const void *k,
                           const void *v, const void *out, const float *lse, const int32_t *q_idx,

@@ -17,6 +17,14 @@ void prof_end(cudaStream_t s);
 // VSA_OK for cudaSuccess; otherwise records the error (vsa_last_cuda_error)
 // and returns VSA_ERR_CUDA.
 vsa_status status_from_cuda(cudaError_t e);
+// vsa_bwd_reuse that also records `dkdv_done` on the stream once dk and dv
+// are final (after the dK/dV pass, before the dQ pass), so a caller can
+// start copying them while dQ is computed.
+vsa_status bwd_reuse_event(const vsa_desc *desc, const void *dO, const void *q, const void *k, const void *v,
+                           const void *o_sparse, const float *lse, const int32_t *q_idx, const int32_t *q_cnt,
+                           int idx_cap, const int32_t *kv_ptr, const int32_t *kv_qidx, const int32_t *q_var,
+                           const int32_t *kv_var, const void *gate, void *dq, void *dk, void *dv, int reuse,
+                           void *workspace, size_t workspace_bytes, vsa_stream_t stream, cudaEvent_t dkdv_done);
 
 // Identity (cuCtxGetId) of the calling thread's current CUDA context, 0 if
 // there is none yet. A device reset gives the device a new context and so

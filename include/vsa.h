@@ -350,8 +350,8 @@ vsa_status vsa_head_slice(const vsa_desc *desc, int groups, int g, vsa_desc *sli
  * copied host -> device (strided 2D copies into a compact staging slot) on
  * an internal stream while earlier slices compute on `stream`, and each
  * slice's results are copied device -> host on a second internal stream as
- * soon as they are final (O and LSE after the forward, the gradients after
- * the backward); two staging slots alternate.
+ * soon as they are final (O and LSE after the forward, dk and dv after the
+ * dK/dV pass, dq after the dQ pass); two staging slots alternate.
  * Each slice runs vsa_build_block_map (topk, with the KV-owned index),
  * vsa_fwd_reuse and vsa_bwd_reuse (the tile means pooled once per slice)
  * on its own descriptor, so every output is bit-identical to vsa_fwd and

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 from bwd_tile_mean_gb300 import vsa
-from bwd_tile_mean_gb300.inputs import Problem, make_tensors
-from tests.helpers import plan_for, to_device
+from bwd_tile_mean_gb300.inputs import Problem, make_tensors, tnd_problem
+from tests.helpers import plan_for
 
 pytestmark = pytest.mark.gpu
 
@@ -26,9 +26,14 @@ def test_static_scratch_matches_workspace_entry_point_twice():
                 kv_var=[256, 173, 0, 79, 256, 256, 12, 256, 128], topk=3, seed=41),
         Problem("noalloc-b", "bhsd", 2, 2, 2, 128, 128, 128, 5, 7, q_var=[128] * 5,
                 kv_var=[128, 5, 128, 0, 77, 128, 1], topk=2, seed=42, dtype="fp16"),
+        tnd_problem("noalloc-tnd", [300, 17, 129, 256], [540, 23, 200, 383], 6, 3, dtype="fp16", topk=2,
+                    seed=43),
+        # just under the array's size: 16 * 1000 * 128 * 2 = 4,096,000 of 4,194,304 floats
+        Problem("noalloc-near-limit", "bshd", 1, 16, 16, 128, 128, 128, 1000, 1000, q_var=[128] * 1000,
+                kv_var=[128] * 999 + [77], topk=8, seed=44),
     ]
     for p in problems:  # two calls in a row, on different problems, reuse the array
-        t = to_device(make_tensors(p))
+        t = make_tensors(p, device="cuda")
         ref = plan_for(p)
         ref.build_block_map(t["q"], t["k"], p.topk, need_bwd_index=True)
         want = _outputs(ref)
