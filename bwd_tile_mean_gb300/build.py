@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libvsa.so")
 SOURCES = ["vsa_api.cu", "index_kernels.cu", "fwd_kernel.cu", "bwd_kernels.cu", "noalloc.cu", "tile3d.cu", "waitcheck.cu",
-           "host_step.cu", "check_inputs.cu"]
+           "host_step.cu", "check_inputs.cu", "compress_kernels.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]

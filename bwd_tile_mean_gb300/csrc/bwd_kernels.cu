@@ -1,5 +1,6 @@
 // bwd_kernels.cu -- block-sparse attention backward on tcgen05, plus the
-// row-sum preprocess and the gated compression branch's backward.
+// row-sum preprocess and the compression gate's gradient (the compression
+// branch's own backward is in compress_kernels.cu).
 //
 // Pages: Ascend test_npu_block_sparse_attention_backward.py
 // (_softmax_backward_np: dS = P (dP - rowsum(P dP)); the TND/GQA backward
@@ -963,126 +964,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
 }
 
-// --------------------------------------------------- compression backward
-// dc_i = sum over the query rows of tile i of gate (*) dO (fp32, per dim).
-template <typename T>
-__global__ void __launch_bounds__(128) k_compress_dc(Prob p, const T *__restrict__ dO, const T *__restrict__ gate,
-                                                     float *__restrict__ dc) {
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, e = threadIdx.x;
-    const int rows = q_rows(p, b, i);
-    float acc = 0.f;
-    for (int t = 0; t < rows; ++t) {
-        const long long o = tok_off(p, true, b, i * p.tile_q + t, h) + e;
-        acc = fmaf(to_f<T>(gate[o]), to_f<T>(dO[o]), acc);
-    }
-    dc[(((long long)b * p.Hq + h) * p.nQ + i) * 128 + e] = acc;
-}
-
-// Per query tile: A_j (softmax over non-empty KV tiles of scale pq.pk_j),
-// dA_j = dc . pv_j, ds_j = A_j (dA_j - sum A dA); stores A and ds, and
-// dpq = scale sum_j ds_j pk_j.
-__global__ void __launch_bounds__(128) k_compress_rows(Prob p, const float *__restrict__ pq,
-                                                       const float *__restrict__ pk, const float *__restrict__ pv,
-                                                       const float *__restrict__ dc, float *__restrict__ A,
-                                                       float *__restrict__ ds, float *__restrict__ dpq) {
-    extern __shared__ float sh[];  // sA[nKV], sD[nKV]
-    float *sA = sh, *sD = sh + p.nKV;
-    __shared__ __align__(16) float spq[128];
-    __shared__ __align__(16) float sdc[128];
-    __shared__ float red[4];
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
-    spq[t] = pq[row * 128 + t];
-    sdc[t] = dc[row * 128 + t];
-    __syncthreads();
-    const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
-    const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
-    // scores and dA: warp w takes tiles j = w, w+4, ...; its lanes split the
-    // 128 dims (one float4 each, coalesced) and reduce across the warp
-    float mx = -INFINITY;
-    const float4 q4 = reinterpret_cast<const float4 *>(spq)[lane];
-    const float4 c4 = reinterpret_cast<const float4 *>(sdc)[lane];
-    for (int j = w; j < p.nKV; j += 4) {
-        float x = -INFINITY, da = 0.f;
-        if (kv_valid(p, b, j) > 0) {
-            const float4 k4 = reinterpret_cast<const float4 *>(pkh + (long long)j * 128)[lane];
-            const float4 v4 = reinterpret_cast<const float4 *>(pvh + (long long)j * 128)[lane];
-            float acc = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
-            float acc2 = c4.x * v4.x + c4.y * v4.y + c4.z * v4.z + c4.w * v4.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                acc2 += __shfl_xor_sync(0xffffffffu, acc2, off);
-            }
-            x = acc * p.scale;
-            da = acc2;
-        }
-        if (lane == 0) {
-            sA[j] = x;
-            sD[j] = da;
-        }
-        mx = fmaxf(mx, x);
-    }
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[w] = mx;
-    __syncthreads();
-    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    float sum = 0.f;
-    for (int j = t; j < p.nKV; j += 128) {
-        const float ev = sA[j] == -INFINITY ? 0.f : __expf(sA[j] - mx);
-        sA[j] = ev;
-        sum += ev;
-    }
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) red[w] = sum;
-    __syncthreads();
-    sum = red[0] + red[1] + red[2] + red[3];
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    __syncthreads();
-    float sad = 0.f;
-    for (int j = t; j < p.nKV; j += 128) {
-        sA[j] *= inv;
-        sad += sA[j] * sD[j];
-    }
-    for (int off = 16; off > 0; off >>= 1) sad += __shfl_xor_sync(0xffffffffu, sad, off);
-    if (lane == 0) red[w] = sad;
-    __syncthreads();
-    sad = red[0] + red[1] + red[2] + red[3];
-    for (int j = t; j < p.nKV; j += 128) {
-        const float d = sA[j] * (sD[j] - sad);
-        sD[j] = d;
-        A[row * p.nKV + j] = sA[j];
-        ds[row * p.nKV + j] = d;
-    }
-    __syncthreads();
-    float acc = 0.f;
-    for (int j = 0; j < p.nKV; ++j) acc = fmaf(sD[j], pkh[(long long)j * 128 + t], acc);
-    dpq[row * 128 + t] = acc * p.scale;
-}
-
-// Per KV tile: dpv_j = sum_{h in group, i} A_ij dc_i and
-// dpk_j = scale sum_{h, i} ds_ij pq_i.
-__global__ void __launch_bounds__(128) k_compress_cols(Prob p, const float *__restrict__ pq,
-                                                       const float *__restrict__ dc, const float *__restrict__ A,
-                                                       const float *__restrict__ ds, float *__restrict__ dpk,
-                                                       float *__restrict__ dpv) {
-    const int j = blockIdx.x, hk = blockIdx.y, b = blockIdx.z, e = threadIdx.x, g = p.Hq / p.Hkv;
-    float ak = 0.f, av = 0.f;
-    for (int h = hk * g; h < hk * g + g; ++h) {
-        const long long base = ((long long)b * p.Hq + h) * p.nQ;
-        for (int i = 0; i < p.nQ; ++i) {
-            const long long row = base + i;
-            ak = fmaf(ds[row * p.nKV + j], pq[row * 128 + e], ak);
-            av = fmaf(A[row * p.nKV + j], dc[row * 128 + e], av);
-        }
-    }
-    const long long o = (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 + e;
-    dpk[o] = ak * p.scale;
-    dpv[o] = av;
-}
-
 }  // namespace
 
 namespace {
@@ -1213,26 +1094,5 @@ cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate, const float *pq, const float *pk,
-                                const float *pv, float *dc, float *A, float *ds, float *dpq, float *dpk,
-                                float *dpv, cudaStream_t s) {
-    dim3 gq(p.nQ, p.Hq, p.B), gk(p.nKV, p.Hkv, p.B);
-    prof_begin("compress_dc", s);
-    if (p.dtype == T_BF16)
-        k_compress_dc<__nv_bfloat16><<<gq, 128, 0, s>>>(p, (const __nv_bfloat16 *)dO, (const __nv_bfloat16 *)gate, dc);
-    else
-        k_compress_dc<__half><<<gq, 128, 0, s>>>(p, (const __half *)dO, (const __half *)gate, dc);
-    prof_end(s);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    prof_begin("compress_rows", s);
-    k_compress_rows<<<gq, 128, sizeof(float) * 2 * p.nKV, s>>>(p, pq, pk, pv, dc, A, ds, dpq);
-    prof_end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    prof_begin("compress_cols", s);
-    k_compress_cols<<<gk, 128, 0, s>>>(p, pq, dc, A, ds, dpk, dpv);
-    prof_end(s);
-    return cudaGetLastError();
-}
 
 }  // namespace vsa

@@ -1,6 +1,7 @@
 // fwd_kernel.cu -- block-sparse attention forward on the 5th-generation
-// tensor core (tcgen05, accumulators in TMEM, operands staged by TMA), and
-// the forward of the gated compression branch.
+// tensor core (tcgen05, accumulators in TMEM, operands staged by TMA); the
+// gated compression branch's c comes from compress_kernels.cu and is added
+// in the epilogue.
 //
 // Pages: Ascend test_npu_block_sparse_attention_backward.py
 // (cpu_block_sparse_attention_tnd_gqa_with_lse: softmax attention over the
@@ -806,59 +807,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     }
 }
 
-// ----------------------------------------------------- compression fwd
-// One block per (b, h, query tile): a_j = scale pq . pk_j over non-empty
-// KV tiles, A = softmax(a), c[e] = sum_j A_j pv_j[e] (fp32).
-__global__ void __launch_bounds__(128) k_compress_fwd(Prob p, const float *__restrict__ pq,
-                                                      const float *__restrict__ pk,
-                                                      const float *__restrict__ pv, float *__restrict__ c) {
-    extern __shared__ float sA[];  // [nKV]
-    __shared__ __align__(16) float spq[128];
-    __shared__ float red[4];
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const long long row = ((long long)b * p.Hq + h) * p.nQ + i;
-    spq[t] = pq[row * 128 + t];
-    __syncthreads();
-    const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
-    const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
-    // scores: warp w takes tiles j = w, w+4, ...; its lanes split the 128
-    // dims (one float4 each, coalesced) and reduce across the warp
-    float mx = -INFINITY;
-    const float4 q4 = reinterpret_cast<const float4 *>(spq)[lane];
-    for (int j = w; j < p.nKV; j += 4) {
-        float x = -INFINITY;
-        if (kv_valid(p, b, j) > 0) {
-            const float4 k4 = reinterpret_cast<const float4 *>(pkh + (long long)j * 128)[lane];
-            float acc = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            x = acc * p.scale;
-        }
-        if (lane == 0) sA[j] = x;
-        mx = fmaxf(mx, x);
-    }
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[w] = mx;
-    __syncthreads();
-    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    float sum = 0.f;
-    for (int j = t; j < p.nKV; j += 128) {
-        const float e = (sA[j] == -INFINITY) ? 0.f : __expf(sA[j] - mx);
-        sA[j] = e;
-        sum += e;
-    }
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) red[w] = sum;
-    __syncthreads();
-    sum = red[0] + red[1] + red[2] + red[3];
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    float acc = 0.f;
-    for (int j = 0; j < p.nKV; ++j) acc = fmaf(sA[j], pvh[(long long)j * 128 + t], acc);
-    c[row * 128 + t] = acc * inv;
-}
-
 }  // namespace
 
 cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
@@ -902,14 +850,5 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk, const float *pv, float *c,
-                                cudaStream_t s) {
-    dim3 grid(p.nQ, p.Hq, p.B);
-    if (grid.x == 0) return cudaSuccess;
-    prof_begin("compress_fwd", s);
-    k_compress_fwd<<<grid, 128, sizeof(float) * p.nKV, s>>>(p, pq, pk, pv, c);
-    prof_end(s);
-    return cudaGetLastError();
-}
 
 }  // namespace vsa
