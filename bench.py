@@ -310,6 +310,14 @@ def head_shard(p, t, ws, rank, dev):
     return ps, ts, (q0, sd.Hq)
 
 
+def l2_note(q, k):
+    """How the step's inputs compare with L2 (no flush between steps)."""
+    qb, kb = q.numel() * q.element_size(), k.numel() * k.element_size()
+    size = "larger" if 4 * min(qb, kb) > 126e6 else "not all larger"
+    return (f"inputs {size} than L2 together (q, dO {qb / 1e6:.1f} MB each, k, v {kb / 1e6:.1f} MB each; "
+            f"126 MB L2); no flush")
+
+
 def host_link(h_in, d_in, h_out, d_out, dev, stream, e0, e1, reps=3):
     """This machine's host<->device copy rates (GB/s) for one contiguous tensor
     from / to pinned memory: each direction alone and both at once (the
@@ -522,8 +530,7 @@ def ours(args):
         "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
         "config": {"workload": wl, "selected_pairs": job_pairs, "tflop_per_step": job_flops / 1e12,
                    "fwd_tflop_per_step": fwd_flops * (job_flops / step_flops) / 1e12,
-                   "l2": "inputs larger than L2 (each of q, k, v, dO is 786 MB vs 126 MB L2); no flush"
-                   if args.config == 3 and not shard else "see workload sizes; no flush",
+                   "l2": l2_note(q, k),
                    "parallelism": (f"heads split over {ws} GPUs ({heads[1]} query heads each, no exchange)" if shard
                                    else f"replicas x{ws}")},
         "pct_of_peak": {"bf16_burst": value / ws / pk.get("bf16_tflops", 1900.0),
