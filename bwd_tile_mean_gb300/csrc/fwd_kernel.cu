@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // exactly those tiles right after.
 // Warp roles (each CTA): warps 0-7 softmax (warp w: TMEM lanes 32 (w % 4),
 // chunks of parity w / 4, and in the epilogue O columns [64 (w / 4), +64)),
-// warp 8 loads, warp 9 owns TMEM and (even CTA) issues the MMAs.
+// warp 8 loads, warp 9 owns TMEM and (even CTA) issues the S MMAs, warp 10
+// (even CTA) issues the O += P V MMAs.
 // TMEM columns: S buffers [0,128), [128,256), [256,384) (P packed into the
 // first 64 columns of its S buffer), O [384,512).
 constexpr int kF2Stages = 6;
@@ -487,7 +488,7 @@ constexpr int kF2KH = 16 * 1024;  // half a K chunk: 64 keys x 128 dims, two 64-
 constexpr int kF2VH = 16 * 1024;  // half a V chunk: 128 keys x 64 dims, one box
 constexpr int kF2OffK = kF2Q, kF2OffV = kF2OffK + kF2Stages * kF2KH, kF2OffCtl = kF2OffV + kF2Stages * kF2VH;
 constexpr size_t kF2Smem = kF2OffCtl + 2560;
-constexpr int kF2Threads = 320, kF2ProdWarp = 8, kF2MmaWarp = 9;
+constexpr int kF2Threads = 352, kF2ProdWarp = 8, kF2MmaWarp = 9, kF2PvWarp = 10;
 enum : unsigned { kSite2Prod = 0x111, kSite2Mma = 0x112, kSite2Soft = 0x113, kSite2Epi = 0x114 };
 
 // S = Q K_half^T for one chunk on the pair: A = the CTA's Q (boxes 16 KB
@@ -531,8 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     uint8_t *sQ = sm, *sK = sm + kF2OffK, *sV = sm + kF2OffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kF2OffCtl);
     uint64_t *b_q = bars, *b_kv = bars + 1, *b_free = b_kv + kF2Stages, *b_s = b_free + kF2Stages;
-    uint64_t *b_p = b_s + 3, *b_o = b_p + 3, *b_fin = b_o + 1, *b_mref = b_fin + 1;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 22 barriers (176 bytes)
+    uint64_t *b_p = b_s + 3, *b_o = b_p + 3, *b_fin = b_o + 1, *b_mref = b_fin + 2;
+    uint64_t *b_pvd = b_mref + 1;  // (even CTA) O += P V of buffer x's chunk done: x may take S again
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 26 barriers (208 bytes)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     volatile int *s_over = reinterpret_cast<volatile int *>(s_tmem + 3);       // a chunk passed SumLimit here
@@ -558,7 +560,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         }
         mbar_init(b_o, 1);
         mbar_init(b_fin, 1);
+        mbar_init(b_fin + 1, 1);
         mbar_init(b_mref, 4);  // the four warps that take chunk 0
+        for (int x = 0; x < 3; ++x) mbar_init(b_pvd + x, 1);
         *s_abort = 0;
         *s_over = 0;
         *s_over_peer = 0;
@@ -621,34 +625,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             issued_kv = c + 1;
         }
     } else if (warp == kF2MmaWarp && leader && N > 0) {
-        // ------------------------------------------- MMA issuer of the pair (whole warp, one lane issues)
+        // --------------------------- S issuer of the pair (whole warp, one lane issues)
+        // S(c) goes into buffer c % 3 once K(c) has landed and O += P V has
+        // read the chunk three back from that buffer.
         const uint32_t idS = idesc_f16(bf16, 256, 128, false, false);
-        const uint32_t idO = idesc_f16(bf16, 256, 128, false, true);
-        const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-        const uint32_t tO = tbase + 384;
+        const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
         bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSite2Mma);
-        for (int c = 0; ok && c < 3 && c < N; ++c) {
-            const int st = c % kF2Stages;
+        for (int c = 0; ok && c < N; ++c) {
+            const int st = c % kF2Stages, x = c % 3;
+            if (c >= 3 && !(ok = mbar_wait_warp(b_pvd + x, ((c / 3) - 1) & 1, s_abort, a.err, kSite2Mma))) break;
             if (!(ok = mbar_wait_warp(b_kv + st, (c / kF2Stages) & 1, s_abort, a.err, kSite2Mma))) break;
             tc_fence_after();
-            issue_qk2(tbase + c * 128, aQ, aK + st * kF2KH, idS);
-            mma2_commit_mc_w(b_s + c, 3);
+            issue_qk2(tbase + x * 128, aQ, aK + st * kF2KH, idS);
+            mma2_commit_mc_w(b_s + x, 3);
             mma_started = 1;
         }
+    } else if (warp == kF2PvWarp && leader && N > 0) {
+        // ------------------------ PV issuer of the pair (whole warp, one lane issues)
+        // Its waits for P overlap the S issuer's MMAs and the other way round.
+        // S(c) completed before the softmax could write P(c), so once
+        // O += P(c) V(c) is done both K(c) and V(c) are read.
+        const uint32_t idO = idesc_f16(bf16, 256, 128, false, true);
+        const uint32_t aV = smem_addr(sV);
+        const uint32_t tO = tbase + 384;
+        bool ok = true;
         for (int c = 0; ok && c < N; ++c) {
             const int st = c % kF2Stages, x = c % 3;
             if (!(ok = mbar_wait_warp(b_p + x, (c / 3) & 1, s_abort, a.err, kSite2Mma))) break;
             tc_fence_after();
             issue_pv2(tO, tbase + x * 128, aV + st * kF2VH, idO, c > 0);  // O += P(c) V(c)
-            mma2_commit_mc_w(b_free + st, 3);  // K(c), V(c) read; O holds chunks 0..c
-            const int n = c + 3;
-            if (n < N) {
-                const int sn = n % kF2Stages;
-                if (!(ok = mbar_wait_warp(b_kv + sn, (n / kF2Stages) & 1, s_abort, a.err, kSite2Mma))) break;
-                tc_fence_after();
-                issue_qk2(tbase + x * 128, aQ, aK + sn * kF2KH, idS);  // S(c+3) over P(c), read by the PV above
-                mma2_commit_mc_w(b_s + x, 3);
-            }
+            mma_started = 1;
+            mma2_commit_mc_w(b_free + st, 3);  // K(c), V(c) read, in both CTAs
+            mma2_commit_mc_w(b_pvd + x, 1);    // P(c) read: buffer x may take S(c + 3)
         }
         if (ok) mma2_commit_mc_w(b_o, 3);
     } else if (warp < 8) {
@@ -786,10 +794,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             while (globaltimer() - t0 < 100000ull) {
             }
         }
-        if (warp == kF2MmaWarp && mma_started) {  // the pair's MMAs finish before TMEM is released
+        if ((warp == kF2MmaWarp || warp == kF2PvWarp) && mma_started) {
+            // the MMAs this warp issued finish before TMEM is released
             int never = 0;
-            mma2_commit_mc_w(b_fin, 1);
-            __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
+            uint64_t *bf = b_fin + (warp == kF2PvWarp ? 1 : 0);
+            mma2_commit_mc_w(bf, 1);
+            __all_sync(0xffffffffu, mbar_wait(bf, 0, &never, nullptr, 0, 200000000ull));
         }
     }
     // the odd CTA's overflow flag goes to the even CTA, which records the tile
