@@ -29,7 +29,8 @@
 // layout (BSHD/TND: a run of Hs*D elements per token; BHSD: a run of
 // Hs*S*D per batch entry), copied with cudaMemcpy2DAsync. The step per
 // slice calls the same entry points as a device caller (vsa_build_block_map,
-// vsa_fwd_reuse, vsa_bwd_reuse on the slice's descriptor), so results are
+// vsa_fwd_reuse, and vsa_bwd_reuse through an internal variant that also
+// marks when dk and dv are final, on the slice's descriptor), so results are
 // bit-identical to running the whole problem on the device; with a gate, the
 // gated compression branch runs too (its tile means are per head as well,
 // and the three calls of a slice share its staging workspace, so q's and
@@ -37,7 +38,6 @@
 // forward). No
 // device memory is allocated here: the caller provides the staging buffer.
 #include <cstdint>
-#include <vector>
 
 #include "vsa.h"
 #include "vsa_internal.h"
@@ -92,8 +92,6 @@ SlotLayout slot_layout(const vsa_desc &s, int cap, bool gated) {
     return L;
 }
 
-// Key/value heads per slice, in order (they sum to hkv).
-std::vector<int> slice_plan(int hkv, int per_slice) { return std::vector<int>(hkv / per_slice, per_slice); }
 
 // The slice of heads [h0, h0 + hs) of a [.., H, ..] tensor as a 2D copy:
 // `rows` runs of `width` bytes, `pitch` bytes apart in the full tensor,
@@ -206,19 +204,13 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
     ok = ok && cu(cudaEventRecord(ev_start, sc)) && cu(cudaStreamWaitEvent(s_in, ev_start, 0)) &&
          cu(cudaStreamWaitEvent(s_out, ev_start, 0));
 
-    const int qpk = desc->Hq / desc->Hkv;     // query heads per key/value head
     const size_t row = (size_t)desc->D * 2;  // bytes per (token, head)
-    const std::vector<int> plan = slice_plan(desc->Hkv, sd.Hkv);
-    int hk0 = 0;  // first key/value head of slice g
-    for (int g = 0; ok && g < (int)plan.size(); hk0 += plan[g], ++g) {
-        const int slot = g & 1;
+    const vsa_desc &sg = sd;                 // every slice's problem
+    const SlotLayout &Lg = L;
+    for (int g = 0; ok && g < groups; ++g) {
+        const int slot = g & 1, hq0 = g * sg.Hq, hk0 = g * sg.Hkv;  // the slice's first heads
         uint8_t *base = static_cast<uint8_t *>(device_buf) + slot * L.bytes;
-        vsa_desc sg = sd;  // this slice's problem
-        sg.Hkv = plan[g];
-        sg.Hq = plan[g] * qpk;
-        const SlotLayout Lg = slot_layout(sg, cap, gated);
-        const Strided rq = head_slice(*desc, true, hk0 * qpk, sg.Hq, row),
-                      rk = head_slice(*desc, false, hk0, sg.Hkv, row);
+        const Strided rq = head_slice(*desc, true, hq0, sg.Hq, row), rk = head_slice(*desc, false, hk0, sg.Hkv, row);
         // inputs of slice g; the slot's previous inputs were read by step g-2
         if (g >= 2) ok = cu(cudaStreamWaitEvent(s_in, ev_comp[slot], 0));
         // (q, k, v first: the block map and the forward start before dO lands)
@@ -257,7 +249,7 @@ vsa_status step_host(const vsa_desc *desc, int groups, bool train, const void *q
         // the end of the step
         ok = ok && cu(cudaStreamWaitEvent(s_out, ev_fwd[slot], 0));
         if (ok && out) ok = cu(copy_out(out, base + Lg.out, rq, s_out));
-        if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, hk0 * qpk, sg.Hq), s_out));
+        if (ok && lse) ok = cu(copy_out(lse, lse_d, lse_slice(*desc, hq0, sg.Hq), s_out));
         if (ok && train)
             ok = cu(cudaStreamWaitEvent(s_out, ev_dkv[slot], 0)) && cu(copy_out(dk, base + Lg.dk, rk, s_out)) &&
                  cu(copy_out(dv, base + Lg.dv, rk, s_out)) && cu(cudaStreamWaitEvent(s_out, ev_comp[slot], 0)) &&
