@@ -113,10 +113,11 @@ cudaError_t launch_pool_qkv(const Prob &p, const void *q, float *pq, const void 
 // over ascending d, as in the fixed-order definition.
 //
 // Top-k: scores map to order-preserving 32-bit keys (-0 folded into +0, so
-// equal scores give equal keys); a 32-step bitwise search finds the k-th
-// largest key T (the largest T with at least k keys >= T). The selection is
-// every key > T plus the lowest-indexed keys == T up to k, which is the
-// repeated-argmax rule with ties to the lower tile index.
+// equal scores give equal keys); a radix search over four 8-bit digits
+// (a 256-bin histogram per warp and pass) finds the k-th largest key T
+// (the largest T with at least k keys >= T). The selection is every key > T
+// plus the lowest-indexed keys == T up to k, which is the repeated-argmax
+// rule with ties to the lower tile index.
 constexpr int kSelChunk = 128;
 constexpr int kSelPitch = 132;
 
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict_
     float *spk = sm;                                  // [kSelChunk][kSelPitch]
     float *spq = spk + kSelChunk * kSelPitch;         // [R][128]
     float *ssc = spq + R * 128;                       // [R][nKV]
+    int *shist = reinterpret_cast<int *>(ssc + R * p.nKV) + (threadIdx.x >> 5) * 256;  // this warp's 256 bins
     const int b = blockIdx.z, h = blockIdx.y, hk = h / (p.Hq / p.Hkv);
     const int i0 = blockIdx.x * R, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = 128;
@@ -208,17 +210,60 @@ __global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict_
         uint32_t T = 0xFFFFFFFFu;  // no key reaches it: nothing selected when k = 0
         int need = 0;             // keys == T to take, lowest index first
         if (k > 0) {
-            uint32_t pre = 0u;
-            for (int bit = 31; bit >= 0; --bit) {
-                const uint32_t cand = pre | (1u << bit);
-                int c = 0;
-                for (int j = lane; j < p.nKV; j += 32) c += score_key(sc[j]) >= cand;
-                if ((int)__reduce_add_sync(0xffffffffu, (unsigned)c) >= k) pre = cand;
+            // T is found 8 bits at a time from the top: among the keys that
+            // match the bits found so far, the digit at which the count of
+            // keys with a larger digit first reaches `rem` (the keys still
+            // to take); those larger keys are taken and leave `rem`. After
+            // the last digit, rem = the keys == T to take.
+            uint32_t prefix = 0u, known = 0u;
+            int rem = k;
+#pragma unroll 1
+            for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) shist[lane * 8 + u] = 0;
+                __syncwarp();
+                for (int j = lane; j < p.nKV; j += 32) {
+                    const uint32_t key = score_key(sc[j]);
+                    if ((key & known) == prefix) atomicAdd(&shist[(key >> shift) & 255u], 1);
+                }
+                __syncwarp();
+                // lane l holds the digits 255 - 8l down to 248 - 8l
+                int c[8], sum = 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    c[u] = shist[255 - 8 * lane - u];
+                    sum += c[u];
+                }
+                int inc = sum;  // keys with digits from 255 down to this lane's last
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+                    if (lane >= off) inc += y;
+                }
+                const int exc = inc - sum;
+                const int L = __ffs(__ballot_sync(0xffffffffu, exc < rem && inc >= rem)) - 1;
+                int digit = 0, above = 0;
+                if (lane == L) {
+                    int acc = exc;
+                    bool found = false;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {  // the first digit (descending) whose count reaches rem
+                        const bool here = !found && acc + c[u] >= rem;
+                        digit = here ? 255 - 8 * lane - u : digit;
+                        above = here ? acc : above;
+                        found = found || here;
+                        acc += c[u];
+                    }
+                }
+                digit = __shfl_sync(0xffffffffu, digit, L);
+                above = __shfl_sync(0xffffffffu, above, L);
+                rem -= above;
+                prefix |= (uint32_t)digit << shift;
+                known |= 255u << shift;
+                __syncwarp();  // every lane has read the bins before the next pass clears them
             }
-            T = pre;
-            int gt = 0;
-            for (int j = lane; j < p.nKV; j += 32) gt += score_key(sc[j]) > T;
-            need = k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+            T = prefix;
+            need = rem;
         }
         int cnt = 0, taken = 0;
         for (int j0 = 0; j0 < p.nKV; j0 += 32) {
@@ -241,7 +286,8 @@ __global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict_
 }
 
 size_t select_smem(int rpw, int nKV) {
-    return sizeof(float) * ((size_t)kSelChunk * kSelPitch + (size_t)8 * rpw * 128 + (size_t)8 * rpw * nKV);
+    return sizeof(float) * ((size_t)kSelChunk * kSelPitch + (size_t)8 * rpw * 128 + (size_t)8 * rpw * nKV) +
+           sizeof(int) * 8 * 256;  // one 256-bin histogram per warp
 }
 
 cudaError_t launch_select(const Prob &p, const float *pq, const float *pk, int topk, uint8_t *map, int *q_idx,
