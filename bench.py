@@ -311,11 +311,15 @@ def head_shard(p, t, ws, rank, dev):
 
 
 def l2_note(q, k):
-    """How the step's inputs compare with L2 (no flush between steps)."""
+    """How the step's inputs compare with the 126 MB L2 (no flush between steps)."""
     qb, kb = q.numel() * q.element_size(), k.numel() * k.element_size()
-    size = "larger" if 4 * min(qb, kb) > 126e6 else "not all larger"
-    return (f"inputs {size} than L2 together (q, dO {qb / 1e6:.1f} MB each, k, v {kb / 1e6:.1f} MB each; "
-            f"126 MB L2); no flush")
+    if min(qb, kb) > 126e6:
+        size = "each input larger than L2"
+    elif 2 * (qb + kb) > 126e6:
+        size = "inputs larger than L2 together, not each"
+    else:
+        size = "inputs fit in L2"
+    return f"{size} (q, dO {qb / 1e6:.1f} MB each; k, v {kb / 1e6:.1f} MB each; L2 126 MB); no flush"
 
 
 def host_link(h_in, d_in, h_out, d_out, dev, stream, e0, e1, reps=3):

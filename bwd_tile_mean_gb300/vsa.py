@@ -288,10 +288,13 @@ class Plan:
     max_seqlen_q / max_seqlen_kv (host ints) instead of Sq / Skv per batch.
 
     With a gate, the plan's methods keep the tile means in its workspace
-    between calls (vsa_fwd_reuse / vsa_bwd_reuse): it tracks what its own
-    calls pooled, so a module-level call that writes plan.workspace with
-    other tensors must be followed by build_block_map before the next gated
-    forward or backward.
+    between calls (vsa_fwd_reuse / vsa_bwd_reuse). It tracks what its own
+    calls pooled and reuses means only for the same tensor objects whose
+    torch version counter has not moved. Two things it cannot see must be
+    followed by build_block_map before the next gated forward or backward:
+    a module-level call that writes plan.workspace with other tensors, and
+    a write to q, k or v that bypasses the version counter (through a raw
+    pointer or .data).
     """
 
     def __init__(self, layout, dtype, B, Hq, Hkv, D, tile_q, tile_kv, nQ, nKV, Sq, Skv, idx_cap, gate=False,
