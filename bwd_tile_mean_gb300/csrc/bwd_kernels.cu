@@ -14,6 +14,7 @@
 // recompute S and dP on the tensor core, so neither needs atomics and every
 // output element is written by exactly one CTA.
 #include <climits>
+#include <type_traits>
 
 #include "sm103_ptx.cuh"
 #include "vsa_internal.h"
@@ -283,10 +284,12 @@ __device__ __forceinline__ void issue_ss(uint32_t d, uint32_t aA, uint32_t aB, u
 }
 // D (+)= A B with A [128 x 128] in TMEM (packed 16-bit pairs, 8 columns per
 // K = 16) and B [K = 128 rows x N = 128] stored row-major (N contiguous),
-// read MN-major (D halves 16 KB apart, 8-row groups 1 KB apart).
+// read MN-major (D halves 16 KB apart, 8-row groups 1 KB apart). KS = the
+// K = 16 steps taken: 8, or 4 for the first 64 rows of B only.
+template <int KS = 8>
 __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t aB, uint32_t idesc, bool acc) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
+    for (int kk = 0; kk < KS; ++kk)
         mma_f16_ts_w(d, a_tmem + kk * 8, sdesc_sw128(aB + kk * 2048, kBox, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -676,7 +679,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 constexpr int kDqKStages = 3, kDqVStages = 2;
 constexpr int kDqOffQ = 0, kDqOffO = kTile, kDqOffK = 2 * kTile, kDqOffV = (2 + kDqKStages) * kTile;
 constexpr int kDqOffCtl = kDqOffV + kDqVStages * kTile;
-constexpr size_t kDqSmem = kDqOffCtl + 256;
+constexpr int kDqOffHalf = kDqOffCtl + 256;  // one bit per chunk: at most 64 valid keys
+constexpr size_t kDqSmem = kDqOffHalf + kMaxChunks / 8;
+static_assert(kDqSmem <= 232448, "dQ shared memory exceeds the 227 KB a CTA may use");
 
 template <typename T>
 __global__ void __launch_bounds__(kDqThreads, 1)
@@ -698,6 +703,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 22);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
+    unsigned *s_half = reinterpret_cast<unsigned *>(sm + kDqOffHalf);  // [kMaxChunks / 32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int subs = p.tile_q >> 7;
@@ -738,16 +744,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (warp == kProdWarp) {
         // number of 128-key chunks with valid keys (counts clamped to
         // idx_cap, tile ids outside [0, nKV) skipped, as in win_load)
+        // and, per chunk, whether it holds at most 64 valid keys (then its
+        // MMAs run over the first 64 keys only)
         const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);
         const int *idx = a.q_idx + qrow * a.cap;
         const int per = p.tile_kv >> 7;
-        int total = 0;
-        for (int n = lane; n < cnt; n += 32) {
-            const int j = idx[n];
-            total += (j >= 0 && j < p.nKV) ? min(per, (kv_valid(p, b, j) + 127) >> 7) : 0;
-        }
+        for (int x = lane; x < kMaxChunks / 32; x += 32) s_half[x] = 0u;
+        __syncwarp();
+        int total = 0;  // chunks of the entries before this group of 32
+        for (int n0 = 0; n0 < cnt; n0 += 32) {
+            const int n = n0 + lane, j = n < cnt ? idx[n] : -1;
+            const int kvv = (j >= 0 && j < p.nKV) ? kv_valid(p, b, j) : 0;
+            const int nch = min(per, (kvv + 127) >> 7);
+            int inc = nch;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += y;
+            }
+            for (int k = 0, ci = total + inc - nch; k < nch; ++k, ++ci)
+                if (ci < kMaxChunks && kvv - k * 128 <= 64) atomicOr(&s_half[ci >> 5], 1u << (ci & 31));
+            total += __shfl_sync(0xffffffffu, inc, 31);
+        }
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
     } else if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
@@ -804,17 +822,26 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         // each, the read of one overlaps the other's MMAs.
         const bool isP = warp == kDqPMmaWarp;
         const uint32_t idS = idesc_f16(bf16, 128, 128, false, false);
+        const uint32_t idS64 = idesc_f16(bf16, 128, 64, false, false);  // chunks of at most 64 valid keys
         const uint32_t aA = smem_addr(isP ? sO : sQ), aB = smem_addr(isP ? sV : sK);
         const uint32_t tD = tbase + (isP ? 128 : 0);
         const int nst = isP ? kDqVStages : kDqKStages;
         uint64_t *b_full = isP ? b_vf : b_kf;
         bool ok = mbar_wait_warp(b_q, 0, s_abort, a.err, kSiteDqMma);
+        unsigned hw = 0u;  // the chunk bits of c's word, read once per 32 chunks ahead of the waits
         for (int c = 0; ok && c < N; ++c) {
             const int sx = c % nst;
+            if ((c & 31) == 0) hw = s_half[c >> 5];
+            const bool hc = (hw >> (c & 31)) & 1u;
             if (!(ok = mbar_wait_warp(b_full + sx, (c / nst) & 1, s_abort, a.err, kSiteDqMma))) break;
             if (c > 0 && !(ok = mbar_wait_warp(b_sfree + isP, (c - 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ss(tD, aA, aB + sx * kTile, idS);  // S = Q K^T | dP = dO V^T
+            // S = Q K^T | dP = dO V^T, over the chunk's first 64 keys when no
+            // others are valid (a branch, so each form keeps its descriptor constant)
+            if (hc)
+                issue_ss(tD, aA, aB + sx * kTile, idS64);
+            else
+                issue_ss(tD, aA, aB + sx * kTile, idS);
             mma_commit_w(b_sf + isP);
             if (isP) mma_commit_w(b_ve + sx);  // V_c free once dP(c) is done
             mma_started = 1;
@@ -828,11 +855,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const uint32_t aK = smem_addr(sK);
         const uint32_t tQ = tbase + 256, tX = tbase + 384;
         bool ok = true;
+        unsigned hw = 0u;  // as for the S / dP issuers
         for (int c = 0; ok && c < N; ++c) {
             const int sk = c % kDqKStages;
+            if ((c & 31) == 0) hw = s_half[c >> 5];
+            const bool hc = (hw >> (c & 31)) & 1u;
             if (!(ok = mbar_wait_warp(b_dsf + (c & 1), (c >> 1) & 1, s_abort, a.err, kSiteDqMma))) break;
             tc_fence_after();
-            issue_ts(tQ, tX + (c & 1) * 64, aK + sk * kTile, idQ, c > 0);  // dQ += dS K
+            if (hc)  // dQ += dS K over the first 64 keys (the rest are not valid)
+                issue_ts<4>(tQ, tX + (c & 1) * 64, aK + sk * kTile, idQ, c > 0);
+            else
+                issue_ts(tQ, tX + (c & 1) * 64, aK + sk * kTile, idQ, c > 0);  // dQ += dS K
             mma_commit_w(b_dq + (c & 1));
             mma_commit_w(b_ke + sk);
             mma_started = 1;
@@ -849,57 +882,80 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         bool ok = true;
         ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, a.q_sub ? a.q_sub + qrow * a.cap : nullptr,
                                 clampi(a.q_cnt[qrow], 0, a.cap), lane);
-        for (int c = 0; c < N; ++c) {
-            int crow = 0, cval = 0, cbits = -1;
-            win_chunk(p, b, cw, c, lane, crow, cval, cbits);
-            int valid = cval - ch * 64;
-            // query blocks: a row whose block did not select this tile sees no key of it
-            if (a.q_sub && !((cbits >> ((half * 128 + r) / a.block_q)) & 1)) valid = 0;
-            uint32_t sr[64], dr[64];
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
-            if (!ok) break;
-            tc_fence_after();
-            tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-            tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(b_sfree);  // S of this chunk is in registers
-            ok = __all_sync(0xffffffffu, mbar_wait(b_sf + 1, c & 1, s_abort, a.err, kSiteDqSoft));
-            if (!ok) break;
-            tc_fence_after();
-            tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
-            tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(b_sfree + 1);  // and dP
-            if (valid < 64) {  // keys past the valid count: P = 0
-#pragma unroll
-                for (int kk = 0; kk < 64; ++kk)
-                    if (kk >= valid) sr[kk] = __float_as_uint(-INFINITY);
-            }
-            // P = 2^(S scale log2e - LSE log2e), dS = P (dP - Dvec), on pairs
-            const uint64_t sc2 = f32x2(sl2, sl2), nl2x = f32x2(nl2, nl2), nd2 = f32x2(ndv, ndv);
-            uint32_t dw[32];
-#pragma unroll
-            for (int t2 = 0; t2 < 32; ++t2) {
-                const float2 x = f32x2_split(
-                    ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2x));
-                const uint64_t pp = f32x2(ex2(x.x), ex2(x.y));
-                const uint64_t dd = fmul_x2(pp, fadd_x2(f32x2(__uint_as_float(dr[2 * t2]), __uint_as_float(dr[2 * t2 + 1])), nd2));
-                const float2 d2 = f32x2_split(dd);
-                dw[t2] = pack2<T>(d2.x, d2.y);
-            }
-            if (c >= 2) {  // dS buffer c&1 was read by dQ(c-2)
-                ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (c & 1), ((c >> 1) - 1) & 1, s_abort, a.err,
-                                                       kSiteDqSoft));
+        // The chunk loop is instantiated twice: with the half-chunk skip
+        // below, for query tiles that selected a chunk of at most 64 valid
+        // keys, and without it, so that the other tiles run a loop whose
+        // code the skip does not change.
+        auto chunks = [&](auto with_half) {
+            for (int c = 0; c < N; ++c) {
+                int crow = 0, cval = 0, cbits = -1;
+                win_chunk(p, b, cw, c, lane, crow, cval, cbits);
+                int valid = cval - ch * 64;
+                // query blocks: a row whose block did not select this tile sees no key of it
+                if (a.q_sub && !((cbits >> ((half * 128 + r) / a.block_q)) & 1)) valid = 0;
+                uint32_t sr[64], dr[64];
+                ok = __all_sync(0xffffffffu, mbar_wait(b_sf, c & 1, s_abort, a.err, kSiteDqSoft));
                 if (!ok) break;
                 tc_fence_after();
+                tmem_ld32(tl + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                tmem_ld32(tl + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(b_sfree);  // S of this chunk is in registers
+                ok = __all_sync(0xffffffffu, mbar_wait(b_sf + 1, c & 1, s_abort, a.err, kSiteDqSoft));
+                if (!ok) break;
+                tc_fence_after();
+                tmem_ld32(tl + 128 + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(dr));
+                tmem_ld32(tl + 128 + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(b_sfree + 1);  // and dP
+                // A chunk of at most 64 valid keys runs N = 64 MMAs (no S, dP for
+                // keys 64..127, which the loads above read as stale columns) and
+                // a dQ MMA over the first 64 keys only: the warps of the key half
+                // 64..127 write no dS. They still take every barrier in step, so
+                // no arrival of theirs can count towards another chunk's phase.
+                if constexpr (decltype(with_half)::value) {
+                    if (ch == 1 && cval <= 64) {
+                        mbar_arrive(b_dsf + (c & 1));
+                        continue;
+                    }
+                }
+                if (valid < 64) {  // keys past the valid count: P = 0
+    #pragma unroll
+                    for (int kk = 0; kk < 64; ++kk)
+                        if (kk >= valid) sr[kk] = __float_as_uint(-INFINITY);
+                }
+                // P = 2^(S scale log2e - LSE log2e), dS = P (dP - Dvec), on pairs
+                const uint64_t sc2 = f32x2(sl2, sl2), nl2x = f32x2(nl2, nl2), nd2 = f32x2(ndv, ndv);
+                uint32_t dw[32];
+    #pragma unroll
+                for (int t2 = 0; t2 < 32; ++t2) {
+                    const float2 x = f32x2_split(
+                        ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2x));
+                    const uint64_t pp = f32x2(ex2(x.x), ex2(x.y));
+                    const uint64_t dd = fmul_x2(pp, fadd_x2(f32x2(__uint_as_float(dr[2 * t2]), __uint_as_float(dr[2 * t2 + 1])), nd2));
+                    const float2 d2 = f32x2_split(dd);
+                    dw[t2] = pack2<T>(d2.x, d2.y);
+                }
+                if (c >= 2) {  // dS buffer c&1 was read by dQ(c-2)
+                    ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (c & 1), ((c >> 1) - 1) & 1, s_abort, a.err,
+                                                           kSiteDqSoft));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                tmem_st32(tl + 384 + (c & 1) * 64 + ch * 32, dw);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_dsf + (c & 1));
             }
-            tmem_st32(tl + 384 + (c & 1) * 64 + ch * 32, dw);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_dsf + (c & 1));
-        }
+        };
+        unsigned any_half = 0u;
+        for (int x = 0; x < (N + 31) / 32; ++x) any_half |= s_half[x];
+        if (any_half)
+            chunks(std::true_type{});
+        else
+            chunks(std::false_type{});
         if (ok && N > 0) {
             const int cp = N - 1;
             ok = __all_sync(0xffffffffu, mbar_wait(b_dq + (cp & 1), (cp >> 1) & 1, s_abort, a.err, kSiteDqSoft));

@@ -340,12 +340,15 @@ __global__ void __launch_bounds__(kCThreads) k_compress_cols(Prob p, const float
         }
 }
 
+// The row passes' shared memory depends on nKV; their limit is raised to
+// what any launch may use, once.
+constexpr int kCSmemCap = 200 * 1024;
 // Query tiles per CTA of the row passes: the most (up to kCQ) whose score
 // rows (rows_per_q floats per tile, per query tile) fit beside the staged
 // chunks in 200 KB of shared memory; 0 when not even one fits.
 int rows_per_cta(const Prob &p, int fixed_floats, int rows_per_q) {
     for (int qb = kCQ; qb >= 1; qb /= 2)
-        if ((size_t)(fixed_floats + (size_t)qb * rows_per_q * p.nKV) * 4 <= 200u * 1024u) return qb;
+        if ((size_t)(fixed_floats + (size_t)qb * rows_per_q * p.nKV) * 4 <= (size_t)kCSmemCap) return qb;
     return 0;
 }
 
@@ -358,7 +361,7 @@ cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk,
     const int qb = rows_per_cta(p, fixed, 1);
     if (qb == 0) return cudaErrorInvalidValue;
     const int smem = (fixed + qb * p.nKV) * 4;
-    const cudaError_t ae = ensure_smem_limit((const void *)k_compress_fwd, smem);
+    const cudaError_t ae = ensure_smem_limit((const void *)k_compress_fwd, kCSmemCap);
     if (ae != cudaSuccess) return ae;
     dim3 grid((p.nQ + qb - 1) / qb, p.Hq, p.B);
     prof_begin("compress_fwd", s);
@@ -384,7 +387,7 @@ cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate,
     const int qb = rows_per_cta(p, fixed, 2);
     if (qb == 0) return cudaErrorInvalidValue;
     const int smem = (fixed + 2 * qb * p.nKV) * 4;
-    if ((e = ensure_smem_limit((const void *)k_compress_rows, smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem_limit((const void *)k_compress_rows, kCSmemCap)) != cudaSuccess) return e;
     dim3 gr((p.nQ + qb - 1) / qb, p.Hq, p.B);
     prof_begin("compress_rows", s);
     k_compress_rows<<<gr, kCThreads, smem, s>>>(p, pq, pk, pv, dc, A, ds, dpq, qb);

@@ -119,8 +119,13 @@ PFN_cuCtxGetId_v12000 ctx_id_fn() {
     }
     return fn;
 }
+struct AttrSet {
+    unsigned long long ctx;  // context id
+    const void *kernel;
+    int bytes;               // the limit set there
+};
 std::mutex g_attr_mu;
-std::vector<std::pair<unsigned long long, const void *>> g_attr_done;  // (context id, kernel)
+std::vector<AttrSet> g_attr_done;
 }  // namespace
 
 unsigned long long current_context_id() {
@@ -139,14 +144,20 @@ cudaError_t ensure_smem_limit(const void *kernel, int bytes) {
     if (ctx) {
         std::lock_guard<std::mutex> lock(g_attr_mu);
         for (const auto &e : g_attr_done)
-            if (e.first == ctx && e.second == kernel) return cudaSuccess;
+            if (e.ctx == ctx && e.kernel == kernel && e.bytes >= bytes) return cudaSuccess;
     }
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     ctx = current_context_id();  // the call above brings the context up if it was not yet
     if (ctx) {
         std::lock_guard<std::mutex> lock(g_attr_mu);
-        g_attr_done.emplace_back(ctx, kernel);
+        bool found = false;
+        for (auto &x : g_attr_done)
+            if (x.ctx == ctx && x.kernel == kernel) {
+                x.bytes = bytes > x.bytes ? bytes : x.bytes;
+                found = true;
+            }
+        if (!found) g_attr_done.push_back({ctx, kernel, bytes});
     }
     return cudaSuccess;
 }

@@ -30,9 +30,10 @@ vsa_status bwd_reuse_event(const vsa_desc *desc, const void *dO, const void *q, 
 // there is none yet. A device reset gives the device a new context and so
 // a new id, which is how per-device set-up learns it must be redone.
 unsigned long long current_context_id();
-// Raises a kernel's dynamic shared-memory limit to `bytes` once per context
-// (the attribute belongs to the device's context, so every GPU and every
-// context after a reset gets its own call); thread-safe.
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` in the
+// current context (the attribute belongs to the device's context, so every
+// GPU and every context after a reset gets its own call); a later call with
+// a larger size raises it again. Thread-safe.
 cudaError_t ensure_smem_limit(const void *kernel, int bytes);
 
 // Host-side validation shared by the entry points: descriptor -> Prob
