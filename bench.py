@@ -451,8 +451,18 @@ def ours(args):
     # (training: q, k, v, dO [, gate] in, O, dq, dk, dv out; inference: q, k, v [, gate] in, O out)
     ins = (("q", q), ("k", k), ("v", v)) + ((("dO", dO),) if train else ()) + ((("gate", gate),) if gated else ())
     outs = (("out", out),) + ((("dq", dq), ("dk", dk), ("dv", dv)) if train else ())
+    # A throwaway allocation of twice their size is taken (and written)
+    # first and released once the buffers exist: on the Grace hosts these
+    # runs use, the first host memory a process took right after another
+    # process had released its own stalled 60-250 ms in about one copy in
+    # five, pinned by cudaHostAlloc or by cudaHostRegister alike, while
+    # buffers allocated after it stalled in 1 of 576 calls.
+    nbytes = sum(x.numel() * x.element_size() for _, x in list(ins) + list(outs))
+    throwaway = torch.empty(2 * nbytes, dtype=torch.uint8, pin_memory=True)
+    throwaway.fill_(0)
     host_in = {n: x.to("cpu").pin_memory() for n, x in ins}
     host_out = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for n, x in outs}
+    del throwaway
     groups = max(g for g in range(1, 9) if p.Hkv % g == 0)
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
@@ -544,6 +554,7 @@ def ours(args):
                 "h2d_bytes_per_step": job_h2d, "d2h_bytes_per_step": job_d2h,
                 "path": f"{'vsa_train_step_host' if train else 'vsa_fwd_step_host'}: {groups} head slices, "
                         "copies overlapped with the kernels",
+                "host_memory": "torch pinned (cudaHostAlloc), taken after a same-sized throwaway allocation",
                 "host_link_GB_per_s": link, "calls": e_steps,
                 "call_ms": {"median": round(statistics.median(per_call), 3), "min": round(min(per_call), 3),
                             "max": round(max(per_call), 3)}},

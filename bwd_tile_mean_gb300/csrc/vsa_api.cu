@@ -140,21 +140,21 @@ unsigned long long current_context_id() {
 }
 
 cudaError_t ensure_smem_limit(const void *kernel, int bytes) {
+    // one lock over the check and the set: a thread that needs less cannot
+    // set its limit after another thread raised it
+    std::lock_guard<std::mutex> lock(g_attr_mu);
     unsigned long long ctx = current_context_id();
-    if (ctx) {
-        std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (ctx)
         for (const auto &e : g_attr_done)
             if (e.ctx == ctx && e.kernel == kernel && e.bytes >= bytes) return cudaSuccess;
-    }
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     ctx = current_context_id();  // the call above brings the context up if it was not yet
     if (ctx) {
-        std::lock_guard<std::mutex> lock(g_attr_mu);
         bool found = false;
         for (auto &x : g_attr_done)
             if (x.ctx == ctx && x.kernel == kernel) {
-                x.bytes = bytes > x.bytes ? bytes : x.bytes;
+                x.bytes = bytes;  // only ever raised: a smaller request returned above
                 found = true;
             }
         if (!found) g_attr_done.push_back({ctx, kernel, bytes});
