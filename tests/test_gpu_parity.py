@@ -36,6 +36,13 @@ def extra_cases():
         Problem("topk-ge-nkv", "bshd", 1, 2, 1, 128, 256, 256, 2, 3, q_var=[256, 256], kv_var=[256, 40, 0],
                 topk=5, seed=23),
         topk_varlen(),
+        # chunks with exactly 64 and 65 valid keys on both sides of the
+        # 64-key form of dQ (first and second chunk of a 256-token tile),
+        # every non-empty tile selected
+        Problem("chunk-64-edges", "bshd", 1, 4, 2, 128, 256, 256, 3, 8, q_var=[256, 256, 256],
+                kv_var=[64, 65, 192, 193, 256, 63, 129, 0], topk=7, seed=24),
+        tnd_problem("tnd-chunk-64-edges", [300, 256, 129], [320, 449, 192], 4, 4, dtype="bf16", tile=256,
+                    topk=2, seed=25),
     ]
 
 
