@@ -83,15 +83,16 @@ template <typename T> struct SumLimit;
 template <> struct SumLimit<__nv_bfloat16> { static constexpr float value = 0x1p64f; };
 template <> struct SumLimit<__half> { static constexpr float value = 0x1p15f; };
 
-// P = exp2(scale log2e s - m) for the 128 scores of one row, packed to
-// 16-bit pairs into the 64 TMEM columns at taddr; returns the fp32 row sum
+// P = exp2(scale log2e s - m) for the 128 scores of one row (or the 32-key
+// quarters [Q0, Q1) of them), packed to 16-bit pairs into the 64 TMEM
+// columns at taddr; returns the fp32 row sum of those keys
 // (scale-and-subtract and the sum on paired f32 instructions).
-template <typename T>
+template <typename T, int Q0 = 0, int Q1 = 4>
 __device__ __forceinline__ float exp_row(const uint32_t (&sr)[128], float m, float sl2, uint32_t taddr) {
     const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m, -m);
     uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = Q0; q4 < Q1; ++q4) {
         uint32_t w16[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -501,10 +502,12 @@ __device__ __forceinline__ void issue_qk2(uint32_t d, uint32_t aQ, uint32_t aK, 
 }
 // O += P V_half on the pair: A = P in TMEM (128 keys packed in the S
 // buffer's first 64 columns, 8 per K = 16 step), B = the CTA's 64 head
-// dims of the chunk's 128 keys, read MN-major (8-key groups 1 KB apart).
+// dims of the chunk's 128 keys, read MN-major (8-key groups 1 KB apart);
+// K = 16 steps [K0, K1).
+template <int K0, int K1>
 __device__ __forceinline__ void issue_pv2(uint32_t d, uint32_t p_tmem, uint32_t aV, uint32_t idesc, bool acc) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
+    for (int kk = K0; kk < K1; ++kk)
         mma2_ts_w(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kF2VH, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -534,7 +537,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     uint64_t *b_q = bars, *b_kv = bars + 1, *b_free = b_kv + kF2Stages, *b_s = b_free + kF2Stages;
     uint64_t *b_p = b_s + 3, *b_o = b_p + 3, *b_fin = b_o + 1, *b_mref = b_fin + 2;
     uint64_t *b_pvd = b_mref + 1;  // (even CTA) O += P V of buffer x's chunk done: x may take S again
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 26 barriers (208 bytes)
+    uint64_t *b_plo = b_pvd + 3;   // (even CTA) P of buffer x's first 64 keys stored, in both CTAs
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 29 barriers (232 bytes)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     volatile int *s_over = reinterpret_cast<volatile int *>(s_tmem + 3);       // a chunk passed SumLimit here
@@ -563,6 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         mbar_init(b_fin + 1, 1);
         mbar_init(b_mref, 4);  // the four warps that take chunk 0
         for (int x = 0; x < 3; ++x) mbar_init(b_pvd + x, 1);
+        for (int x = 0; x < 3; ++x) mbar_init(b_plo + x, 8);  // as b_p
         *s_abort = 0;
         *s_over = 0;
         *s_over_peer = 0;
@@ -651,10 +656,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         bool ok = true;
         for (int c = 0; ok && c < N; ++c) {
             const int st = c % kF2Stages, x = c % 3;
+            // O += P(c) V(c) in two halves: keys 0..63 as soon as their P
+            // is stored, keys 64..127 once the softmax has finished the row
+            if (!(ok = mbar_wait_warp(b_plo + x, (c / 3) & 1, s_abort, a.err, kSite2Mma))) break;
+            tc_fence_after();
+            issue_pv2<0, 4>(tO, tbase + x * 128, aV + st * kF2VH, idO, c > 0);
+            mma_started = 1;
             if (!(ok = mbar_wait_warp(b_p + x, (c / 3) & 1, s_abort, a.err, kSite2Mma))) break;
             tc_fence_after();
-            issue_pv2(tO, tbase + x * 128, aV + st * kF2VH, idO, c > 0);  // O += P(c) V(c)
-            mma_started = 1;
+            issue_pv2<4, 8>(tO, tbase + x * 128, aV + st * kF2VH, idO, true);
             mma2_commit_mc_w(b_free + st, 3);  // K(c), V(c) read, in both CTAs
             mma2_commit_mc_w(b_pvd + x, 1);    // P(c) read: buffer x may take S(c + 3)
         }
@@ -669,6 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         bool ok = true, over = false;
         ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, cnt, lane);
         const uint32_t cp0 = cluster_addr(smem_addr(b_p), 0);
+        const uint32_t cplo = cluster_addr(smem_addr(b_plo), 0);
         for (int c = grp; c < N; c += 2) {
             const int x = c % 3;
             int crow = 0, valid = 0, cbits = -1;
@@ -708,7 +719,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
                 if (!(ok = mbar_wait_warp(b_mref, 0, s_abort, a.err, kSite2Soft))) break;
                 m_ref = s_mref[r];
             }
-            const float ls = exp_row<T>(sr, m_ref, sl2, tl + x * 128);
+            // P of keys 0..63 first, handed over before keys 64..127
+            float ls = exp_row<T, 0, 2>(sr, m_ref, sl2, tl + x * 128);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cplo + 8u * x);
+            ls += exp_row<T, 2, 4>(sr, m_ref, sl2, tl + x * 128);
             over = over || !(ls <= SumLimit<T>::value);
             l += ls;
             tmem_wait_st();
