@@ -323,7 +323,7 @@ def l2_note(q, k):
 
 
 def host_link(h_in, d_in, h_out, d_out, dev, stream, e0, e1, reps=3):
-    """This machine's host<->device copy rates (GB/s) for one contiguous tensor
+    """Host<->device copy rates (GB/s) of this machine for one contiguous tensor
     from / to pinned memory: each direction alone and both at once (the
     host-buffer step moves its inputs and outputs through this link)."""
     import torch
@@ -452,11 +452,11 @@ def ours(args):
     ins = (("q", q), ("k", k), ("v", v)) + ((("dO", dO),) if train else ()) + ((("gate", gate),) if gated else ())
     outs = (("out", out),) + ((("dq", dq), ("dk", dk), ("dv", dv)) if train else ())
     # A throwaway allocation of twice their size is taken (and written)
-    # first and released once the buffers exist: on the Grace hosts these
-    # runs use, the first host memory a process took right after another
-    # process had released its own stalled 60-250 ms in about one copy in
-    # five, pinned by cudaHostAlloc or by cudaHostRegister alike, while
-    # buffers allocated after it stalled in 1 of 576 calls.
+    # first and released once the buffers exist. On a Grace host, copies
+    # from the first host memory a process took right after another
+    # process had released its own were measured to stall 60-250 ms in
+    # about one copy in five, pinned by cudaHostAlloc or by cudaHostRegister
+    # alike, while buffers allocated after it stalled in 1 of 576 calls.
     nbytes = sum(x.numel() * x.element_size() for _, x in list(ins) + list(outs))
     throwaway = torch.empty(2 * nbytes, dtype=torch.uint8, pin_memory=True)
     throwaway.fill_(0)
