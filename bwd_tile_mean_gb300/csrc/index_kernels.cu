@@ -147,25 +147,30 @@ __global__ void __launch_bounds__(256) k_select(Prob p, const float *__restrict_
         reinterpret_cast<float4 *>(spq)[e] = v;
     }
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * D;
+    // The next chunk of key means is loaded into registers while the current
+    // one is scored, and stored to shared memory at the top of the next pass.
+    float4 buf[16];
+    auto load_chunk = [&](int j0) {
+        const int nj = min(kSelChunk, p.nKV - j0);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int e = threadIdx.x + u * 256;  // 4096 16-byte words per full chunk
+            buf[u] = e < nj * (D / 4) ? __ldg(reinterpret_cast<const float4 *>(pkh + (long long)j0 * D) + e)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_chunk(0);
     for (int j0 = 0; j0 < p.nKV; j0 += kSelChunk) {
         const int nj = min(kSelChunk, p.nKV - j0);
-        __syncthreads();
-        {
-            float4 buf[16];
+        __syncthreads();  // the previous chunk is scored
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = threadIdx.x + u * 256;  // 4096 16-byte words per full chunk
-                buf[u] = e < nj * (D / 4) ? __ldg(reinterpret_cast<const float4 *>(pkh + (long long)j0 * D) + e)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = threadIdx.x + u * 256;
-                if (e < nj * (D / 4))
-                    *reinterpret_cast<float4 *>(spk + (e / (D / 4)) * kSelPitch + (e % (D / 4)) * 4) = buf[u];
-            }
+        for (int u = 0; u < 16; ++u) {
+            const int e = threadIdx.x + u * 256;
+            if (e < nj * (D / 4))
+                *reinterpret_cast<float4 *>(spk + (e / (D / 4)) * kSelPitch + (e % (D / 4)) * 4) = buf[u];
         }
         __syncthreads();
+        if (j0 + kSelChunk < p.nKV) load_chunk(j0 + kSelChunk);
         float acc[RPW][4];
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
