@@ -20,6 +20,7 @@ sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -289,9 +290,10 @@ def layout_step(q, p, dev, stream, e0, e1):
 def workload(args):
     from bwd_tile_mean_gb300 import inputs
     p = inputs.config(args.config)
-    if args.config == 3 and args.heads != p.Hq:  # smaller copy of the same workload (profiling captures)
-        p = inputs.Problem(p.name, p.layout, p.B, args.heads, args.heads, p.D, p.tile_q, p.tile_kv, p.nQ, p.nKV,
-                           q_var=p.q_var, kv_var=p.kv_var, topk=p.topk, seed=p.seed)
+    if args.heads is not None and args.heads != p.Hq:  # smaller copy of the same workload (profiling captures)
+        if p.Hq != p.Hkv:
+            raise SystemExit("--heads applies to workloads with as many KV heads as query heads")
+        p = dataclasses.replace(p, Hq=args.heads, Hkv=args.heads)
     return p
 
 
@@ -575,7 +577,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--heads", type=int, default=40, help="heads of the workload (40; fewer only for profiling)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="heads of the workload (its own count by default; fewer only for profiling captures)")
     ap.add_argument("--config", type=int, default=3, choices=[1, 3, 4, 5, 6],
                     help="workload: 3 = video DiT 76,800 tokens (the headline); 1 tiny, 4 gated ragged, "
                          "5 long-video forward only, 6 the long-video grid taken literally (1,024 tiles)")
@@ -586,7 +589,7 @@ def main():
     ap.add_argument("--traffic-command", default="", help="the capture command, recorded with --write-traffic")
     args = ap.parse_args()
     if args.write_traffic:
-        write_traffic(args.write_traffic, args.heads, args.traffic_command)
+        write_traffic(args.write_traffic, args.heads if args.heads is not None else 40, args.traffic_command)
         return
     if args.warmup < 3:
         args.warmup = 3
