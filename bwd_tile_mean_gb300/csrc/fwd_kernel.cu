@@ -573,6 +573,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         *s_over_peer = 0;
         fence_mbar_init();
     }
+    // The producer reads the selection before the cluster sync: the chunk
+    // count every role needs, and the first window of its own walk, so
+    // that Q and the first K/V chunk are requested right after the sync.
+    ChunkWin pcw{};
     if (warp == kF2ProdWarp) {
         // number of 128-key chunks with valid keys (tile ids outside [0, nKV) skipped, as the walk does)
         const int *idx = a.q_idx + qrow * a.cap;
@@ -585,6 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
         if (lane == 0) *s_nchunk = total;
+        pcw = win_begin(p, b, idx, nullptr, cnt, lane);
     } else if (warp == kF2MmaWarp) {
         tmem_alloc2(s_tmem, 512);
         tmem_relinquish2();
@@ -599,7 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
 
     if (warp == kF2ProdWarp && N > 0) {
         // ------------------------------------------------------ producer (whole warp walks the chunks)
-        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, cnt, lane);
+        ChunkWin &cw = pcw;
         if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
