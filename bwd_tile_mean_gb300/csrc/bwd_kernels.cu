@@ -389,7 +389,8 @@ __device__ __forceinline__ bool work_advance(const Prob &p, const BwdArgs &a, in
 template <typename T>
 __global__ void __launch_bounds__(kDkThreads, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+           const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, const Prob p,
            const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
@@ -608,6 +609,13 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const float *cbase = ch ? a.dpk : a.dpv;
         const float *cadd = cbase ? cbase + (((long long)b * p.Hkv + hk) * p.nKV + j) * 128 : nullptr;
         const float mul = ch ? p.scale : 1.f;
+        // Padded layouts: the chunk's 128 rows of dV and dK are staged in the
+        // Q stages (free once every accumulation MMA is done) in the TMA box
+        // layout and stored by four box copies, instead of 16-byte stores
+        // that each touch 32 rows. A varlen chunk may end inside its tile
+        // (its last rows belong to the next sequence): per-thread stores.
+        const bool staged = p.layout != L_TND;
+        uint8_t *stage = sQ + ch * 2 * kBox;  // [2 boxes of 64 dims][128 rows x 128 B]
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t o[32];
@@ -630,9 +638,31 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 }
                 wv[e2] = pack2<T>(v0, v1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
+            if (staged) {
+                // dims q4*32 .. +31: box q4 / 2, 16-byte chunks 4 (q4 % 2) .. +3 of row u, 128-byte swizzle
+                uint8_t *rowp = stage + (q4 >> 1) * kBox + u * 128;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                for (int t = 0; t < 4; ++t)
+                    *reinterpret_cast<uint4 *>(rowp + ((((q4 & 1) * 4 + t) ^ (u & 7)) << 4)) =
+                        make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            }
+        }
+        if (staged) {
+            fence_proxy_async_smem();
+            named_sync(1, 256);  // the 8 epilogue warps have staged their rows
+            if (warp == 0 && lane == 0 && !*s_abort) {
+                for (int t = 0; t < 2; ++t) {
+                    tma_store_4d(t ? &tdk : &tdv, sQ + t * 2 * kBox, 0, key0, hk, bc);
+                    tma_store_4d(t ? &tdk : &tdv, sQ + t * 2 * kBox + kBox, 64, key0, hk, bc);
+                }
+                tma_store_commit();
+                tma_store_wait_read();  // the stage is read before this CTA's shared memory goes
+            }
         }
     }
 
@@ -1112,9 +1142,10 @@ cudaError_t launch_dk_order(const Prob &p, const int *kv_ptr, int cap, int *orde
 }
 
 cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     if (!make_tmap_rows(&tq, p, true, a.q, p.Hq, kDkItem) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
-        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, kDkItem))
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq, kDkItem) ||
+        !make_tmap_rows(&tdk, p, false, a.dk, p.Hkv) || !make_tmap_rows(&tdv, p, false, a.dv, p.Hkv))
         return cudaErrorInvalidValue;
     const long long units = dk_units(p);
     if (units == 0) return cudaSuccess;
@@ -1125,9 +1156,9 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     if (ae != cudaSuccess) return ae;
     prof_begin("bwd_dkdv", s);
     if (p.dtype == T_BF16)
-        k_dkdv<__nv_bfloat16><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__nv_bfloat16><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p, a);
     else
-        k_dkdv<__half><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dkdv<__half><<<grid, kDkThreads, kDkSmem, s>>>(tq, tk, tv, tdo, tdk, tdv, p, a);
     prof_end(s);
     return cudaGetLastError();
 }
