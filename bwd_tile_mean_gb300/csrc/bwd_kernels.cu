@@ -716,8 +716,8 @@ static_assert(kDqSmem <= 232448, "dQ shared memory exceeds the 227 KB a CTA may 
 template <typename T>
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dq(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const Prob p,
-         const BwdArgs a) {
+         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+         const __grid_constant__ CUtensorMap tdq, const Prob p, const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
     if ((smem_addr(sm) & 1023u) != 0) {
@@ -998,6 +998,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const bool add_c = a.dpq && (half * 128 + r) < qv;
         const float *cq = a.dpq ? a.dpq + qrow * 128 + ch * 64 : nullptr;
         const float inv = qv > 0 ? 1.f / (float)qv : 0.f;
+        // Padded layouts: the chunk's 128 rows of dQ are staged in the Q tile
+        // (free once the last S MMA is done) in the TMA box layout and stored
+        // by two box copies; varlen rows past the sequence must not be
+        // written, so there each thread stores its own row.
+        const bool staged = p.layout != L_TND;
 #pragma unroll 1
         for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t o[32];
@@ -1019,9 +1024,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
                 wv[e2] = pack2<T>(v0, v1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dq + q2 * 32);
+            if (staged) {
+                // columns 64 ch + 32 q2 .. +31: box ch, 16-byte chunks 4 q2 .. +3 of row r, 128-byte swizzle
+                uint8_t *rowp = sQ + ch * kBox + r * 128;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                for (int t = 0; t < 4; ++t)
+                    *reinterpret_cast<uint4 *>(rowp + (((q2 * 4 + t) ^ (r & 7)) << 4)) =
+                        make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dq + q2 * 32);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+            }
+        }
+        if (staged) {
+            fence_proxy_async_smem();
+            named_sync(1, 256);  // the 8 epilogue warps have staged their rows
+            if (warp == 0 && lane == 0 && !*s_abort) {
+                tma_store_4d(&tdq, sQ, 0, qrc, h, bc);
+                tma_store_4d(&tdq, sQ + kBox, 64, qrc, h, bc);
+                tma_store_commit();
+                tma_store_wait_read();  // the stage is read before this CTA's shared memory goes
+            }
         }
     }
 
@@ -1164,9 +1189,10 @@ cudaError_t launch_bwd_dkdv(const Prob &p, const BwdArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap_rows(&tq, p, true, a.q, p.Hq) || !make_tmap_rows(&tk, p, false, a.k, p.Hkv) ||
-        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq))
+        !make_tmap_rows(&tv, p, false, a.v, p.Hkv) || !make_tmap_rows(&tdo, p, true, a.dO, p.Hq) ||
+        !make_tmap_rows(&tdq, p, true, a.dq, p.Hq))
         return cudaErrorInvalidValue;
     dim3 grid(p.nQ * (p.tile_q / 128), p.Hq, p.B);
     const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_dq<__nv_bfloat16>, (int)kDqSmem)
@@ -1174,9 +1200,9 @@ cudaError_t launch_bwd_dq(const Prob &p, const BwdArgs &a, cudaStream_t s) {
     if (ae != cudaSuccess) return ae;
     prof_begin("bwd_dq", s);
     if (p.dtype == T_BF16)
-        k_dq<__nv_bfloat16><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__nv_bfloat16><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, tdq, p, a);
     else
-        k_dq<__half><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, p, a);
+        k_dq<__half><<<grid, kDqThreads, kDqSmem, s>>>(tq, tk, tv, tdo, tdq, p, a);
     prof_end(s);
     return cudaGetLastError();
 }

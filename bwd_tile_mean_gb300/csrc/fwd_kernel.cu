@@ -514,7 +514,8 @@ __device__ __forceinline__ void issue_pv2(uint32_t d, uint32_t p_tmem, uint32_t 
 template <typename T>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     k_fwd2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-           const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout, const Prob p,
+           const FwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
     const uint32_t rank = cluster_rank();
@@ -760,6 +761,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         T *out = reinterpret_cast<T *>(a.out) + ro;
         const T *gt = a.gate ? reinterpret_cast<const T *>(a.gate) + ro : nullptr;
         const float *cc = a.gate ? a.c + qrow * 128 + ch * 64 : nullptr;
+        // One output (no gate, O kept only as out), padded layout: the CTA's
+        // 128 rows of O are staged in its Q buffer (free once the last S MMA
+        // is done) in the TMA box layout and stored by two box copies.
+        const bool staged = p.layout != L_TND && !a.gate && (!a.o_sparse || a.o_sparse == a.out);
 #pragma unroll 1
         for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t o[32];
@@ -777,7 +782,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) w[j] = pack2<T>(vals[2 * j], vals[2 * j + 1]);
-            if (osp) {
+            if (osp && !staged) {
                 uint4 *dst = reinterpret_cast<uint4 *>(osp + q2 * 32);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
@@ -797,13 +802,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
                     }
                 }
             }
-            if (gt || out != osp) {
+            if (staged) {
+                // columns 64 ch + 32 q2 .. +31: box ch, 16-byte chunks 4 q2 .. +3 of row r, 128-byte swizzle
+                uint8_t *rowp = sQ + ch * (kF2Q / 2) + r * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(rowp + (((q2 * 4 + u) ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            } else if (gt || out != osp) {
                 uint4 *dst = reinterpret_cast<uint4 *>(out + q2 * 32);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             }
         }
         if (row_ok && ch == 0 && a.lse) a.lse[lse_off(p, b, h, row)] = lse_v;
+        if (staged) {
+            fence_proxy_async_smem();
+            named_sync(1, 256);  // the 8 softmax warps have staged their rows
+            if (warp == 0 && lane == 0 && !*s_abort) {
+                tma_store_4d(&tout, sQ, 0, qbase, h, bc);
+                tma_store_4d(&tout, sQ + kF2Q / 2, 64, qbase, h, bc);
+                tma_store_commit();
+                tma_store_wait_read();  // the stage is read before this CTA's shared memory goes
+            }
+        }
     }
 
     // ------------------------------------------------------------ teardown
@@ -852,8 +874,9 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     if (p.tile_q == 256 && !a.q_sub && a.redo) {
         // a CTA pair per 256-token query tile; the tiles it marks in redo
         // are then recomputed by the single-CTA kernel below
-        CUtensorMap tk2;
-        if (!make_tmap_rows(&tk2, p, false, a.k, p.Hkv, 64)) return cudaErrorInvalidValue;
+        CUtensorMap tk2, tout;
+        if (!make_tmap_rows(&tk2, p, false, a.k, p.Hkv, 64) || !make_tmap_rows(&tout, p, true, a.out, p.Hq))
+            return cudaErrorInvalidValue;
         dim3 grid2(2 * p.nQ, p.Hq, p.B);
         const cudaError_t ae = p.dtype == T_BF16
                                    ? ensure_smem_limit((const void *)k_fwd2<__nv_bfloat16>, (int)kF2Smem)
@@ -861,9 +884,9 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
         if (ae != cudaSuccess) return ae;
         prof_begin("fwd_attn", s);
         if (p.dtype == T_BF16)
-            k_fwd2<__nv_bfloat16><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, p, a1);
+            k_fwd2<__nv_bfloat16><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, p, a1);
         else
-            k_fwd2<__half><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, p, a1);
+            k_fwd2<__half><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, p, a1);
         prof_end(s);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
