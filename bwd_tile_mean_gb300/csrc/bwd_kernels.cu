@@ -771,6 +771,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         *s_abort = 0;
         fence_mbar_init();
     }
+    // The producer reads the selection before the CTA-wide sync: the chunk
+    // count and bits every role needs, and the first window of its own
+    // walk, so that Q, dO and the first K/V chunk are requested right after.
+    ChunkWin pcw{};
     if (warp == kProdWarp) {
         // number of 128-key chunks with valid keys (counts clamped to
         // idx_cap, tile ids outside [0, nKV) skipped, as in win_load)
@@ -797,6 +801,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             total += __shfl_sync(0xffffffffu, inc, 31);
         }
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
+        pcw = win_begin(p, b, idx, nullptr, cnt, lane);
     } else if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
@@ -811,7 +816,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (warp == kProdWarp && N > 0) {
         // ------------------------------------ TMA producer (whole warp, lane 0 issues)
-        ChunkWin cw = win_begin(p, b, a.q_idx + qrow * a.cap, nullptr, clampi(a.q_cnt[qrow], 0, a.cap), lane);
+        ChunkWin &cw = pcw;
         if (lane == 0) {
             mbar_expect_tx(b_q, 2 * kTile);
             tma_load_4d(sQ, &tq, b_q, 0, qrc, h, bc);
