@@ -453,6 +453,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         *s_nwork = n;
         fence_mbar_init();
     }
+    // the producer's first work item is looked up while thread 0 counts
+    WorkIter w{};
+    bool more = false;
+    if (warp == kProdWarp && lane == 0 && kvalid > 0) more = work_first(p, a, b, h0, h_end, j, w);
     if (warp == kMmaWarp) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
@@ -473,8 +477,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         tma_load_4d(sV, &tv, b_kv, 0, kvb + key0, hk, bc);
         tma_load_4d(sV + kBox, &tv, b_kv, 64, kvb + key0, hk, bc);
         issued_kv = 1;
-        WorkIter w;
-        bool more = work_first(p, a, b, h0, h_end, j, w);
         for (int m = 0; more && m < M; ++m) {
             const int st = m % kDkStages;
             if (m >= kDkStages && !mbar_wait(b_qe + st, ((m / kDkStages) - 1) & 1, s_abort, a.err, kSiteDkProd))
