@@ -619,39 +619,46 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const bool staged = p.layout != L_TND;
         uint8_t *stage = sQ + ch * 2 * kBox;  // [2 boxes of 64 dims][128 rows x 128 B]
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t o[32];
+        for (int q8 = 0; q8 < 2; ++q8) {
+            uint32_t o2[2][32];  // two quarters per TMEM round trip
             if (have) {
-                tmem_ld32(tl + 256 + ch * 128 + q4 * 32, o);
-                tmem_wait_ld();
+                tmem_ld32(tl + 256 + ch * 128 + q8 * 64, o2[0]);
+                tmem_ld32(tl + 256 + ch * 128 + q8 * 64 + 32, o2[1]);
+                tmem_wait_ld_regs(o2[0]);
+                tmem_wait_ld_regs(o2[1]);
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = 0u;
+                for (int e = 0; e < 32; ++e) o2[0][e] = o2[1][e] = 0u;
             }
             if (!row_ok) continue;
-            uint32_t wv[16];
 #pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-                float v0 = key_ok ? __uint_as_float(o[2 * e2]) * mul : 0.f;
-                float v1 = key_ok ? __uint_as_float(o[2 * e2 + 1]) * mul : 0.f;
-                if (cadd && key_ok) {
-                    v0 += cadd[q4 * 32 + 2 * e2] * inv;
-                    v1 += cadd[q4 * 32 + 2 * e2 + 1] * inv;
+            for (int hq = 0; hq < 2; ++hq) {
+                const int q4 = q8 * 2 + hq;
+                const uint32_t(&o)[32] = o2[hq];
+                uint32_t wv[16];
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    float v0 = key_ok ? __uint_as_float(o[2 * e2]) * mul : 0.f;
+                    float v1 = key_ok ? __uint_as_float(o[2 * e2 + 1]) * mul : 0.f;
+                    if (cadd && key_ok) {
+                        v0 += cadd[q4 * 32 + 2 * e2] * inv;
+                        v1 += cadd[q4 * 32 + 2 * e2 + 1] * inv;
+                    }
+                    wv[e2] = pack2<T>(v0, v1);
                 }
-                wv[e2] = pack2<T>(v0, v1);
-            }
-            if (staged) {
-                // dims q4*32 .. +31: box q4 / 2, 16-byte chunks 4 (q4 % 2) .. +3 of row u, 128-byte swizzle
-                uint8_t *rowp = stage + (q4 >> 1) * kBox + u * 128;
+                if (staged) {
+                    // dims q4*32 .. +31: box q4 / 2, 16-byte chunks 4 (q4 % 2) .. +3 of row u, 128-byte swizzle
+                    uint8_t *rowp = stage + (q4 >> 1) * kBox + u * 128;
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    *reinterpret_cast<uint4 *>(rowp + ((((q4 & 1) * 4 + t) ^ (u & 7)) << 4)) =
-                        make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
-            } else {
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
+                    for (int t = 0; t < 4; ++t)
+                        *reinterpret_cast<uint4 *>(rowp + ((((q4 & 1) * 4 + t) ^ (u & 7)) << 4)) =
+                            make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                } else {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + q4 * 32);
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                    for (int t = 0; t < 4; ++t)
+                        d4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
+                }
             }
         }
         if (staged) {
@@ -959,14 +966,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     }
                 }
                 if (valid < 64) {  // keys past the valid count: P = 0
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < 64; ++kk)
                         if (kk >= valid) sr[kk] = __float_as_uint(-INFINITY);
                 }
                 // P = 2^(S scale log2e - LSE log2e), dS = P (dP - Dvec), on pairs
                 const uint64_t sc2 = f32x2(sl2, sl2), nl2x = f32x2(nl2, nl2), nd2 = f32x2(ndv, ndv);
                 uint32_t dw[32];
-    #pragma unroll
+#pragma unroll
                 for (int t2 = 0; t2 < 32; ++t2) {
                     const float2 x = f32x2_split(
                         ffma_x2(f32x2(__uint_as_float(sr[2 * t2]), __uint_as_float(sr[2 * t2 + 1])), sc2, nl2x));
