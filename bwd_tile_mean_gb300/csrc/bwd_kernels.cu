@@ -12,7 +12,9 @@
 // rowsum(P dP) equals Dvec = rowsum(dO * O), computed once per query row
 // by k_bwd_prep. The KV-owned pass k_dkdv and the Q-owned pass k_dq each
 // recompute S and dP on the tensor core, so neither needs atomics and every
-// output element is written by exactly one CTA.
+// output element is written by exactly one CTA. In padded layouts both
+// write their rows through shared memory (the Q tiles, free by then) with
+// TMA box stores.
 #include <climits>
 #include <type_traits>
 

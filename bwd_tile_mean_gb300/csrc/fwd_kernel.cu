@@ -11,6 +11,11 @@
 // FastVideo test_vsa256_backward.py (gated compression composes
 // out = sparse_out + gate * compress_out without touching sparse_out).
 //
+// 256-token query tiles without query-block masks run on CTA pairs
+// (k_fwd2, further down); the single-CTA kernel k_fwd described here takes
+// 128-token tiles, tiles with query-block masks, and the tiles k_fwd2 hands
+// back for a recompute.
+//
 // One CTA computes one query tile: two groups of 128 rows (A and B; the
 // two halves of a 256-token video tile, or a single group for 128-token
 // tiles) of one head against the tile's selected KV tiles, cut into
@@ -476,7 +481,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // magnitude, so nothing is rescaled. A chunk whose row sum passes
 // SumLimit (an element that the 16-bit P cannot hold) marks the tile in
 // `redo`; the single-CTA kernel, which moves its reference, recomputes
-// exactly those tiles right after.
+// exactly those tiles right after. Each chunk's P is handed to the O += P V
+// issuer in two halves (keys 0..63, then 64..127), so the first four
+// K = 16 steps run while the softmax finishes the row. The epilogue stages
+// O in the Q buffer and writes it with TMA box stores when O is the only
+// output of a padded layout.
 // Warp roles (each CTA): warps 0-7 softmax (warp w: TMEM lanes 32 (w % 4),
 // chunks of parity w / 4, and in the epilogue O columns [64 (w / 4), +64)),
 // warp 8 loads, warp 9 owns TMEM and (even CTA) issues the S MMAs, warp 10
