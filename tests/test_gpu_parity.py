@@ -221,6 +221,27 @@ def test_forward_parity_varlen_mask(p):
     _fwd_check(p, t, plan, g, qi, qc)
 
 
+def test_forward_separate_o_sparse_without_gate():
+    """O as the only output goes out through shared memory and box stores; a
+    separate o_sparse buffer without a gate takes the per-thread stores for
+    both. The two must agree bit for bit, with each other and across runs,
+    and match the oracle."""
+    p = extra_cases()[1]  # BSHD, 256-token tiles, GQA, ragged and empty tiles
+    t = make_tensors(p)
+    plan, g = run_map(p, t)
+    out1, lse1, _ = plan.forward(g["q"], g["k"], g["v"])
+    out2 = torch.empty_like(g["q"])
+    osp2 = torch.empty_like(g["q"])
+    plan.forward(g["q"], g["k"], g["v"], out=out2, o_sparse=osp2)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert torch.equal(out1, out2) and torch.equal(out1, osp2)
+    _, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    rows = p.rows()
+    ro, _, _ = orc.forward_rows(p, t["q"], t["k"], t["v"], qi, qc, p.cap, rows=rows)
+    check_tol(f"{p.name} out", orc._scatter_rows(p, rows, ro), out1.double().cpu().numpy(), OUT_TOL)
+
+
 def test_forward_bhsd_equals_bshd_and_inference_equals_training():
     p = config(1)
     t = make_tensors(p)
