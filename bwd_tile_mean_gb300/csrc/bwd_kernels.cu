@@ -791,14 +791,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         // idx_cap, tile ids outside [0, nKV) skipped, as in win_load)
         // and, per chunk, whether it holds at most 64 valid keys (then its
         // MMAs run over the first 64 keys only)
-        const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);
         const int *idx = a.q_idx + qrow * a.cap;
+        // the row's first 32 entries are read without waiting for their
+        // count (a row holds idx_cap entries), so the two reads overlap
+        const int jfirst = lane < a.cap ? idx[lane] : -1;
+        const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);
         const int per = p.tile_kv >> 7;
         for (int x = lane; x < kMaxChunks / 32; x += 32) s_half[x] = 0u;
         __syncwarp();
         int total = 0;  // chunks of the entries before this group of 32
         for (int n0 = 0; n0 < cnt; n0 += 32) {
-            const int n = n0 + lane, j = n < cnt ? idx[n] : -1;
+            const int n = n0 + lane, j = n < cnt ? (n0 == 0 ? jfirst : idx[n]) : -1;
             const int kvv = (j >= 0 && j < p.nKV) ? kv_valid(p, b, j) : 0;
             const int nch = min(per, (kvv + 127) >> 7);
             int inc = nch;

@@ -561,6 +561,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     const int bc = (p.layout == L_TND ? 0 : b);
     const long long qrow = ((long long)b * p.Hq + h) * p.nQ + i;
     const int cnt = clampi(a.q_cnt[qrow], 0, a.cap);  // counts past idx_cap are invalid input
+    // the producer reads the row's first 32 entries without waiting for
+    // their count (a row holds idx_cap entries), so the two reads overlap
+    const int jfirst = (warp == kF2ProdWarp && lane < a.cap) ? a.q_idx[qrow * a.cap + lane] : -1;
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
@@ -593,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         const int per = p.tile_kv >> 7;
         int total = 0;
         for (int n = lane; n < cnt; n += 32) {
-            const int j = idx[n];
+            const int j = n < 32 ? jfirst : idx[n];
             total += (j >= 0 && j < p.nKV) ? min(per, (kv_valid(p, b, j) + 127) >> 7) : 0;
         }
 #pragma unroll
