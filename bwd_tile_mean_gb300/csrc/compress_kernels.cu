@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kCThreads) k_compress_fwd(Prob p, const float 
 // ------------------------------------------------------------ backward
 // dc_i = sum over the query rows of tile i of gate (*) dO (fp32, per dim).
 // Thread: 8 dims (one 16-byte load of each tensor), rows phase, phase + 8,
-// ...; the eight phases' partial sums are added in a fixed order.
+// ..., four rows' loads issued before their sums (taken in row order); the
+// eight phases' partial sums are added in a fixed order.
 template <typename T>
 __global__ void __launch_bounds__(128) k_compress_dc(Prob p, const T *__restrict__ dO, const T *__restrict__ gate,
                                                      float *__restrict__ dc) {
@@ -183,16 +184,26 @@ __global__ void __launch_bounds__(128) k_compress_dc(Prob p, const T *__restrict
     float acc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-    for (int r = phase; r < rows; r += 8) {
-        const long long o = tok_off(p, true, b, i * p.tile_q + r, h) + e0;
-        const uint4 gv = *reinterpret_cast<const uint4 *>(gate + o);
-        const uint4 dv = *reinterpret_cast<const uint4 *>(dO + o);
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    for (int r0 = phase; r0 < rows; r0 += 32) {
+        uint4 gv[4], dv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 g2 = unpack2<T>(gw[u]), d2 = unpack2<T>(dw[u]);
-            acc[2 * u] = fmaf(g2.x, d2.x, acc[2 * u]);
-            acc[2 * u + 1] = fmaf(g2.y, d2.y, acc[2 * u + 1]);
+        for (int k = 0; k < 4; ++k) {
+            if (r0 + 8 * k < rows) {
+                const long long o = tok_off(p, true, b, i * p.tile_q + r0 + 8 * k, h) + e0;
+                gv[k] = *reinterpret_cast<const uint4 *>(gate + o);
+                dv[k] = *reinterpret_cast<const uint4 *>(dO + o);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (r0 + 8 * k >= rows) break;
+            const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w}, dw[4] = {dv[k].x, dv[k].y, dv[k].z, dv[k].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 g2 = unpack2<T>(gw[u]), d2 = unpack2<T>(dw[u]);
+                acc[2 * u] = fmaf(g2.x, d2.x, acc[2 * u]);
+                acc[2 * u + 1] = fmaf(g2.y, d2.y, acc[2 * u + 1]);
+            }
         }
     }
 #pragma unroll

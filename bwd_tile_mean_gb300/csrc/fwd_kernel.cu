@@ -117,17 +117,16 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[128], float m, flo
     return (s0.x + s0.y) + (s1.x + s1.y);
 }
 
+constexpr int kRedoGroup = 16;  // query tiles of one head per CTA of the redo launch
+constexpr int kFwdBars = 16;
+
+// One query tile (i, h, b) with the CTA's TMEM columns at *s_tmem (512 of
+// them, allocated by the kernel); its barriers are initialised here and
+// invalidated on the way out, so the next tile of the same CTA starts from
+// fresh ones.
 template <typename T>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-    k_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-          const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *sm = smem_raw;
-    if (a.redo_only && !a.redo[((long long)blockIdx.z * p.Hq + blockIdx.y) * p.nQ + blockIdx.x]) return;
-    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
-        if (threadIdx.x == 0) set_error(a.err, 0x1FF);
-        return;
-    }
+__device__ __forceinline__ void fwd_tile(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                         const Prob &p, const FwdArgs &a, uint8_t *sm, int i, int h, int b) {
     uint8_t *sQ = sm + kOffQ, *sK = sm + kOffK, *sV = sm + kOffV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffCtl);
     uint64_t *b_q = bars + 0, *b_kf = bars + 1, *b_vf = bars + 3, *b_ke = bars + 5, *b_sf = bars + 7;
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int *s_csub = reinterpret_cast<int *>(s_cval + kMaxChunks);  // query-block bits of each chunk's tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    const int hk = h / (p.Hq / p.Hkv);
     // rows of each 128-row group (0 if the group does not exist)
     int nrows[2];
     for (int g = 0; g < 2; ++g) {
@@ -209,9 +208,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             total += __shfl_sync(0xffffffffu, inc, 31);
         }
         if (lane == 0) *s_nchunk = min(total, kMaxChunks);
-    } else if (warp == kFwdMmaWarp) {
-        tmem_alloc(s_tmem, 512);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -457,10 +453,49 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         __all_sync(0xffffffffu, mbar_wait(b_fin, 0, &never, nullptr, 0, 200000000ull));
     }
     tc_fence_before();
+    __syncthreads();  // every wait on this tile's barriers is over
+    if (threadIdx.x == 0)
+        for (int x = 0; x < kFwdBars; ++x) mbar_inval(bars + x);
+}
+
+// One tile per CTA; in the redo launch (redo_only) a CTA takes kRedoGroup
+// consecutive query tiles of one head and computes those marked in redo,
+// one after the other (a CTA none of whose tiles is marked leaves at once,
+// so the launch costs little when nothing is marked).
+template <typename T>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    k_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+          const __grid_constant__ CUtensorMap tv, const Prob p, const FwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const long long row0 = ((long long)b * p.Hq + h) * p.nQ;
+    const int i0 = a.redo_only ? (int)blockIdx.x * kRedoGroup : (int)blockIdx.x;
+    const int ntiles = a.redo_only ? min(kRedoGroup, p.nQ - i0) : 1;
+    if (a.redo_only) {
+        bool any = false;
+        for (int x = 0; x < ntiles; ++x) any = any || a.redo[row0 + i0 + x] != 0;
+        if (!any) return;
+    }
+    if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_error(a.err, 0x1FF);
+        return;
+    }
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffCtl + kFwdBars * 8);
+    const int warp = threadIdx.x >> 5;
+    if (warp == kFwdMmaWarp) {
+        tmem_alloc(s_tmem, 512);
+        tmem_relinquish();
+    }
+    for (int x = 0; x < ntiles; ++x) {
+        if (a.redo_only && !a.redo[row0 + i0 + x]) continue;
+        fwd_tile<T>(tq, tk, tv, p, a, sm, i0 + x, h, b);
+    }
+    tc_fence_before();
     __syncthreads();
     if (warp == kFwdMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tbase, 512);
+        tmem_dealloc(*s_tmem, 512);
     }
 }
 
@@ -483,9 +518,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // `redo`; the single-CTA kernel, which moves its reference, recomputes
 // exactly those tiles right after. Each chunk's P is handed to the O += P V
 // issuer in two halves (keys 0..63, then 64..127), so the first four
-// K = 16 steps run while the softmax finishes the row. The epilogue stages
-// O in the Q buffer and writes it with TMA box stores when O is the only
-// output of a padded layout.
+// K = 16 steps run while the softmax finishes the row. In padded layouts
+// the epilogue stages its rows in shared memory in the TMA box layout and
+// writes them with box stores when O is the only output, or when gated:
+// out in the Q buffer and O (the sparse output) in the first two K stages.
+// The gated instantiation (kGated) copies the gate's rows into the Q
+// buffer as soon as the last S MMA has read Q, while the last chunks'
+// softmax and O += P V still run, and its epilogue turns them into
+// out = O + gate * c in place; the ungated one has none of this code.
 // Warp roles (each CTA): warps 0-7 softmax (warp w: TMEM lanes 32 (w % 4),
 // chunks of parity w / 4, and in the epilogue O columns [64 (w / 4), +64)),
 // warp 8 loads, warp 9 owns TMEM and (even CTA) issues the S MMAs, warp 10
@@ -520,10 +560,11 @@ __device__ __forceinline__ void issue_pv2(uint32_t d, uint32_t p_tmem, uint32_t 
         mma2_ts_w(d, p_tmem + kk * 8, sdesc_sw128(aV + kk * 2048, kF2VH, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-template <typename T>
+template <typename T, bool kGated>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     k_fwd2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout, const Prob p,
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout,
+           const __grid_constant__ CUtensorMap tgate, const __grid_constant__ CUtensorMap tosp, const Prob p,
            const FwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
@@ -548,7 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
     uint64_t *b_p = b_s + 3, *b_o = b_p + 3, *b_fin = b_o + 1, *b_mref = b_fin + 2;
     uint64_t *b_pvd = b_mref + 1;  // (even CTA) O += P V of buffer x's chunk done: x may take S again
     uint64_t *b_plo = b_pvd + 3;   // (even CTA) P of buffer x's first 64 keys stored, in both CTAs
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 29 barriers (232 bytes)
+    uint64_t *b_qd = b_plo + 3;    // the last S MMA has read Q (both CTAs)
+    uint64_t *b_g = b_qd + 1;      // this CTA's gate rows have landed in the Q buffer
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kF2OffCtl + 256);  // after 31 barriers (248 bytes)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     int *s_nchunk = reinterpret_cast<int *>(s_tmem + 2);
     volatile int *s_over = reinterpret_cast<volatile int *>(s_tmem + 3);       // a chunk passed SumLimit here
@@ -581,6 +624,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         mbar_init(b_mref, 4);  // the four warps that take chunk 0
         for (int x = 0; x < 3; ++x) mbar_init(b_pvd + x, 1);
         for (int x = 0; x < 3; ++x) mbar_init(b_plo + x, 8);  // as b_p
+        if constexpr (kGated) {
+            mbar_init(b_qd, 1);
+            mbar_init(b_g, 1);
+        }
         *s_abort = 0;
         *s_over = 0;
         *s_over_peer = 0;
@@ -647,6 +694,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             }
             issued_kv = c + 1;
         }
+        if constexpr (kGated) {
+            // the gate's rows into the Q buffer once the last S MMA has read it
+            if (p.layout != L_TND && lane == 0 && issued_kv == N && mbar_wait(b_qd, 0, s_abort, a.err, kSite2Prod)) {
+                tma_prefetch_desc(&tgate);
+                mbar_expect_tx(b_g, kF2Q);
+                tma_load_4d(sQ, &tgate, b_g, 0, qbase, h, bc);
+                tma_load_4d(sQ + kF2Q / 2, &tgate, b_g, 64, qbase, h, bc);
+            }
+        }
     } else if (warp == kF2MmaWarp && leader && N > 0) {
         // --------------------------- S issuer of the pair (whole warp, one lane issues)
         // S(c) goes into buffer c % 3 once K(c) has landed and O += P V has
@@ -662,6 +718,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             issue_qk2(tbase + x * 128, aQ, aK + st * kF2KH, idS);
             mma2_commit_mc_w(b_s + x, 3);
             mma_started = 1;
+        }
+        if constexpr (kGated) {
+            if (ok && p.layout != L_TND) mma2_commit_mc_w(b_qd, 3);  // Q read by every S MMA, in both CTAs
         }
     } else if (warp == kF2PvWarp && leader && N > 0) {
         // ------------------------ PV issuer of the pair (whole warp, one lane issues)
@@ -756,6 +815,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
             ok = mbar_wait_warp(b_o, 0, s_abort, a.err, kSite2Epi);
             if (ok) tc_fence_after();
         }
+        // gated padded layouts: the gate's rows come by TMA once Q is no
+        // longer read (with no chunk no MMA runs and the gate is read directly)
+        const bool gate_tma = kGated && p.layout != L_TND && N > 0;
+        if (ok && gate_tma) ok = mbar_wait_warp(b_g, 0, s_abort, a.err, kSite2Epi);
         // the row sum: both warps' parts (every softmax warp comes here once)
         s_lsum[grp * 128 + r] = l;
         named_sync(1, 256);
@@ -777,33 +840,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
         // 128 rows of O are staged in its Q buffer (free once the last S MMA
         // is done) in the TMA box layout and stored by two box copies.
         const bool staged = p.layout != L_TND && !a.gate && (!a.o_sparse || a.o_sparse == a.out);
+        // Gated, padded layout: out = O + gate (*) c is staged in the Q
+        // buffer (where the gate's rows are), O in the first two K stages
+        // (free once O is complete), both in the TMA box layout.
+        const bool gstaged = kGated && p.layout != L_TND;
+        if constexpr (kGated) {
 #pragma unroll 1
-        for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t o[32];
-            if (have) {
-                tmem_ld32(tl + 384 + ch * 64 + q2 * 32, o);
-                tmem_wait_ld();
-            } else {
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld32(tl + 384 + ch * 64 + q2 * 32, o);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = 0u;
-            }
-            if (!row_ok) continue;
-            float vals[32];
+                    for (int j = 0; j < 32; ++j) o[j] = 0u;
+                }
+                if (!row_ok) continue;
+                float vals[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(o[j]) * inv_l;
-            uint32_t w[16];
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(o[j]) * inv_l;
+                uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = pack2<T>(vals[2 * j], vals[2 * j + 1]);
-            if (osp && !staged) {
-                uint4 *dst = reinterpret_cast<uint4 *>(osp + q2 * 32);
+                for (int j = 0; j < 16; ++j) w[j] = pack2<T>(vals[2 * j], vals[2 * j + 1]);
+                // columns 64 ch + 32 q2 .. +31: box ch, 16-byte chunks 4 q2 .. +3 of row r, 128-byte swizzle
+                uint8_t *rq = sQ + ch * (kF2Q / 2) + r * 128, *rk = sK + ch * (kF2Q / 2) + r * 128;
+                if (gstaged && osp) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            }
-            if (gt) {
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4 *>(rk + (((q2 * 4 + u) ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+                if (osp && !gstaged) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(osp + q2 * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
                 const uint4 *gsrc = reinterpret_cast<const uint4 *>(gt + q2 * 32);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const uint4 gv = gsrc[u];
+                    const uint4 gv = gate_tma ? *reinterpret_cast<const uint4 *>(rq + (((q2 * 4 + u) ^ (r & 7)) << 4))
+                                              : gsrc[u];
                     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
@@ -813,27 +890,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF2Threads, 1)
                                                 vals[u * 8 + t * 2 + 1] + g2.y * cc[e + 1]);
                     }
                 }
+                if (gstaged) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4 *>(rq + (((q2 * 4 + u) ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + q2 * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
             }
-            if (staged) {
-                // columns 64 ch + 32 q2 .. +31: box ch, 16-byte chunks 4 q2 .. +3 of row r, 128-byte swizzle
-                uint8_t *rowp = sQ + ch * (kF2Q / 2) + r * 128;
+        } else {
+#pragma unroll 1
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld32(tl + 384 + ch * 64 + q2 * 32, o);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4 *>(rowp + (((q2 * 4 + u) ^ (r & 7)) << 4)) =
-                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            } else if (gt || out != osp) {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + q2 * 32);
+                    for (int j = 0; j < 32; ++j) o[j] = 0u;
+                }
+                if (!row_ok) continue;
+                float vals[32];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(o[j]) * inv_l;
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w[j] = pack2<T>(vals[2 * j], vals[2 * j + 1]);
+                if (osp && !staged) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(osp + q2 * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+                if (gt) {
+                    const uint4 *gsrc = reinterpret_cast<const uint4 *>(gt + q2 * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 gv = gsrc[u];
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 g2 = unpack2<T>(gw[t]);
+                            const int e = q2 * 32 + u * 8 + t * 2;
+                            w[u * 4 + t] = pack2<T>(vals[u * 8 + t * 2] + g2.x * cc[e],
+                                                    vals[u * 8 + t * 2 + 1] + g2.y * cc[e + 1]);
+                        }
+                    }
+                }
+                if (staged) {
+                    // columns 64 ch + 32 q2 .. +31: box ch, 16-byte chunks 4 q2 .. +3 of row r, 128-byte swizzle
+                    uint8_t *rowp = sQ + ch * (kF2Q / 2) + r * 128;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4 *>(rowp + (((q2 * 4 + u) ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                } else if (gt || out != osp) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + q2 * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
             }
         }
         if (row_ok && ch == 0 && a.lse) a.lse[lse_off(p, b, h, row)] = lse_v;
-        if (staged) {
+        if (gstaged || staged) {
             fence_proxy_async_smem();
             named_sync(1, 256);  // the 8 softmax warps have staged their rows
             if (warp == 0 && lane == 0 && !*s_abort) {
                 tma_store_4d(&tout, sQ, 0, qbase, h, bc);
                 tma_store_4d(&tout, sQ + kF2Q / 2, 64, qbase, h, bc);
+                if (gstaged && a.o_sparse && a.o_sparse != a.out) {
+                    tma_store_4d(&tosp, sK, 0, qbase, h, bc);
+                    tma_store_4d(&tosp, sK + kF2Q / 2, 64, qbase, h, bc);
+                }
                 tma_store_commit();
                 tma_store_wait_read();  // the stage is read before this CTA's shared memory goes
             }
@@ -886,25 +1017,41 @@ cudaError_t launch_fwd(const Prob &p, const FwdArgs &a, cudaStream_t s) {
     if (p.tile_q == 256 && !a.q_sub && a.redo) {
         // a CTA pair per 256-token query tile; the tiles it marks in redo
         // are then recomputed by the single-CTA kernel below
-        CUtensorMap tk2, tout;
+        CUtensorMap tk2, tout, tgate, tosp;
         if (!make_tmap_rows(&tk2, p, false, a.k, p.Hkv, 64) || !make_tmap_rows(&tout, p, true, a.out, p.Hq))
             return cudaErrorInvalidValue;
+        tgate = tout;  // read only when gated
+        tosp = tout;   // written only when O is a separate tensor
+        if ((a.gate && !make_tmap_rows(&tgate, p, true, a.gate, p.Hq)) ||
+            (a.o_sparse && a.o_sparse != a.out && !make_tmap_rows(&tosp, p, true, a.o_sparse, p.Hq)))
+            return cudaErrorInvalidValue;
         dim3 grid2(2 * p.nQ, p.Hq, p.B);
-        const cudaError_t ae = p.dtype == T_BF16
-                                   ? ensure_smem_limit((const void *)k_fwd2<__nv_bfloat16>, (int)kF2Smem)
-                                   : ensure_smem_limit((const void *)k_fwd2<__half>, (int)kF2Smem);
+        // the gated instantiation adds the gate's copy and the staged sum;
+        // the other one compiles without any of it
+        const void *kern = p.dtype == T_BF16 ? (a.gate ? (const void *)k_fwd2<__nv_bfloat16, true>
+                                                       : (const void *)k_fwd2<__nv_bfloat16, false>)
+                                             : (a.gate ? (const void *)k_fwd2<__half, true>
+                                                       : (const void *)k_fwd2<__half, false>);
+        const cudaError_t ae = ensure_smem_limit(kern, (int)kF2Smem);
         if (ae != cudaSuccess) return ae;
         prof_begin("fwd_attn", s);
-        if (p.dtype == T_BF16)
-            k_fwd2<__nv_bfloat16><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, p, a1);
-        else
-            k_fwd2<__half><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, p, a1);
+        if (p.dtype == T_BF16) {
+            if (a.gate)
+                k_fwd2<__nv_bfloat16, true><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, tgate, tosp, p, a1);
+            else
+                k_fwd2<__nv_bfloat16, false><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, tgate, tosp, p, a1);
+        } else {
+            if (a.gate)
+                k_fwd2<__half, true><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, tgate, tosp, p, a1);
+            else
+                k_fwd2<__half, false><<<grid2, kF2Threads, kF2Smem, s>>>(tq, tk2, tv, tout, tgate, tosp, p, a1);
+        }
         prof_end(s);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         a1.redo_only = 1;
     }
-    dim3 grid(p.nQ, p.Hq, p.B);
+    dim3 grid(a1.redo_only ? (p.nQ + kRedoGroup - 1) / kRedoGroup : p.nQ, p.Hq, p.B);
     const cudaError_t ae = p.dtype == T_BF16 ? ensure_smem_limit((const void *)k_fwd<__nv_bfloat16>, (int)kFwdSmem)
                                              : ensure_smem_limit((const void *)k_fwd<__half>, (int)kFwdSmem);
     if (ae != cudaSuccess) return ae;

@@ -242,6 +242,32 @@ def test_forward_separate_o_sparse_without_gate():
     check_tol(f"{p.name} out", orc._scatter_rows(p, rows, ro), out1.double().cpu().numpy(), OUT_TOL)
 
 
+def test_gated_tiles_without_chunks():
+    """Gated padded layout from an explicit block mask in which some query
+    tiles select nothing, or only a tile without valid keys: their out is
+    gate (*) c alone, with the gate read directly (no chunk ran), next to
+    tiles whose gate rows are copied in once their last S MMA is done. Out,
+    o_sparse and the gradients match the oracle."""
+    p = Problem("gated-mask-no-chunks", "bshd", 1, 4, 2, 128, 256, 256, 4, 5, q_var=[256, 256, 200, 256],
+                kv_var=[256, 173, 0, 79, 256], gate="randn01", seed=61)
+    t = make_tensors(p)
+    m = (np.random.default_rng(61).random((p.B, p.Hq, p.nQ, p.nKV)) < 0.6).astype(np.uint8)
+    m[0, 0, 1, :] = 0      # nothing selected
+    m[0, 1, 0, :] = 0
+    m[0, 1, 0, 2] = 1      # only the tile without valid keys
+    m[0, 2, 3, :] = 1      # everything
+    plan = plan_for(p)
+    g = to_device(t)
+    plan.mask_to_index(torch.as_tensor(m).cuda(), need_bwd_index=True)
+    ref = orc.run_full(p, t, mask=m)
+    assert ref["q_cnt"][0, 0, 1] == 0 and ref["q_cnt"][0, 1, 0] == 0
+    dq, dk, dv = _bwd_check(p, t, plan, g, ref)
+    out, lse, osp = plan.forward(g["q"], g["k"], g["v"], gate=g["gate"])
+    torch.cuda.synchronize()
+    check_tol(f"{p.name} o_sparse", ref["o_sparse"], osp.double().cpu().numpy(), OUT_TOL)
+    assert torch.all(osp[0, 256:512, 0] == 0) and torch.all(osp[0, 0:256, 1] == 0)
+
+
 def test_forward_bhsd_equals_bshd_and_inference_equals_training():
     p = config(1)
     t = make_tensors(p)
