@@ -29,9 +29,47 @@ namespace {
 
 constexpr int kCQ = 16;        // query tiles per CTA (row passes), at most
 constexpr int kCJ = 32;        // key/value tiles per staged chunk
-constexpr int kCPitch = 129;   // floats per staged row
+constexpr int kCPitch = 132;   // floats per staged row (16-byte aligned; 8 lanes' 16-byte reads hit distinct banks)
 constexpr int kCJB = 16;       // key/value tiles per CTA (column pass)
 constexpr int kCThreads = 256;
+
+// Floats per row of the [query tile][key/value tile] score and A / ds
+// rows held in shared memory: nKV rounded up to a multiple of 4, so that
+// four consecutive tiles' values are one 16-byte read.
+__host__ __device__ __forceinline__ int nkv_pitch(const Prob &p) { return (p.nKV + 3) & ~3; }
+__device__ __forceinline__ float4 ld4(const float *x) { return *reinterpret_cast<const float4 *>(x); }
+// a (+)= x . y over 4 consecutive dims, in dim order
+__device__ __forceinline__ float dot4(float4 x, float4 y, float a) {
+    a = fmaf(x.x, y.x, a);
+    a = fmaf(x.y, y.y, a);
+    a = fmaf(x.z, y.z, a);
+    return fmaf(x.w, y.w, a);
+}
+// acc[u] += sum over jj of sS[(q0 + u) pitch + j0 + jj] st[jj][d], jj in
+// ascending order (rows q0 + u < nq); four jj per 16-byte read of sS.
+__device__ __forceinline__ void acc_staged(float (&acc)[8], const float *sS, int pitch, int j0, int nj,
+                                           const float *st, int d, int q0, int nq) {
+    int jj = 0;
+    for (; jj + 4 <= nj; jj += 4) {
+        const float v0 = st[jj * kCPitch + d], v1 = st[(jj + 1) * kCPitch + d];
+        const float v2 = st[(jj + 2) * kCPitch + d], v3 = st[(jj + 3) * kCPitch + d];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (q0 + u < nq) {
+                const float4 a = ld4(sS + (q0 + u) * pitch + j0 + jj);
+                acc[u] = fmaf(a.x, v0, acc[u]);
+                acc[u] = fmaf(a.y, v1, acc[u]);
+                acc[u] = fmaf(a.z, v2, acc[u]);
+                acc[u] = fmaf(a.w, v3, acc[u]);
+            }
+    }
+    for (; jj < nj; ++jj) {
+        const float v = st[jj * kCPitch + d];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (q0 + u < nq) acc[u] = fmaf(sS[(q0 + u) * pitch + j0 + jj], v, acc[u]);
+    }
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -44,29 +82,28 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Stage rows [j0, j0 + nj) of a [nKV, 128] fp32 matrix into st[kCJ][kCPitch]:
-// each thread issues its four 16-byte loads before storing any, so the L2
-// round trips overlap.
+// Rows [j0, j0 + nj) of a [nKV, 128] fp32 matrix, staged through shared
+// memory as st[kCJ][kCPitch] in two steps: chunk_load issues a thread's
+// four 16-byte loads into registers, chunk_store writes them. The passes
+// below load chunk n + 1 right after storing chunk n, so its L2 round trip
+// overlaps the arithmetic on chunk n.
 static_assert(kCJ * 32 == 4 * kCThreads, "a chunk is four 16-byte loads per thread");
-__device__ __forceinline__ void stage_chunk(float *st, const float *__restrict__ src, int j0, int nj) {
+__device__ __forceinline__ int chunk_rows(int nKV, int j0) { return j0 < nKV ? min(kCJ, nKV - j0) : 0; }
+__device__ __forceinline__ void chunk_load(float4 (&v)[4], const float *__restrict__ src, int j0, int nj) {
     const float4 *s4 = reinterpret_cast<const float4 *>(src + (long long)j0 * 128);
     const int n4 = nj * 32;
-    float4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int x = threadIdx.x + k * kCThreads;
         v[k] = x < n4 ? s4[x] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+}
+__device__ __forceinline__ void chunk_store(float *st, const float4 (&v)[4], int nj) {
+    const int n4 = nj * 32;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int x = threadIdx.x + k * kCThreads;
-        if (x < n4) {
-            float *d = st + (x >> 5) * kCPitch + (x & 31) * 4;
-            d[0] = v[k].x;
-            d[1] = v[k].y;
-            d[2] = v[k].z;
-            d[3] = v[k].w;
-        }
+        if (x < n4) *reinterpret_cast<float4 *>(st + (x >> 5) * kCPitch + (x & 31) * 4) = v[k];
     }
 }
 // Copy n floats (a multiple of 4; both sides 16-byte aligned) into shared
@@ -116,37 +153,42 @@ __global__ void __launch_bounds__(kCThreads) k_compress_fwd(Prob p, const float 
     extern __shared__ __align__(16) float sm[];
     float *sq = sm;                      // [kCQ][128] this CTA's query means
     float *st = sq + kCQ * 128;          // [kCJ][kCPitch] staged pk, then pv
-    float *sA = st + kCJ * kCPitch;      // [qb][nKV] scores, then A
+    float *sA = st + kCJ * kCPitch;      // [qb][nkv_pitch] scores, then A
     const int h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
+    const int pa = nkv_pitch(p);
     const int i0 = blockIdx.x * qb, nq = min(qb, p.nQ - i0);
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const long long row0 = ((long long)b * p.Hq + h) * p.nQ + i0;
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
     const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    float4 pf[4];
+    chunk_load(pf, pkh, 0, chunk_rows(p.nKV, 0));
     load_rows(sq, pq + row0 * 128, nq * 128);
     // scores: thread (tile j0 + lane, rows w and w + 8; a row past nq is
     // computed from whatever sq holds there and not stored)
     for (int j0 = 0; j0 < p.nKV; j0 += kCJ) {
         const int nj = min(kCJ, p.nKV - j0);
         __syncthreads();
-        stage_chunk(st, pkh, j0, nj);
+        chunk_store(st, pf, nj);
         __syncthreads();
+        if (j0 + kCJ < p.nKV) chunk_load(pf, pkh, j0 + kCJ, chunk_rows(p.nKV, j0 + kCJ));
+        else chunk_load(pf, pvh, 0, chunk_rows(p.nKV, 0));  // the c pass's first chunk
         if (lane < nj && w < nq) {
             const bool valid = kv_valid(p, b, j0 + lane) > 0;
             const int w2 = min(w + 8, kCQ - 1);
             float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < 128; ++d) {
-                const float kd = st[lane * kCPitch + d];
-                a0 = fmaf(sq[w * 128 + d], kd, a0);
-                a1 = fmaf(sq[w2 * 128 + d], kd, a1);
+#pragma unroll 4
+            for (int d = 0; d < 128; d += 4) {
+                const float4 kd = ld4(st + lane * kCPitch + d);
+                a0 = dot4(ld4(sq + w * 128 + d), kd, a0);
+                a1 = dot4(ld4(sq + w2 * 128 + d), kd, a1);
             }
-            sA[w * p.nKV + j0 + lane] = valid ? a0 * p.scale : -INFINITY;
-            if (w + 8 < nq) sA[(w + 8) * p.nKV + j0 + lane] = valid ? a1 * p.scale : -INFINITY;
+            sA[w * pa + j0 + lane] = valid ? a0 * p.scale : -INFINITY;
+            if (w + 8 < nq) sA[(w + 8) * pa + j0 + lane] = valid ? a1 * p.scale : -INFINITY;
         }
     }
     __syncthreads();
-    for (int q = w; q < nq; q += 8) softmax_row(sA + q * p.nKV, p.nKV, lane);
+    for (int q = w; q < nq; q += 8) softmax_row(sA + q * pa, p.nKV, lane);
     // c = A pv: thread (dim t % 128, rows 8 (t / 128) .. + 8)
     const int d = t & 127, q0 = (t >> 7) * 8;
     float acc[8];
@@ -155,14 +197,10 @@ __global__ void __launch_bounds__(kCThreads) k_compress_fwd(Prob p, const float 
     for (int j0 = 0; j0 < p.nKV; j0 += kCJ) {
         const int nj = min(kCJ, p.nKV - j0);
         __syncthreads();
-        stage_chunk(st, pvh, j0, nj);
+        chunk_store(st, pf, nj);
         __syncthreads();
-        for (int jj = 0; jj < nj; ++jj) {
-            const float v = st[jj * kCPitch + d];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (q0 + u < nq) acc[u] = fmaf(sA[(q0 + u) * p.nKV + j0 + jj], v, acc[u]);
-        }
+        if (j0 + kCJ < p.nKV) chunk_load(pf, pvh, j0 + kCJ, chunk_rows(p.nKV, j0 + kCJ));
+        acc_staged(acc, sA, pa, j0, nj, st, d, q0, nq);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -227,45 +265,53 @@ __global__ void __launch_bounds__(kCThreads) k_compress_rows(Prob p, const float
     float *sc = sq + kCQ * 128;          // [kCQ][128] dc rows
     float *sk = sc + kCQ * 128;          // [kCJ][kCPitch] staged pk
     float *sv = sk + kCJ * kCPitch;      // [kCJ][kCPitch] staged pv
-    float *sA = sv + kCJ * kCPitch;      // [qb][nKV] scores, then A
-    float *sD = sA + qb * p.nKV;         // [qb][nKV] dA, then ds
+    const int pa = nkv_pitch(p);
+    float *sA = sv + kCJ * kCPitch;      // [qb][pa] scores, then A
+    float *sD = sA + qb * pa;            // [qb][pa] dA, then ds
     const int h = blockIdx.y, b = blockIdx.z, hk = h / (p.Hq / p.Hkv);
     const int i0 = blockIdx.x * qb, nq = min(qb, p.nQ - i0);
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const long long row0 = ((long long)b * p.Hq + h) * p.nQ + i0;
     const float *pkh = pk + ((long long)b * p.Hkv + hk) * p.nKV * 128;
     const float *pvh = pv + ((long long)b * p.Hkv + hk) * p.nKV * 128;
+    float4 fk[4], fv[4];
+    chunk_load(fk, pkh, 0, chunk_rows(p.nKV, 0));
+    chunk_load(fv, pvh, 0, chunk_rows(p.nKV, 0));
     load_rows(sq, pq + row0 * 128, nq * 128);
     load_rows(sc, dc + row0 * 128, nq * 128);
     for (int j0 = 0; j0 < p.nKV; j0 += kCJ) {
         const int nj = min(kCJ, p.nKV - j0);
         __syncthreads();
-        stage_chunk(sk, pkh, j0, nj);
-        stage_chunk(sv, pvh, j0, nj);
+        chunk_store(sk, fk, nj);
+        chunk_store(sv, fv, nj);
         __syncthreads();
+        // the next chunk (after the last one: the dpq pass's first pk chunk)
+        const int jn = j0 + kCJ < p.nKV ? j0 + kCJ : 0;
+        chunk_load(fk, pkh, jn, chunk_rows(p.nKV, jn));
+        if (j0 + kCJ < p.nKV) chunk_load(fv, pvh, jn, chunk_rows(p.nKV, jn));
         if (lane < nj && w < nq) {
             const bool valid = kv_valid(p, b, j0 + lane) > 0;
             const int w2 = min(w + 8, kCQ - 1);
             float s0 = 0.f, s1 = 0.f, d0 = 0.f, d1 = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < 128; ++d) {
-                const float kd = sk[lane * kCPitch + d], vd = sv[lane * kCPitch + d];
-                s0 = fmaf(sq[w * 128 + d], kd, s0);
-                s1 = fmaf(sq[w2 * 128 + d], kd, s1);
-                d0 = fmaf(sc[w * 128 + d], vd, d0);
-                d1 = fmaf(sc[w2 * 128 + d], vd, d1);
+#pragma unroll 2
+            for (int d = 0; d < 128; d += 4) {
+                const float4 kd = ld4(sk + lane * kCPitch + d), vd = ld4(sv + lane * kCPitch + d);
+                s0 = dot4(ld4(sq + w * 128 + d), kd, s0);
+                s1 = dot4(ld4(sq + w2 * 128 + d), kd, s1);
+                d0 = dot4(ld4(sc + w * 128 + d), vd, d0);
+                d1 = dot4(ld4(sc + w2 * 128 + d), vd, d1);
             }
-            sA[w * p.nKV + j0 + lane] = valid ? s0 * p.scale : -INFINITY;
-            sD[w * p.nKV + j0 + lane] = valid ? d0 : 0.f;
+            sA[w * pa + j0 + lane] = valid ? s0 * p.scale : -INFINITY;
+            sD[w * pa + j0 + lane] = valid ? d0 : 0.f;
             if (w + 8 < nq) {
-                sA[(w + 8) * p.nKV + j0 + lane] = valid ? s1 * p.scale : -INFINITY;
-                sD[(w + 8) * p.nKV + j0 + lane] = valid ? d1 : 0.f;
+                sA[(w + 8) * pa + j0 + lane] = valid ? s1 * p.scale : -INFINITY;
+                sD[(w + 8) * pa + j0 + lane] = valid ? d1 : 0.f;
             }
         }
     }
     __syncthreads();
     for (int q = w; q < nq; q += 8) {
-        float *ra = sA + q * p.nKV, *rd = sD + q * p.nKV;
+        float *ra = sA + q * pa, *rd = sD + q * pa;
         softmax_row(ra, p.nKV, lane);
         float sad = 0.f;
         for (int j = lane; j < p.nKV; j += 32) sad += ra[j] * rd[j];
@@ -286,14 +332,10 @@ __global__ void __launch_bounds__(kCThreads) k_compress_rows(Prob p, const float
     for (int j0 = 0; j0 < p.nKV; j0 += kCJ) {
         const int nj = min(kCJ, p.nKV - j0);
         __syncthreads();
-        stage_chunk(sk, pkh, j0, nj);
+        chunk_store(sk, fk, nj);
         __syncthreads();
-        for (int jj = 0; jj < nj; ++jj) {
-            const float kv = sk[jj * kCPitch + d];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (q0 + u < nq) acc[u] = fmaf(sD[(q0 + u) * p.nKV + j0 + jj], kv, acc[u]);
-        }
+        if (j0 + kCJ < p.nKV) chunk_load(fk, pkh, j0 + kCJ, chunk_rows(p.nKV, j0 + kCJ));
+        acc_staged(acc, sD, pa, j0, nj, sk, d, q0, nq);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -359,7 +401,7 @@ constexpr int kCSmemCap = 200 * 1024;
 // chunks in 200 KB of shared memory; 0 when not even one fits.
 int rows_per_cta(const Prob &p, int fixed_floats, int rows_per_q) {
     for (int qb = kCQ; qb >= 1; qb /= 2)
-        if ((size_t)(fixed_floats + (size_t)qb * rows_per_q * p.nKV) * 4 <= (size_t)kCSmemCap) return qb;
+        if ((size_t)(fixed_floats + (size_t)qb * rows_per_q * nkv_pitch(p)) * 4 <= (size_t)kCSmemCap) return qb;
     return 0;
 }
 
@@ -371,7 +413,7 @@ cudaError_t launch_compress_fwd(const Prob &p, const float *pq, const float *pk,
     const int fixed = kCQ * 128 + kCJ * kCPitch;
     const int qb = rows_per_cta(p, fixed, 1);
     if (qb == 0) return cudaErrorInvalidValue;
-    const int smem = (fixed + qb * p.nKV) * 4;
+    const int smem = (fixed + qb * nkv_pitch(p)) * 4;
     const cudaError_t ae = ensure_smem_limit((const void *)k_compress_fwd, kCSmemCap);
     if (ae != cudaSuccess) return ae;
     dim3 grid((p.nQ + qb - 1) / qb, p.Hq, p.B);
@@ -397,7 +439,7 @@ cudaError_t launch_compress_bwd(const Prob &p, const void *dO, const void *gate,
     const int fixed = 2 * kCQ * 128 + 2 * kCJ * kCPitch;
     const int qb = rows_per_cta(p, fixed, 2);
     if (qb == 0) return cudaErrorInvalidValue;
-    const int smem = (fixed + 2 * qb * p.nKV) * 4;
+    const int smem = (fixed + 2 * qb * nkv_pitch(p)) * 4;
     if ((e = ensure_smem_limit((const void *)k_compress_rows, kCSmemCap)) != cudaSuccess) return e;
     dim3 gr((p.nQ + qb - 1) / qb, p.Hq, p.B);
     prof_begin("compress_rows", s);
