@@ -209,6 +209,33 @@ def test_scores_far_above_the_first_chunk(dtype):
     _bwd_check(p, t, plan, g, ref)
 
 
+def test_far_scores_on_some_tiles_of_several_redo_groups():
+    # 20 query tiles per head: the forward's recompute launch gives each CTA
+    # 16 consecutive tiles of a head, so this spans a full group and a
+    # partial one. Every third query tile has the common component that puts
+    # its scores on the last KV tile far above its first chunk's max (those
+    # tiles are recomputed), the rest do not; the recomputed tiles of a
+    # group are computed one after the other by one CTA. Outputs and
+    # gradients match the oracle.
+    p = Problem("far-scores-groups", "bshd", 1, 2, 2, 128, 256, 256, 20, 4, q_var=[256] * 20,
+                kv_var=[256, 256, 200, 256], topk=4, seed=82)
+    t = make_tensors(p)
+    T = t["q"].dtype
+    q = t["q"].float()
+    for i in range(0, p.nQ, 3):
+        q[:, i * 256:(i + 1) * 256] = q[:, i * 256:(i + 1) * 256] * 0.5 + 1.0
+    t["q"] = q.to(T)
+    k = t["k"].float()
+    k[:, 3 * 256:] = 6.0 + 0.5 * k[:, 3 * 256:]
+    t["k"] = k.to(T)
+    plan, g = run_map(p, t)
+    _, qi, qc, _ = orc.build_block_map(p, t["q"], t["k"], p.topk, p.cap)
+    assert np.all(qc == 4)
+    _fwd_check(p, t, plan, g, qi, qc)
+    ref = orc.run_full(p, t)
+    _bwd_check(p, t, plan, g, ref)
+
+
 @pytest.mark.parametrize("p", [config(2)] + [npu_problem(c) for c in load_golden("npu_tnd_cases.json")["cases"]],
                          ids=lambda p: p.name)
 def test_forward_parity_varlen_mask(p):
