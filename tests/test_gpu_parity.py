@@ -322,6 +322,12 @@ def gated_cases():
                 kv_var=[256, 173, 0, 79], topk=2, gate="randn01", seed=32),
         tnd_problem("gated-tnd-topk", [300, 17, 129], [540, 23, 200], 4, 2, dtype="fp16", topk=2,
                     gate="randn01", seed=33),
+        # the CTA-pair forward's gated epilogue: fp16 through the staged box
+        # stores, and varlen 256-token tiles through its per-thread stores
+        Problem("gated-fp16-bshd", "bshd", 1, 4, 2, 128, 256, 256, 4, 6, q_var=[256, 200, 256, 97],
+                kv_var=[256, 64, 160, 0, 256, 40], topk=3, gate="randn01", seed=34, dtype="fp16"),
+        tnd_problem("gated-tnd-256", [300, 517, 129], [540, 260, 700], 4, 2, dtype="bf16", tile=256, topk=2,
+                    gate="randn01", seed=35),
     ]
 
 
